@@ -1,0 +1,291 @@
+/*
+ * gemm_oracle.c -- the CPU oracle for the GEMM path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load or call this code.  The
+ * library (tiled_tensor_core_persistent_gb300) never does, and it shares no
+ * code, header, table or constant with it.
+ *
+ * What it computes (the plain definition, no blocking, fusion or reordering):
+ *
+ *   D_ref(i,j) = act( alpha * sA * sB * sum_{k=0}^{K-1} a(i,k) * b(k,j)
+ *                     + [beta != 0] * beta * c(i,j)
+ *                     + bias(j) )
+ *
+ *   - "CUTLASS" (stanleyjacob.dev), Part I, the one-GEMM identity
+ *     D = alpha * (A @ B) + beta * C with A M x K, B K x N, D M x N.
+ *   - same page, Part II (LinearCombination epilogue: alpha * acc + beta * C)
+ *     and Part VII Lab 4 (ReLU or GELU applied after alpha*AB + beta*C).
+ *   - same page, Part IV Stage 5 (bias add, GELU and a dequantisation scale
+ *     fused into the epilogue): the bias is added before the activation, and
+ *     the FP8 per-tensor scales sA, sB multiply the raw sum.
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *   - bias is indexed by the output column j and added before act;
+ *   - GELU is the exact erf form 0.5*x*(1+erf(x/sqrt(2)));
+ *   - ReLU is x > 0 ? x : 0;
+ *   - beta == 0 means C is not read at all (a NaN in C does not propagate).
+ *
+ * Arithmetic: every stored input is decoded to its exact value (bf16 and e4m3
+ * values are exact in double), the dot product is summed in double in
+ * increasing k, and the result is returned in double, unrounded.
+ *
+ * Operand storage (the "layout" of the logical M x K matrix A and K x N
+ * matrix B): ROW = row-major with leading dimension ld, COL = column-major.
+ * C is row-major M x N with leading dimension ldc.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { OR_ROW = 0, OR_COL = 1 };
+enum { OR_BF16 = 0, OR_E4M3 = 1, OR_F32 = 2 };
+enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_GELU = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* Exact decoders, written from the bit-level definitions of the formats.   */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+ * Normal: (-1)^s * 2^(e-127) * (1 + f/128); subnormal (e = 0):
+ * (-1)^s * 2^(-126) * (f/128); e = 255: infinity (f = 0) or NaN. */
+double oracle_decode_bf16(uint16_t bits) {
+    int s = (bits >> 15) & 1;
+    int e = (bits >> 7) & 0xFF;
+    int f = bits & 0x7F;
+    double v;
+    if (e == 0xFF) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f / 128.0, -126);
+    } else {
+        v = ldexp(1.0 + (double)f / 128.0, e - 127);
+    }
+    return s ? -v : v;
+}
+
+/* float8 e4m3 ("fn" variant from the FP8 formats paper cited on the CUTLASS
+ * page, Part XI item 11): 1 sign, 4 exponent bits (bias 7), 3 fraction bits,
+ * no infinities, NaN only for exponent 15 with fraction 7, largest finite
+ * value 448.  Subnormal (e = 0): (-1)^s * 2^(-6) * (f/8). */
+double oracle_decode_e4m3(uint8_t bits) {
+    int s = (bits >> 7) & 1;
+    int e = (bits >> 3) & 0xF;
+    int f = bits & 0x7;
+    double v;
+    if (e == 0xF && f == 0x7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f / 8.0, -6);
+    } else {
+        v = ldexp(1.0 + (double)f / 8.0, e - 7);
+    }
+    return s ? -v : v;
+}
+
+/* IEEE binary32, decoded through its bits for the same reason. */
+static double decode_f32(const void* p) {
+    float x;
+    memcpy(&x, p, sizeof x);
+    return (double)x;
+}
+
+static double g_bf16_table[65536];
+static double g_e4m3_table[256];
+static pthread_once_t g_tables_once = PTHREAD_ONCE_INIT;
+
+static void build_tables(void) {
+    for (int i = 0; i < 65536; ++i) g_bf16_table[i] = oracle_decode_bf16((uint16_t)i);
+    for (int i = 0; i < 256; ++i) g_e4m3_table[i] = oracle_decode_e4m3((uint8_t)i);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Activation functions.                                                     */
+/* ------------------------------------------------------------------------ */
+
+double oracle_act(int act, double x) {
+    switch (act) {
+    case OR_ACT_RELU:
+        return x > 0.0 ? x : 0.0;
+    case OR_ACT_GELU:
+        return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+    default:
+        return x;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* The problem description shared by the entry points.                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int M, N, K;
+    double alpha, beta, scale_a, scale_b;
+    const void* A; long long lda; int opA;
+    const void* B; long long ldb; int opB;
+    int ab_dtype;
+    const void* C; long long ldc; int c_dtype;
+    const void* bias; int bias_dtype;
+    int act;
+    /* optional instrumented operation counter (tiny problems only) */
+    int count_ops;
+} oracle_problem;
+
+static double load_ab(const void* base, int dtype, long long idx) {
+    if (dtype == OR_E4M3) return g_e4m3_table[((const uint8_t*)base)[idx]];
+    if (dtype == OR_F32) return decode_f32((const float*)base + idx);
+    return g_bf16_table[((const uint16_t*)base)[idx]];
+}
+
+static double load_vec(const void* base, int dtype, long long idx) {
+    if (dtype == OR_F32) return decode_f32((const float*)base + idx);
+    return g_bf16_table[((const uint16_t*)base)[idx]];
+}
+
+/* Element (i,k) of the logical A and element (k,j) of the logical B. */
+static long long a_index(const oracle_problem* p, int i, int k) {
+    return p->opA == OR_ROW ? (long long)i * p->lda + k : (long long)k * p->lda + i;
+}
+static long long b_index(const oracle_problem* p, int k, int j) {
+    return p->opB == OR_ROW ? (long long)k * p->ldb + j : (long long)j * p->ldb + k;
+}
+
+/* One output element, straight from the definition. */
+static double element(const oracle_problem* p, int i, int j, long long* n_mul, long long* n_add) {
+    double s = 0.0;
+    for (int k = 0; k < p->K; ++k) {
+        double a = load_ab(p->A, p->ab_dtype, a_index(p, i, k));
+        double b = load_ab(p->B, p->ab_dtype, b_index(p, k, j));
+        s = s + a * b;
+        if (p->count_ops) { ++*n_mul; ++*n_add; }
+    }
+    double d = p->alpha * p->scale_a * p->scale_b * s;
+    if (p->beta != 0.0) d += p->beta * load_vec(p->C, p->c_dtype, (long long)i * p->ldc + j);
+    if (p->bias) d += load_vec(p->bias, p->bias_dtype, j);
+    return oracle_act(p->act, d);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Threaded drivers over a list of (row, col) output positions.              */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const oracle_problem* p;
+    const int* rows; int nrows;   /* output positions: rows[r] x cols[c] */
+    const int* cols; int ncols;
+    double* out;                  /* nrows x ncols, row-major */
+    long long begin, end;         /* flattened range for this worker */
+    long long n_mul, n_add;
+} work_item;
+
+static void* worker(void* arg) {
+    work_item* w = (work_item*)arg;
+    for (long long t = w->begin; t < w->end; ++t) {
+        int r = (int)(t / w->ncols), c = (int)(t % w->ncols);
+        w->out[t] = element(w->p, w->rows[r], w->cols[c], &w->n_mul, &w->n_add);
+    }
+    return NULL;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static long long run_positions(const oracle_problem* p, const int* rows, int nrows,
+                               const int* cols, int ncols, double* out, int nthreads,
+                               long long* n_mul, long long* n_add) {
+    pthread_once(&g_tables_once, build_tables);
+    long long total = (long long)nrows * ncols;
+    if (total <= 0) return 0;
+    int nt = resolve_threads(nthreads);
+    if ((long long)nt > total) nt = (int)total;
+    work_item* items = (work_item*)calloc((size_t)nt, sizeof(work_item));
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    if (!items || !th) { free(items); free(th); return -1; }
+    for (int t = 0; t < nt; ++t) {
+        items[t].p = p;
+        items[t].rows = rows; items[t].nrows = nrows;
+        items[t].cols = cols; items[t].ncols = ncols;
+        items[t].out = out;
+        items[t].begin = total * t / nt;
+        items[t].end = total * (t + 1) / nt;
+    }
+    for (int t = 1; t < nt; ++t) pthread_create(&th[t], NULL, worker, &items[t]);
+    worker(&items[0]);
+    for (int t = 1; t < nt; ++t) pthread_join(th[t], NULL);
+    long long m = 0, a = 0;
+    for (int t = 0; t < nt; ++t) { m += items[t].n_mul; a += items[t].n_add; }
+    if (n_mul) *n_mul = m;
+    if (n_add) *n_add = a;
+    free(items); free(th);
+    return total;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exported entry points (called through ctypes from oracle/__init__.py).    */
+/* ------------------------------------------------------------------------ */
+
+#define PROBLEM_ARGS                                                          \
+    int M, int N, int K, double alpha, const void* A, long long lda, int opA, \
+    const void* B, long long ldb, int opB, int ab_dtype, double beta,          \
+    const void* C, long long ldc, int c_dtype, const void* bias,               \
+    int bias_dtype, int act, double scale_a, double scale_b
+
+static oracle_problem make_problem(PROBLEM_ARGS) {
+    oracle_problem p;
+    memset(&p, 0, sizeof p);
+    p.M = M; p.N = N; p.K = K;
+    p.alpha = alpha; p.beta = beta; p.scale_a = scale_a; p.scale_b = scale_b;
+    p.A = A; p.lda = lda; p.opA = opA;
+    p.B = B; p.ldb = ldb; p.opB = opB;
+    p.ab_dtype = ab_dtype;
+    p.C = C; p.ldc = ldc; p.c_dtype = c_dtype;
+    p.bias = bias; p.bias_dtype = bias_dtype;
+    p.act = act;
+    return p;
+}
+
+/* Selected rows x selected columns of D_ref, written to out (nrows x ncols).
+ * Returns the number of elements computed, or -1 on allocation failure. */
+long long oracle_gemm_select(PROBLEM_ARGS, const int* rows, int nrows,
+                             const int* cols, int ncols, double* out, int nthreads) {
+    oracle_problem p = make_problem(M, N, K, alpha, A, lda, opA, B, ldb, opB, ab_dtype,
+                                    beta, C, ldc, c_dtype, bias, bias_dtype, act,
+                                    scale_a, scale_b);
+    return run_positions(&p, rows, nrows, cols, ncols, out, nthreads, NULL, NULL);
+}
+
+/* The whole M x N result, row-major in out.  When count_ops is non-zero the
+ * scalar multiplies and adds of the dot products are counted one by one into
+ * *n_mul and *n_add (instrumentation for tiny problems). */
+long long oracle_gemm_full(PROBLEM_ARGS, double* out, int nthreads, int count_ops,
+                           long long* n_mul, long long* n_add) {
+    oracle_problem p = make_problem(M, N, K, alpha, A, lda, opA, B, ldb, opB, ab_dtype,
+                                    beta, C, ldc, c_dtype, bias, bias_dtype, act,
+                                    scale_a, scale_b);
+    p.count_ops = count_ops;
+    int* rows = (int*)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
+    int* cols = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    if (!rows || !cols) { free(rows); free(cols); return -1; }
+    for (int i = 0; i < M; ++i) rows[i] = i;
+    for (int j = 0; j < N; ++j) cols[j] = j;
+    long long r = run_positions(&p, rows, M, cols, N, out, nthreads, n_mul, n_add);
+    free(rows); free(cols);
+    return r;
+}
+
+/* Decoders over arrays, for the exhaustive pins. */
+void oracle_decode_bf16_array(const uint16_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_bf16(in[i]);
+}
+void oracle_decode_e4m3_array(const uint8_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e4m3(in[i]);
+}
+void oracle_act_array(int act, const double* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_act(act, in[i]);
+}

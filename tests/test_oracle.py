@@ -1,0 +1,290 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test ties the oracle to something other than its own formula: exact
+rational brute force, library routines on the decoded values (numpy matmul,
+torch's dtype conversions), closed forms (identity, permutation, rank-1),
+textbook constants (the normal CDF behind exact GELU) and invariants (layout
+transposition, per-tensor scale folding, the 2*M*N*K operation count).  A
+dropped term, a wrong sign or index, or a transposed operand in the oracle
+fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_tensor_core_persistent_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    return inputs.raw_bits(torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """Decode through torch (an implementation independent of the oracle's)."""
+    t = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def store(logical: np.ndarray, layout: str) -> tuple:
+    """Row-major or column-major storage of a logical matrix (ld = inner extent)."""
+    if layout == "row":
+        return np.ascontiguousarray(logical), logical.shape[1]
+    return np.ascontiguousarray(logical.T), logical.shape[0]
+
+
+def op(layout):
+    return oracle.ROW if layout == "row" else oracle.COL
+
+
+# ---------------------------------------------------------------- decoders
+
+def test_bf16_decoder_exhaustive_against_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.decode_bf16(bits)
+    ref = bf16_values(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e4m3_decoder_exhaustive_against_torch():
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ours = oracle.decode_e4m3(bits)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # 0x7F and 0xFF only
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.nanmax(ours) == 448.0 and np.nanmin(ours) == -448.0
+
+
+# ------------------------------------------------------ brute force (exact)
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (2, 3, 1), (3, 2, 4), (4, 4, 4), (7, 5, 3), (5, 7, 6)])
+@pytest.mark.parametrize("layouts", [("row", "col"), ("col", "row"), ("row", "row"), ("col", "col")])
+def test_tiny_shapes_exact_rational(M, N, K, layouts):
+    """Every element against exact rational arithmetic on torch-decoded values."""
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    a_bits = bf16_bits(rng.uniform(-2, 2, (M, K)))
+    b_bits = bf16_bits(rng.uniform(-2, 2, (K, N)))
+    c_bits = bf16_bits(rng.uniform(-2, 2, (M, N)))
+    bias_bits = bf16_bits(rng.uniform(-1, 1, (N,)))
+    a, b = bf16_values(a_bits), bf16_values(b_bits)
+    c, bias = bf16_values(c_bits), bf16_values(bias_bits)
+    alpha, beta = 0.75, -1.25  # exactly representable
+    As, lda = store(a_bits, layouts[0])
+    Bs, ldb = store(b_bits, layouts[1])
+    got = oracle.Problem(M, N, K, As, lda, op(layouts[0]), Bs, ldb, op(layouts[1]),
+                         alpha=alpha, beta=beta, C=c_bits, ldc=N, bias=bias_bits).full(1)
+    for i in range(M):
+        for j in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                s += Fraction(a[i, k]) * Fraction(b[k, j])
+            ref = Fraction(alpha) * s + Fraction(beta) * Fraction(c[i, j]) + Fraction(bias[j])
+            # K <= 6 products of bf16 values: the fp64 sum is exact here
+            assert got[i, j] == float(ref), (i, j)
+
+
+# ------------------------------------------------- library routine (numpy)
+
+@pytest.mark.parametrize("layouts", [("row", "col"), ("col", "row"), ("row", "row"), ("col", "col")])
+def test_integer_inputs_equal_numpy_matmul(layouts):
+    """Integer-valued bf16 inputs: every partial sum is exact, so the oracle
+    equals numpy's float64 matmul bit for bit in any summation order."""
+    M, N, K = 37, 29, 513
+    rng = np.random.default_rng(7)
+    a = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    b = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    As, lda = store(bf16_bits(a), layouts[0])
+    Bs, ldb = store(bf16_bits(b), layouts[1])
+    got = oracle.Problem(M, N, K, As, lda, op(layouts[0]), Bs, ldb, op(layouts[1])).full()
+    assert np.array_equal(got, a.astype(np.float64) @ b.astype(np.float64))
+
+
+def test_random_bf16_close_to_numpy_matmul():
+    M, N, K = 64, 48, 300
+    rng = np.random.default_rng(11)
+    a_bits = bf16_bits(rng.standard_normal((M, K)))
+    b_bits = bf16_bits(rng.standard_normal((K, N)))
+    got = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, np.ascontiguousarray(b_bits.T), K,
+                         oracle.COL).full()
+    ref = bf16_values(a_bits) @ bf16_values(b_bits)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_padded_leading_dimensions_ignore_padding():
+    """ld larger than the extent: padding (NaN) is never read."""
+    M, N, K = 9, 11, 13
+    rng = np.random.default_rng(3)
+    a = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    b = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    lda, ldb = 24, 16
+    As = np.full((M, lda), np.nan, np.float32); As[:, :K] = a
+    Bs = np.full((N, ldb), np.nan, np.float32); Bs[:, :K] = b.T
+    got = oracle.Problem(M, N, K, bf16_bits(As), lda, oracle.ROW, bf16_bits(Bs), ldb,
+                         oracle.COL).full()
+    assert np.array_equal(got, a.astype(np.float64) @ b.astype(np.float64))
+
+
+# ------------------------------------------------------------ closed forms
+
+def test_identity_and_permutation():
+    n, N = 16, 10
+    rng = np.random.default_rng(5)
+    b_bits = bf16_bits(rng.uniform(-8, 8, (n, N)))
+    b = bf16_values(b_bits)
+    eye = bf16_bits(np.eye(n))
+    got = oracle.Problem(n, N, n, eye, n, oracle.ROW, b_bits, N, oracle.ROW).full()
+    assert np.array_equal(got, b)
+    perm = rng.permutation(n)
+    P = np.zeros((n, n), np.float32)
+    P[np.arange(n), perm] = 1.0
+    got = oracle.Problem(n, N, n, bf16_bits(P), n, oracle.ROW, b_bits, N, oracle.ROW).full()
+    assert np.array_equal(got, b[perm])
+
+
+def test_rank_one_closed_form():
+    """(u v^T)(w x^T) = (v . w) u x^T, with small integers so all is exact."""
+    M, K, N = 12, 20, 9
+    rng = np.random.default_rng(9)
+    u = rng.integers(-3, 4, M).astype(np.float64)
+    v = rng.integers(-3, 4, K).astype(np.float64)
+    w = rng.integers(-3, 4, K).astype(np.float64)
+    x = rng.integers(-3, 4, N).astype(np.float64)
+    A = np.outer(u, v)
+    B = np.outer(w, x)
+    got = oracle.Problem(M, N, K, bf16_bits(A), K, oracle.ROW,
+                         bf16_bits(np.ascontiguousarray(B.T)), K, oracle.COL).full()
+    assert np.array_equal(got, float(v @ w) * np.outer(u, x))
+
+
+def test_operation_count_is_2mnk():
+    M, N, K = 5, 6, 7
+    a = bf16_bits(np.ones((M, K)))
+    b = bf16_bits(np.ones((N, K)))
+    out, n_mul, n_add = oracle.Problem(M, N, K, a, K, oracle.ROW, b, K, oracle.COL).count_ops()
+    assert n_mul + n_add == 2 * M * N * K
+    assert n_mul == M * N * K
+    assert np.all(out == K)
+
+
+# ------------------------------------------------------------- epilogue
+
+def _small_problem(act="none", alpha=1.0, beta=0.0, with_c=False, with_bias=False, c_nan=False):
+    M, N, K = 8, 12, 16
+    rng = np.random.default_rng(21)
+    a_bits = bf16_bits(rng.uniform(-1, 1, (M, K)))
+    b_bits = bf16_bits(rng.uniform(-1, 1, (N, K)))
+    c = rng.uniform(-1, 1, (M, N))
+    if c_nan:
+        c[:] = np.nan
+    c_bits = bf16_bits(c) if with_c else None
+    bias_bits = bf16_bits(rng.uniform(-1, 1, N)) if with_bias else None
+    p = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL, alpha=alpha,
+                       beta=beta, C=c_bits, ldc=N, bias=bias_bits, act=act)
+    ref_ab = bf16_values(a_bits) @ bf16_values(b_bits).T
+    return p, ref_ab, (bf16_values(c_bits) if with_c else None), \
+        (bf16_values(bias_bits) if with_bias else None)
+
+
+def test_alpha_zero_leaves_beta_c_plus_bias():
+    p, _, c, bias = _small_problem(alpha=0.0, beta=0.5, with_c=True, with_bias=True)
+    assert np.array_equal(p.full(), 0.5 * c + bias[None, :])
+
+
+def test_beta_zero_never_reads_c():
+    p, ref_ab, _, _ = _small_problem(beta=0.0, with_c=True, c_nan=True)
+    got = p.full()
+    assert not np.isnan(got).any()
+    np.testing.assert_allclose(got, ref_ab, rtol=1e-13, atol=1e-13)
+
+
+def test_relu_kills_negatives_and_keeps_positives():
+    p, ref_ab, _, bias = _small_problem(act="relu", with_bias=True)
+    pre = ref_ab + bias[None, :]
+    got = p.full()
+    assert (pre < 0).any() and (pre > 0).any()
+    assert np.all(got[pre < 0] == 0.0)
+    np.testing.assert_allclose(got[pre > 0], pre[pre > 0], rtol=1e-13, atol=1e-13)
+
+
+def test_gelu_textbook_values():
+    with open(os.path.join(GOLDEN, "normal_cdf.json")) as f:
+        pts = json.load(f)["points"]
+    x = np.array([p[0] for p in pts])
+    phi = np.array([p[1] for p in pts])
+    np.testing.assert_allclose(oracle.act("gelu", x), x * phi, rtol=1e-14, atol=1e-16)
+    assert oracle.act("gelu", np.array([0.0]))[0] == 0.0
+    big = oracle.act("gelu", np.array([12.0, -12.0]))
+    assert big[0] == 12.0 and abs(big[1]) < 1e-30
+
+
+def test_fused_activation_equals_separate_pass():
+    """The 'GEMM then activation' comparison the CUTLASS page's Lab 4 asks for."""
+    for act in ("relu", "gelu"):
+        p_fused, _, _, _ = _small_problem(act=act, with_bias=True, beta=0.5, with_c=True)
+        p_plain, _, _, _ = _small_problem(act="none", with_bias=True, beta=0.5, with_c=True)
+        np.testing.assert_array_equal(p_fused.full(), oracle.act(act, p_plain.full()))
+
+
+def test_scales_fold_into_alpha():
+    M, N, K = 6, 5, 32
+    rng = np.random.default_rng(4)
+    q_a = torch.from_numpy(rng.uniform(-400, 400, (M, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    q_b = torch.from_numpy(rng.uniform(-400, 400, (N, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    a_bits, b_bits = inputs.raw_bits(q_a), inputs.raw_bits(q_b)
+    base = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL).full()
+    ref = q_a.to(torch.float64).numpy() @ q_b.to(torch.float64).numpy().T
+    np.testing.assert_allclose(base, ref, rtol=1e-13)
+    scaled = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL,
+                            alpha=2.0, scale_a=0.25, scale_b=3.0).full()
+    np.testing.assert_allclose(scaled, 1.5 * base, rtol=1e-15)
+
+
+def test_select_matches_full():
+    case = inputs.make_case("sel", 40, 33, 70, seed=99, opA="col", opB="row", beta=0.5,
+                            bias_std=0.1, act="gelu")
+    p = oracle.Problem(case.M, case.N, case.K, inputs.raw_bits(case.A), case.lda, oracle.COL,
+                       inputs.raw_bits(case.B), case.ldb, oracle.ROW, alpha=case.alpha,
+                       beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
+                       bias=inputs.raw_bits(case.bias), act="gelu")
+    full = p.full()
+    rows, cols = np.array([0, 17, 39]), np.array([1, 32, 5])
+    assert np.array_equal(p.select(rows, cols), full[np.ix_(rows, cols)])
+
+
+def test_k_zero_is_epilogue_only():
+    M, N = 4, 6
+    rng = np.random.default_rng(8)
+    c_bits = bf16_bits(rng.uniform(-1, 1, (M, N)))
+    bias_bits = bf16_bits(rng.uniform(-1, 1, N))
+    a = np.zeros((M, 8), np.uint16)
+    b = np.zeros((N, 8), np.uint16)
+    got = oracle.Problem(M, N, 0, a, 8, oracle.ROW, b, 8, oracle.COL, beta=2.0, C=c_bits,
+                         ldc=N, bias=bias_bits, act="relu").full()
+    ref = np.maximum(2.0 * bf16_values(c_bits) + bf16_values(bias_bits)[None, :], 0.0)
+    assert np.array_equal(got, ref)
+
+
+def test_input_generator_recipes():
+    """The generators honour their recipes (values, padding, integer range)."""
+    c = inputs.square_512(integer=True)
+    vals = c.A.to(torch.float32)[:, :c.K]
+    assert torch.all(vals == vals.round()) and vals.abs().max() <= 4
+    r = inputs.make_case("pad", 5, 7, 9, seed=1, opA="row", opB="row")
+    assert r.lda == 16 and r.ldb == 8
+    assert torch.isnan(r.A.to(torch.float32)[:, 9:]).all()
+    f = inputs.make_case("f8", 8, 8, 32, seed=2, dist="normal", ab_dtype="e4m3")
+    assert f.A.dtype == torch.float8_e4m3fn
+    assert float(f.A.to(torch.float32)[:, :32].abs().max()) == 448.0

@@ -1,0 +1,178 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module holds no GEMM arithmetic: it only draws operands with the value
+distributions, shapes, storage orders and padded leading dimensions of the
+workloads, on the CPU with ``torch.Generator``.  Both the CUDA path (through
+the binding) and the oracle (through raw bits) consume exactly what it returns.
+
+Storage convention (same as the C ABI): the logical A is M x K and the logical
+B is K x N.  ``"row"`` stores a matrix row-major with leading dimension ld
+(element (r,c) at r*ld + c), ``"col"`` stores it column-major (element (r,c)
+at c*ld + r).  C and D are always row-major M x N.  Leading dimensions are
+padded up to a multiple of 16 bytes; the padding is filled with NaN (bf16) or
+the e4m3 NaN pattern so that a kernel reading it would be caught.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+_ELEM_BYTES = {"bf16": 2, "e4m3": 1, "f32": 4}
+_TORCH = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "f32": torch.float32}
+E4M3_MAX = 448.0
+
+
+def padded_ld(extent: int, dtype: str) -> int:
+    """Smallest leading dimension >= extent whose byte size is a multiple of 16."""
+    q = 16 // _ELEM_BYTES[dtype]
+    return max(q, (extent + q - 1) // q * q)
+
+
+def _store(logical: torch.Tensor, layout: str, dtype: str, ld: Optional[int] = None):
+    """Place a logical (rows x cols) fp32 matrix into padded storage of `dtype`."""
+    rows, cols = logical.shape
+    inner = cols if layout == "row" else rows
+    outer = rows if layout == "row" else cols
+    ld = padded_ld(inner, dtype) if ld is None else ld
+    buf = torch.full((max(outer, 1), ld), float("nan"), dtype=torch.float32)
+    if layout == "row":
+        buf[:rows, :cols] = logical
+    else:
+        buf[:cols, :rows] = logical.t()
+    return buf.to(_TORCH[dtype]), ld
+
+
+def raw_bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
+    """The raw storage bits of a CPU tensor as numpy (uint16 / uint8 / float32)."""
+    if t is None:
+        return None
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.contiguous().view(torch.uint8).numpy()
+    if t.dtype == torch.float32:
+        return t.contiguous().numpy()
+    raise TypeError(t.dtype)
+
+
+@dataclass
+class GemmCase:
+    name: str
+    M: int
+    N: int
+    K: int
+    opA: str
+    opB: str
+    ab_dtype: str
+    d_dtype: str
+    A: torch.Tensor          # storage (CPU)
+    lda: int
+    B: torch.Tensor          # storage (CPU)
+    ldb: int
+    alpha: float = 1.0
+    beta: float = 0.0
+    C: Optional[torch.Tensor] = None
+    ldc: int = 0
+    c_dtype: str = "bf16"
+    bias: Optional[torch.Tensor] = None
+    bias_dtype: str = "bf16"
+    act: str = "none"
+    scale_a: float = 1.0
+    scale_b: float = 1.0
+    ldd: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _draw(gen, shape, dist, K):
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "int4":
+        return torch.randint(-4, 5, shape, generator=gen, dtype=torch.int32).to(torch.float32)
+    if dist == "normal_sqrtk":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) / float(np.sqrt(max(K, 1)))
+    if dist == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32)
+    raise ValueError(dist)
+
+
+def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
+              ab_dtype="bf16", d_dtype="bf16", alpha=1.0, beta=0.0, c_dist=None,
+              c_dtype="bf16", bias_std=None, bias_dtype="bf16", act="none",
+              lda=None, ldb=None, ldc=None, ldd=None) -> GemmCase:
+    """Draw one GEMM problem.  Order of draws: A, B, C, bias (all from `seed`)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    a = _draw(gen, (M, K), dist, K)
+    b = _draw(gen, (K, N), dist, K)
+    scale_a = scale_b = 1.0
+    if ab_dtype == "e4m3":
+        # per-tensor scale amax/448, then the quantised codes (the harness does
+        # this, not the library): q = e4m3(clamp(x / scale, -448, 448)).
+        amax_a = float(a.abs().max()) if a.numel() else 1.0
+        amax_b = float(b.abs().max()) if b.numel() else 1.0
+        scale_a = (amax_a / E4M3_MAX) if amax_a > 0 else 1.0
+        scale_b = (amax_b / E4M3_MAX) if amax_b > 0 else 1.0
+        a = (a / scale_a).clamp(-E4M3_MAX, E4M3_MAX)
+        b = (b / scale_b).clamp(-E4M3_MAX, E4M3_MAX)
+    A, lda = _store(a, opA, ab_dtype, lda)
+    B, ldb = _store(b, opB, ab_dtype, ldb)
+    C = None
+    if beta != 0.0:
+        c = _draw(gen, (M, N), c_dist or dist, K)
+        C, ldc = _store(c, "row", c_dtype, ldc)
+    else:
+        ldc = 0
+    bias = None
+    if bias_std is not None:
+        bias = (torch.randn((N,), generator=gen, dtype=torch.float32) * bias_std).to(_TORCH[bias_dtype])
+    ldd = padded_ld(N, d_dtype) if ldd is None else ldd
+    return GemmCase(name=name, M=M, N=N, K=K, opA=opA, opB=opB, ab_dtype=ab_dtype,
+                    d_dtype=d_dtype, A=A, lda=lda, B=B, ldb=ldb, alpha=alpha, beta=beta,
+                    C=C, ldc=ldc, c_dtype=c_dtype, bias=bias, bias_dtype=bias_dtype,
+                    act=act, scale_a=scale_a, scale_b=scale_b, ldd=ldd,
+                    meta={"seed": seed, "dist": dist})
+
+
+# The workloads, with their sizes and value recipes.  Seeds are fixed per case.
+def square_512(integer: bool = False) -> GemmCase:
+    """512^3, A row / B col bf16, alpha=1 beta=0, fp32 D; U[-1,1] or integers in [-4,4]."""
+    if integer:
+        return make_case("gemm512_int", 512, 512, 512, seed=2, dist="int4", d_dtype="f32")
+    return make_case("gemm512_uniform", 512, 512, 512, seed=1, dist="uniform", d_dtype="f32")
+
+
+def square_4096_beta() -> GemmCase:
+    """4096^3 bf16, A,B ~ N(0,1)/sqrt(K), C ~ N(0,1), alpha=beta=1, bf16 D."""
+    return make_case("gemm4096_beta1", 4096, 4096, 4096, seed=3, dist="normal_sqrtk",
+                     alpha=1.0, beta=1.0, c_dist="normal")
+
+
+def square_8192_gelu() -> GemmCase:
+    """8192^3 bf16, A,B ~ N(0,1)/sqrt(K), D = GELU(AB + bias), bias ~ N(0,0.1), bf16 D."""
+    return make_case("gemm8192_bias_gelu", 8192, 8192, 8192, seed=4, dist="normal_sqrtk",
+                     bias_std=0.1, act="gelu")
+
+
+RAGGED_SHAPES = [(4095, 3001, 1537), (16, 8192, 8192), (8192, 128, 8192)]
+LAYOUT_COMBOS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col")]
+
+
+def ragged(shape_idx: int, combo_idx: int) -> GemmCase:
+    """Ragged/skinny bf16 shapes, U[-1,1], C U[-1,1], beta=0.5, each A/B layout combo."""
+    M, N, K = RAGGED_SHAPES[shape_idx]
+    opA, opB = LAYOUT_COMBOS[combo_idx]
+    seed = 5 + 4 * shape_idx + combo_idx
+    return make_case(f"ragged_{M}x{N}x{K}_{opA}{opB}", M, N, K, seed=seed, dist="uniform",
+                     opA=opA, opB=opB, alpha=1.0, beta=0.5, c_dist="uniform")
+
+
+def fp8_8192_relu() -> GemmCase:
+    """8192^3 e4m3 (N(0,1) quantised with amax/448 per tensor), bias N(0,0.1), ReLU, bf16 D."""
+    return make_case("gemm8192_e4m3_bias_relu", 8192, 8192, 8192, seed=17, dist="normal",
+                     ab_dtype="e4m3", bias_std=0.1, act="relu")
