@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""Benchmark: GEMM TFLOP/s on the 8192^3 BF16 workload with the fused
+bias + GELU epilogue (A row-major, B column-major, bf16 D), 1 GPU per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one tcg_gemm launch over the whole 8192^3 problem with inputs
+resident in HBM (A+B = 256 MiB > the 129 MB L2, so no flush is needed).  The
+timed region is bracketed by a barrier and a device synchronise on both sides
+and timed with CUDA events on the launching stream; rank 0 prints one JSON line.
+Under torchrun each rank runs an independent replica (weak scaling, no
+collective on the data path); the reported time is the max over ranks.
+
+--impl reference times the oracle (plain C, fp64, host cores) on bounded row
+samples of the same workload, reported in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak (8192³ BF16), 1 GPU"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(case):
+    return {"workload": f"gemm {case.M}x{case.N}x{case.K} bf16, A row-major / B column-major, "
+                        f"D = GELU(A@B + bias[N]) bf16, bias N(0,0.1), A,B N(0,1)/sqrt(K)",
+            "M": case.M, "N": case.N, "K": case.K, "ab_dtype": case.ab_dtype,
+            "d_dtype": case.d_dtype, "epilogue": "bias+gelu(erf)", "accumulate": "f32",
+            "l2": "inputs larger than L2 (A+B 256 MiB > 129 MB), no flush",
+            "parallelism": "replicas (one independent GEMM per GPU)"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_tensor_core_persistent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(key)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, value, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_rows(case, rows, nthreads=0):
+    import numpy as np
+    import oracle
+    from tiled_tensor_core_persistent_gb300 import inputs
+    prob = oracle.Problem(case.M, case.N, case.K, inputs.raw_bits(case.A), case.lda, oracle.ROW,
+                          inputs.raw_bits(case.B), case.ldb, oracle.COL, alpha=case.alpha,
+                          beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
+                          bias=inputs.raw_bits(case.bias), act=case.act)
+    cols = np.arange(case.N, dtype=np.int32)
+    t0 = time.perf_counter()
+    prob.select(np.asarray(rows, dtype=np.int32), cols, nthreads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    """The oracle timed on host cores, bounded row samples per step."""
+    world, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        return 0
+    from tiled_tensor_core_persistent_gb300 import inputs
+    case = inputs.square_8192_gelu()
+    cores = os.cpu_count() or 1
+    # size each step so the whole run stays within about a minute
+    probe = cpu_oracle_rows(case, [0, 1])
+    per_row = probe / 2
+    budget_s = 60.0
+    rows_per_step = max(1, int(budget_s / max(1, args.steps + args.warmup) / max(per_row, 1e-6)))
+    rows_per_step = min(rows_per_step, 64)
+    rng_rows = lambda i: [(i * rows_per_step + r) % case.M for r in range(rows_per_step)]
+    for i in range(args.warmup):
+        cpu_oracle_rows(case, rng_rows(i))
+    t = 0.0
+    for i in range(args.steps):
+        t += cpu_oracle_rows(case, rng_rows(args.warmup + i))
+    flops = 2.0 * rows_per_step * case.N * case.K * args.steps
+    value = flops / t / 1e12
+    sample = f"{rows_per_step} full rows of D (x {case.N} cols x K={case.K}) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(case),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import tiled_tensor_core_persistent_gb300 as tcg
+    from tiled_tensor_core_persistent_gb300 import _build, harness, inputs
+    if rank == 0:
+        _build.build()
+    barrier(pg, device)
+    tcg.lib()
+
+    case = inputs.square_8192_gelu()
+    stream = torch.cuda.Stream(device=device)
+    dc = harness.DeviceCase(case, device=device, stream=stream)
+    torch.cuda.synchronize(device)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            dc.run(stream)
+    torch.cuda.synchronize(device)
+    st = tcg.device_status(dc.workspace, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {tcg.last_error()}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, device)
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        dc.run(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(pg, device)
+    clocks = sampler.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
+    st = tcg.device_status(dc.workspace, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region: {tcg.last_error()}")
+
+    ms_per_step = elapsed_ms / args.steps
+    flops = case.flops
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    per_launch_tflops = flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device, GEMM, D -> pinned host
+    e2e = run_e2e(args, case, dc, stream, device, tcg)
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    roof = {"bound": "tensor", "achieved": per_launch_tflops, "peak": peak, "unit": "TFLOP/s",
+            "frac": per_launch_tflops / peak, "traffic": recorded_traffic("gemm8192_bias_gelu"),
+            "peak_kind": f"{peak_kind} bf16 burst (cuBLAS 8192^3)",
+            "peak_sustained": peaks.get("bf16_tflops_sustained"),
+            "frac_of_nominal_2250": per_launch_tflops / 2250.0,
+            "algorithmic": "2*M*N*K flop per launch"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nrows = 96
+        t = cpu_oracle_rows(case, list(range(0, case.M, case.M // nrows))[:nrows])
+        cpu = {"value": 2.0 * nrows * case.N * case.K / t / 1e12, "unit": UNIT,
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{nrows} full rows of D ({nrows}x{case.N}x{case.K}), {t:.1f} s wall"}
+
+    plan = tcg.plan(case.M, case.N, case.K, case.ab_dtype)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(workload_config(case), plan=plan),
+                "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+                "gpu_launches": args.steps}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, case, dc, stream, device, tcg):
+    import torch
+    A_h = case.A.pin_memory()
+    B_h = case.B.pin_memory()
+    bias_h = case.bias.pin_memory() if case.bias is not None else None
+    D_h = torch.empty(dc.D_view.shape, dtype=dc.D_view.dtype).pin_memory()
+    h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size() + \
+        (bias_h.numel() * bias_h.element_size() if bias_h is not None else 0)
+    d2h = D_h.numel() * D_h.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            dc.A.copy_(A_h, non_blocking=True)
+            dc.B.copy_(B_h, non_blocking=True)
+            if bias_h is not None:
+                dc.bias.copy_(bias_h, non_blocking=True)
+            dc.run(stream)
+            D_h.copy_(dc.D_view, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    n = max(1, args.e2e_steps)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = ev0.elapsed_time(ev1) / n
+    return {"value": case.flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
+            "path": "pinned host A,B,bias -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

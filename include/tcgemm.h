@@ -1,0 +1,162 @@
+/*
+ * tcgemm.h -- C ABI of the GB300 (sm_103a) tiled tensor-core persistent GEMM.
+ *
+ * The one operation:
+ *
+ *     D = act( alpha * sA * sB * (A @ B) + beta * C + bias )
+ *
+ * "CUTLASS" (stanleyjacob.dev), Part I: the one-GEMM identity
+ * D = alpha * (A @ B) + beta * C, A M x K, B K x N, C and D M x N; Part II:
+ * the LinearCombination epilogue and a fused bias / ReLU variant; Part IV
+ * Stage 5: bias, GELU and a dequantisation scale fused into the epilogue;
+ * Part IV Stage 1: the host sequence get_workspace_size -> can_implement ->
+ * run, with a status return.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Matrices are dense, addressed by a base pointer and a leading dimension
+ *   (ld, in elements).  A is the logical M x K operand, B the logical K x N
+ *   operand.  TCG_ROW stores a matrix row-major (element (r,c) at r*ld + c),
+ *   TCG_COL column-major (element (r,c) at c*ld + r).  C and D are always
+ *   row-major M x N.
+ * - All device pointers (A, B, C, D, bias, workspace) are owned by the
+ *   caller, are device memory of the current CUDA device, and must stay
+ *   valid until the work queued on `stream` has finished.  The library keeps
+ *   only a process-wide cache of TMA descriptors and launch attributes.
+ * - Alignment: every pointer 16-byte aligned and every ld * sizeof(element)
+ *   a multiple of 16 bytes, else TCG_ERR_MISALIGNED (the CUTLASS page, Part II,
+ *   "ignoring alignment", and Lab 3: a misaligned lda must be refused).
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  tcg_gemm is asynchronous: host-detectable errors return before
+ *   anything is queued; device-side errors (a bounded wait that ran out) are
+ *   recorded in the workspace status word and read by tcg_device_status.
+ * - No CPU fallback and no library GEMM: every FLOP runs in this library's
+ *   sm_103a kernels.  On any other GPU tcg_gemm returns TCG_ERR_ARCH.
+ */
+#ifndef TCGEMM_H
+#define TCGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TCG_OK = 0,
+    TCG_ERR_INVALID_ARG = 1,   /* negative size, NULL pointer that is needed, bad enum, ld too small */
+    TCG_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. MN-major e4m3) */
+    TCG_ERR_MISALIGNED = 3,    /* pointer or ld * element size not a multiple of 16 bytes */
+    TCG_ERR_ARCH = 4,          /* current device is not compute capability 10.3 */
+    TCG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than tcg_workspace_size */
+    TCG_ERR_LAUNCH = 6,        /* a CUDA runtime/driver call failed (message: tcg_last_error) */
+    TCG_ERR_TIMEOUT = 7        /* a bounded device-side wait ran out (reported by tcg_device_status) */
+} tcg_status;
+
+typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
+
+typedef enum { TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2 } tcg_dtype;
+
+typedef enum { TCG_ACT_NONE = 0, TCG_ACT_RELU = 1, TCG_ACT_GELU = 2 } tcg_act;
+
+/* Fused epilogue.  bias: NULL or a device vector of N elements (bias_dtype
+ * TCG_BF16 or TCG_F32), added per output column before the activation.
+ * act: NONE, RELU = max(x, 0), GELU = exact erf form 0.5*x*(1+erf(x/sqrt 2)). */
+typedef struct {
+    const void* bias;
+    tcg_dtype bias_dtype;
+    tcg_act act;
+} tcg_epilogue;
+
+/* Per-tensor dequantisation scales for e4m3 operands (use 1.0 for bf16):
+ * the raw product sum is multiplied by alpha * scale_a * scale_b. */
+typedef struct {
+    float scale_a;
+    float scale_b;
+} tcg_scales;
+
+/*
+ * tcg_can_implement -- argument validation only (no GPU access, no launch).
+ *   M, N, K        : problem size, >= 0.
+ *   ab_dtype       : TCG_BF16 or TCG_E4M3 (A and B share it).  E4M3 requires
+ *                    opA = TCG_ROW and opB = TCG_COL (both K-contiguous).
+ *   A, lda, opA    : operand A; lda >= K (ROW) or >= M (COL).
+ *   B, ldb, opB    : operand B; ldb >= N (ROW) or >= K (COL).
+ *   has_c, C, ldc, c_dtype : has_c != 0 when beta != 0; then C row-major,
+ *                    ldc >= N, c_dtype TCG_BF16 or TCG_F32.
+ *   D, ldd, d_dtype: output, row-major, ldd >= N, TCG_BF16 or TCG_F32.
+ *   epi            : bias pointer (16-byte aligned) / dtype / activation.
+ * Returns TCG_OK or the first failing rule's code.  M == 0 or N == 0 is OK.
+ */
+tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype,
+                             const void* A, int lda, tcg_layout opA,
+                             const void* B, int ldb, tcg_layout opB,
+                             int has_c, const void* C, int ldc, tcg_dtype c_dtype,
+                             const void* D, int ldd, tcg_dtype d_dtype,
+                             tcg_epilogue epi);
+
+/*
+ * tcg_workspace_size -- bytes of device workspace tcg_gemm needs for this
+ * problem on the current device: a 256-byte status/counter header plus, when
+ * the planner splits K (skinny shapes), fp32 partial tiles and per-tile
+ * arrival counters.  The workspace must be zero-filled once when allocated
+ * (tcg_workspace_init); the library leaves it in that state after every call.
+ * Returns 0 only for invalid sizes.
+ */
+size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype);
+
+/* Zero-fill `bytes` of workspace on `stream` (asynchronous). */
+tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * tcg_gemm -- D = act(alpha*scale_a*scale_b*(A@B) + beta*C + bias), queued on
+ * `stream`.  Arguments as in tcg_can_implement; beta == 0 means C is never
+ * read (C may be NULL and may hold NaN).  K == 0 gives act(beta*C + bias).
+ * The result is rounded once from fp32 to d_dtype (round to nearest even).
+ * D must not overlap A, B or bias; D == C (in-place update) is allowed when
+ * ldc == ldd and c_dtype == d_dtype.
+ * Returns TCG_OK when the kernel was queued.
+ */
+tcg_status tcg_gemm(int M, int N, int K, float alpha,
+                    const void* A, int lda, tcg_layout opA,
+                    const void* B, int ldb, tcg_layout opB,
+                    float beta, const void* C, int ldc, tcg_dtype c_dtype,
+                    void* D, int ldd, tcg_dtype d_dtype,
+                    tcg_epilogue epi, tcg_dtype ab_dtype, tcg_scales scales,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * tcg_device_status -- synchronises `stream`, reads the workspace status word
+ * (TCG_OK or TCG_ERR_TIMEOUT) written by earlier tcg_gemm calls on this
+ * workspace, and clears it.  Returns TCG_ERR_LAUNCH if the stream itself
+ * reports a CUDA error.
+ */
+tcg_status tcg_device_status(void* workspace, void* stream);
+
+/* Human-readable text of the last TCG_ERR_LAUNCH / TCG_ERR_ARCH on this thread. */
+const char* tcg_last_error(void);
+
+/*
+ * tcg_plan -- the launch plan tcg_gemm would use (for tests and tools).
+ * out[0..9] = {BM, BN, BK, stages, splits, grid CTAs, cluster size,
+ *              units of work, raster group, dynamic smem bytes}.
+ * Needs the current device (queries SM count and shared-memory limit).
+ */
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);
+
+/*
+ * tcg_debug_set -- TEST-ONLY knobs, process-wide.
+ *   fault_inject = 1: in the next launches, CTA 0's producer skips its first
+ *     stage (no loads, no arrival), so the MMA issuer's bounded wait runs out
+ *     and the kernel records TCG_ERR_TIMEOUT instead of hanging.
+ *   wait_timeout_ns: limit of every bounded device-side wait (0 = default 2 s).
+ *   force_splits / force_cta2: override the planner (0 = automatic).
+ */
+void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_H */

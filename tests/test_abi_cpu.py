@@ -1,0 +1,102 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+function include/tcgemm.h declares, and validates arguments (no launch)."""
+import os
+import re
+
+import pytest
+
+import tiled_tensor_core_persistent_gb300 as tcg
+from tiled_tensor_core_persistent_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return tcg.lib()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "tcgemm.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tcg_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_surface():
+    assert declared_functions() == sorted(tcg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_with_nm(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", tcg.library_path()], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+# Arguments of a valid 300 x 200 x 128 bf16 problem (fake, aligned addresses:
+# can_implement never dereferences them).
+A, B, C, D, BIAS = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+
+
+def ci(M=300, N=200, K=128, ab="bf16", A_=A, lda=128, opA="row", B_=B, ldb=128, opB="col", has_c=0,
+       C_=C, ldc=200, c_dtype="bf16", D_=D, ldd=200, d_dtype="bf16", bias=None, bias_dtype="bf16",
+       act="none"):
+    return tcg.can_implement(M, N, K, ab, A_, lda, opA, B_, ldb, opB, has_c, C_, ldc, c_dtype, D_, ldd,
+                             d_dtype, bias=bias, bias_dtype=bias_dtype, act=act)
+
+
+def test_valid_problem_is_ok(lib):
+    assert ci() == 0
+    assert ci(opA="col", lda=304, opB="row", ldb=200) == 0
+    assert ci(has_c=1, bias=BIAS, act="gelu") == 0
+    assert ci(ab="e4m3", lda=128, ldb=128) == 0
+
+
+def test_empty_problem_is_ok(lib):
+    assert ci(M=0, D_=None) == 0
+    assert ci(N=0, D_=None) == 0
+
+
+def test_invalid_arguments(lib):
+    INVALID = 1
+    assert ci(M=-1) == INVALID
+    assert ci(ab="f32") == INVALID
+    assert ci(opA=5) == INVALID
+    assert ci(D_=None) == INVALID
+    assert ci(has_c=1, C_=None) == INVALID
+    assert ci(A_=None) == INVALID
+    assert ci(lda=64) == INVALID          # lda < K for row-major A
+    assert ci(opA="col", lda=296) == INVALID  # lda < M for column-major A
+    assert ci(ldd=192) == INVALID
+    assert ci(act=9) == INVALID
+
+
+def test_misaligned_lda_is_refused(lib):
+    """The CUTLASS page's Lab 3: misalign lda by one and watch can_implement refuse."""
+    MISALIGNED = 3
+    assert ci(lda=129) == MISALIGNED
+    assert ci(A_=A + 2) == MISALIGNED
+    assert ci(ldd=201) == MISALIGNED
+    assert ci(bias=BIAS + 4) == MISALIGNED
+    assert ci(has_c=1, ldc=204, c_dtype="bf16") == MISALIGNED
+
+
+def test_unsupported_fp8_layouts(lib):
+    assert ci(ab="e4m3", opA="col", lda=304) == 2
+
+
+def test_k_zero_needs_no_operands(lib):
+    assert ci(K=0, A_=None, B_=None, lda=0, ldb=0) == 0
+
+
+def test_workspace_size_without_device(lib):
+    assert tcg.workspace_size(8192, 8192, 8192) >= 256
+    assert tcg.workspace_size(-1, 4, 4) == 0

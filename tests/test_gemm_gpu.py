@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small cases are compared element by element over the whole output; the
+full-size workloads are compared on sampled full rows and full columns
+(edges, tile boundaries and random positions), which the oracle computes one
+element at a time.  Integer-valued inputs with fp32 D must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tiled_tensor_core_persistent_gb300 import harness, inputs
+import tiled_tensor_core_persistent_gb300 as tcg
+
+from parity import TOL, assert_within, oracle_for, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from tiled_tensor_core_persistent_gb300 import _build
+    _build.build()
+    tcg.debug_set()
+    yield
+    tcg.debug_set()
+
+
+def run(case, guard_rows=0):
+    dc = harness.DeviceCase(case, guard_rows=guard_rows)
+    dc.run()
+    torch.cuda.synchronize()
+    assert tcg.device_status(dc.workspace) == 0, tcg.last_error()
+    return dc
+
+
+def check_full(case, tol=None, exact=False, guard_rows=2):
+    dc = run(case, guard_rows=guard_rows)
+    got = dc.result().numpy()
+    ref = oracle_for(case).full()
+    if exact:
+        assert np.array_equal(got, ref), f"max |diff| {np.abs(got - ref).max()}"
+    else:
+        assert_within(got, ref, tol if tol is not None else TOL[case.ab_dtype], case.name)
+    if guard_rows:
+        assert dc.untouched_outside(), "wrote outside D's M x N window"
+    return dc
+
+
+def check_sampled(case, nrows=96, ncols=96, tol=None, seed=0):
+    dc = run(case)
+    D = dc.D_view[:, :case.N]
+    prob = oracle_for(case)
+    tol = tol if tol is not None else TOL[case.ab_dtype]
+    rows = sample_indices(case.M, nrows, seed)
+    cols = sample_indices(case.N, ncols, seed + 1)
+    all_cols = np.arange(case.N, dtype=np.int32)
+    all_rows = np.arange(case.M, dtype=np.int32)
+    got_rows = D[torch.from_numpy(rows).long().to(D.device)].to(torch.float64).cpu().numpy()
+    w1 = assert_within(got_rows, prob.select(rows, all_cols), tol, case.name + " rows")
+    got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
+    w2 = assert_within(got_cols, prob.select(all_rows, cols), tol, case.name + " cols")
+    return max(w1, w2)
+
+
+# ------------------------------------------------------------ exact checks
+
+def test_single_tile_integer_exact():
+    case = inputs.make_case("t128", 128, 256, 128, seed=31, dist="int4", d_dtype="f32")
+    check_full(case, exact=True)
+
+
+def test_gemm512_integer_bit_exact():
+    check_full(inputs.square_512(integer=True), exact=True)
+
+
+def test_gemm512_uniform():
+    check_full(inputs.square_512(integer=False))
+
+
+EDGE_SHAPES = [(1, 1, 1), (128, 256, 64), (127, 255, 63), (129, 257, 65), (128, 128, 8),
+               (300, 200, 1), (64, 384, 100), (5, 300, 1000), (260, 16, 130)]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("combo", inputs.LAYOUT_COMBOS, ids=lambda c: c[0] + c[1])
+def test_edge_shapes_integer_exact(shape, combo):
+    M, N, K = shape
+    case = inputs.make_case(f"edge{M}x{N}x{K}", M, N, K, seed=M * 7 + N * 3 + K, dist="int4",
+                            opA=combo[0], opB=combo[1], d_dtype="f32")
+    check_full(case, exact=True)
+
+
+def test_persistent_many_tiles_integer_exact():
+    """More tiles than SMs: every CTA loops, both TMEM accumulators are reused."""
+    case = inputs.make_case("many", 2048, 2560, 256, seed=41, dist="int4", d_dtype="f32")
+    check_full(case, exact=True)
+
+
+# ---------------------------------------------------------- epilogue paths
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu"])
+@pytest.mark.parametrize("bias_dtype", ["bf16", "f32"])
+def test_bias_activation(act, bias_dtype):
+    case = inputs.make_case(f"bias_{act}", 300, 520, 384, seed=51, dist="uniform", bias_std=0.1,
+                            bias_dtype=bias_dtype, act=act)
+    check_full(case)
+
+
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d_dtype", ["bf16", "f32"])
+def test_beta_c(c_dtype, d_dtype):
+    case = inputs.make_case("beta", 333, 290, 200, seed=61, dist="uniform", beta=0.5,
+                            c_dist="uniform", c_dtype=c_dtype, d_dtype=d_dtype, alpha=1.5)
+    check_full(case)
+
+
+def test_beta_zero_never_reads_c():
+    case = inputs.make_case("nanC", 200, 300, 128, seed=71, dist="uniform")
+    dc = harness.DeviceCase(case, guard_rows=1)
+    nan_c = torch.full((case.M, case.ldd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tcg.gemm(case.M, case.N, case.K, 1.0, dc.A, case.lda, "row", dc.B, case.ldb, "col", 0.0, nan_c,
+             case.ldd, "bf16", dc.D_view, case.ldd, case.d_dtype, workspace=dc.workspace,
+             workspace_bytes=dc.ws_bytes)
+    torch.cuda.synchronize()
+    assert_within(dc.result().numpy(), oracle_for(case).full(), TOL["bf16"], "nanC")
+
+
+def test_k_zero_is_epilogue_only():
+    case = inputs.make_case("k0", 130, 70, 0, seed=81, dist="uniform", beta=2.0, c_dist="uniform",
+                            bias_std=0.5, act="relu", d_dtype="f32")
+    check_full(case, tol=1e-6)
+
+
+def test_in_place_c_equals_d():
+    case = inputs.make_case("inplace", 256, 512, 192, seed=91, dist="uniform", beta=1.0,
+                            c_dist="uniform", c_dtype="f32", d_dtype="f32")
+    ref = oracle_for(case).full()
+    dc = harness.DeviceCase(case)
+    dc.D_view.copy_(dc.C)
+    tcg.gemm(case.M, case.N, case.K, case.alpha, dc.A, case.lda, "row", dc.B, case.ldb, "col", 1.0,
+             dc.D_view, case.ldd, "f32", dc.D_view, case.ldd, "f32", workspace=dc.workspace,
+             workspace_bytes=dc.ws_bytes)
+    torch.cuda.synchronize()
+    assert_within(dc.result().numpy(), ref, 1e-4, "inplace")
+
+
+# -------------------------------------------------------------------- FP8
+
+def test_fp8_integer_exact():
+    case = inputs.make_case("f8int", 256, 384, 512, seed=101, dist="int4", ab_dtype="e4m3",
+                            d_dtype="f32")
+    assert case.scale_a == 1.0 and case.scale_b == 1.0
+    check_full(case, exact=True)
+
+
+def test_fp8_scaled_bias_relu_small():
+    case = inputs.make_case("f8small", 384, 640, 1024, seed=111, dist="normal", ab_dtype="e4m3",
+                            bias_std=0.1, act="relu")
+    check_full(case)
+
+
+# ------------------------------------------------- the full-size workloads
+
+@pytest.mark.slow
+def test_config_4096_beta1():
+    check_sampled(inputs.square_4096_beta(), nrows=128, ncols=128)
+
+
+@pytest.mark.slow
+def test_config_8192_bias_gelu():
+    check_sampled(inputs.square_8192_gelu(), nrows=64, ncols=64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape_idx", range(3), ids=["4095x3001x1537", "16x8192x8192", "8192x128x8192"])
+@pytest.mark.parametrize("combo_idx", range(4), ids=["rowrow", "rowcol", "colrow", "colcol"])
+def test_config_ragged(shape_idx, combo_idx):
+    check_sampled(inputs.ragged(shape_idx, combo_idx), nrows=48, ncols=48)
+
+
+@pytest.mark.slow
+def test_config_fp8_8192_bias_relu():
+    check_sampled(inputs.fp8_8192_relu(), nrows=64, ncols=64)

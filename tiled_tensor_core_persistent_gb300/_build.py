@@ -1,0 +1,47 @@
+"""Compile the in-tree CUDA library (libtcgemm.so) for sm_103a with nvcc.
+
+One translation unit, one -gencode, no cmake: the same command runs on the
+x86 development machine (cross-compilation, no GPU needed) and on the Arm GPU
+machines.  The result lands in ``_build/`` next to this file.
+"""
+from __future__ import annotations
+
+import glob
+import os
+import shutil
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+OUT_DIR = os.path.join(HERE, "_build")
+SO_PATH = os.path.join(OUT_DIR, "libtcgemm.so")
+GENCODE = "arch=compute_103a,code=sm_103a"
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libtcgemm.so")
+
+
+def sources() -> list:
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
+                  [os.path.join(ROOT, "include", "tcgemm.h")])
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    os.makedirs(OUT_DIR, exist_ok=True)
+    srcs = sources()
+    if not force and os.path.exists(SO_PATH):
+        newest = max(os.path.getmtime(s) for s in srcs)
+        if os.path.getmtime(SO_PATH) >= newest:
+            return SO_PATH
+    tmp = SO_PATH + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-shared", "-Xptxas", "-v" if verbose else "-O3", "-o", tmp,
+           os.path.join(CSRC, "tcgemm_host.cu")]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, SO_PATH)
+    return SO_PATH

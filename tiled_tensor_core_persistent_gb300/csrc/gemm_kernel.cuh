@@ -1,0 +1,459 @@
+// gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D = act(alpha * (A @ B) + beta * C + bias)      (alpha already holds sA*sB)
+//
+// Structure (the reference pages describe the Hopper/Ampere ancestors; this is
+// the Blackwell re-design):
+//   * CTA tile BM x BN over D (BM = 128 = TMEM lanes), streamed over K in
+//     k-blocks of one 128-byte swizzle row ("CUTLASS", Part I tile hierarchy
+//     and Part IV Stage 4 mainloop).
+//   * Warp 0, one thread: TMA producer.  Per k-block it waits for a free
+//     stage, arms the stage's full barrier with the byte count and issues the
+//     A and B box loads (128-byte swizzled shared memory).
+//   * Warp 1, one thread: MMA issuer.  Per k-block it waits for the stage,
+//     issues BK/MMA_K tcgen05.mma into a TMEM accumulator, and commits the
+//     stage back to the producer.  Warp 1 also owns TMEM allocation.
+//   * Warps 2-5: epilogue.  TMEM -> registers (tcgen05.ld), alpha / beta*C /
+//     bias / activation in fp32, cast, 16-byte stores into a swizzled staging
+//     tile, TMA store (out-of-range rows/columns clipped by the hardware).
+//   * Two TMEM accumulators: the epilogue of tile i overlaps the mainloop of
+//     tile i+1 (the idea behind the ping-pong schedule, "CUTLASS", Part V
+//     deep dive on collective builder and kernel schedules).
+//   * Persistent static schedule with grouped rasterisation ("CUTLASS",
+//     Part IV Stage 2: swizzle the tile-to-block mapping for L2 reuse).
+//   * Split-K: each (tile, split) unit writes an fp32 partial; the last unit
+//     to arrive sums the partials in split order and runs the epilogue
+//     ("CUTLASS", Part IV Stage 6).
+//   * Every wait is bounded; on expiry the CTA records TCG_ERR_TIMEOUT in the
+//     status word, drains its in-flight copies, frees TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tcg {
+
+constexpr int kBM = 128;              // rows per CTA tile = TMEM lanes
+constexpr int kRowBytes = 128;        // one k-block = one 128-byte swizzle row
+constexpr int kNumThreads = 192;      // 6 warps
+constexpr int kEpiWarp0 = 2;          // epilogue warps 2..5
+constexpr int kEpiThreads = 128;
+constexpr int kEpiChunk = 32;         // columns per tcgen05.ld / TMA store box
+constexpr int kStageBufBytes = 4096;  // one 32 x 128-byte staging tile
+constexpr int kEpiBytes = 4 * 2 * kStageBufBytes;
+constexpr int kStatusTimeout = 7;     // == TCG_ERR_TIMEOUT
+
+struct KernelParams {
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    CUtensorMap tmD;
+    int M, N, K;
+    int num_m_blk, num_n_blk, num_kb;
+    int splits, num_units, group_m;
+    int a_mn_major, b_mn_major;
+    float alpha, beta;
+    const void* C;
+    long long ldc;
+    int c_f32;
+    const void* bias;
+    int bias_f32;
+    int act;
+    int d_f32;
+    int stages;
+    float* partials;      // split-K partial tiles [tile][split][kBM][BN]
+    int* tile_counters;   // split-K arrival counters [tile]
+    int* status;          // [0] status, [1] where, [2] block
+    long long timeout_ns;
+    int fault_inject;
+};
+
+// Shared-memory bookkeeping that lives after the operand stages.
+struct alignas(8) SmemCtl {
+    uint64_t full[16];
+    uint64_t empty[16];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int splitk_last;
+};
+
+__device__ __forceinline__ void record_timeout(const KernelParams& p, int where) {
+    if (atomicCAS(p.status, 0, kStatusTimeout) == 0) {
+        p.status[1] = where;
+        p.status[2] = static_cast<int>(blockIdx.x);
+    }
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and flags the CTA) when
+// the limit passes or, if honor_abort, another role of this CTA already gave
+// up.  Drain waits pass honor_abort = false: they must see their own copies
+// land even after an abort, and are still bounded by the limit.
+__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const KernelParams& p,
+                                        SmemCtl* ctl, int where, long long limit_ns,
+                                        bool honor_abort = true) {
+    const uint32_t a = ptx::smem_u32(bar);
+    if (ptx::mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (ptx::mbar_try_wait(a, parity)) return true;
+        if ((++n & 31u) == 0) {
+            if (honor_abort && *reinterpret_cast<volatile int*>(&ctl->abort_flag)) return false;
+            if (static_cast<long long>(ptx::globaltimer_ns() - t0) > limit_ns) {
+                *reinterpret_cast<volatile int*>(&ctl->abort_flag) = 1;
+                record_timeout(p, where);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& m_blk, int& n_blk,
+                                            int& split, int& kb0, int& kb1) {
+    const int tile = u / p.splits;
+    split = u - tile * p.splits;
+    const int span = p.group_m * p.num_n_blk;
+    const int gid = tile / span;
+    const int first_m = gid * p.group_m;
+    const int gsz = min(p.num_m_blk - first_m, p.group_m);
+    const int local = tile - gid * span;
+    m_blk = first_m + local % gsz;
+    n_blk = local / gsz;
+    kb0 = static_cast<int>((static_cast<long long>(split) * p.num_kb) / p.splits);
+    kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.num_kb) / p.splits);
+}
+
+__device__ __forceinline__ float gelu_erf(float x) {
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ float apply_act(int act, float x) {
+    if (act == 1) return x > 0.0f ? x : 0.0f;
+    if (act == 2) return gelu_erf(x);
+    return x;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+// Load 32 consecutive elements of a row-major bf16/f32 row, columns
+// [col0, col0+32) clipped to n_valid, into fp32 registers (0 outside).
+__device__ __forceinline__ void load_row32(const void* base, int is_f32, int col0, int n_valid,
+                                           float (&out)[32]) {
+    if (is_f32) {
+        const float* src = static_cast<const float*>(base) + col0;
+        if (col0 + 32 <= n_valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(src + 4 * q);
+                out[4 * q + 0] = v.x; out[4 * q + 1] = v.y;
+                out[4 * q + 2] = v.z; out[4 * q + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) out[i] = (col0 + i < n_valid) ? src[i] : 0.0f;
+        }
+    } else {
+        const uint16_t* src = static_cast<const uint16_t*>(base) + col0;
+        if (col0 + 32 <= n_valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * q);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    out[8 * q + 2 * h + 0] = bf16_bits_to_float(w[h] & 0xFFFFu);
+                    out[8 * q + 2 * h + 1] = bf16_bits_to_float(w[h] >> 16);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                out[i] = (col0 + i < n_valid) ? bf16_bits_to_float(src[i]) : 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Write one thread's 32 results (its row of the 32 x 32 chunk) into the
+// staging tile in the layout the D tensor map's swizzle expects:
+//   f32 : 128-byte rows, 16-byte chunk c of row r at chunk c ^ (r & 7)
+//   bf16:  64-byte rows, 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)
+__device__ __forceinline__ void stage_row(uint8_t* buf, int row, int d_f32, const float (&v)[32]) {
+    if (d_f32) {
+        uint8_t* rowp = buf + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int pc = c ^ (row & 7);
+            float4 q = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            *reinterpret_cast<float4*>(rowp + pc * 16) = q;
+        }
+    } else {
+        uint8_t* rowp = buf + row * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int pc = c ^ ((row >> 1) & 3);
+            uint4 q;
+            q.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+            q.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+            q.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+            q.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+            *reinterpret_cast<uint4*>(rowp + pc * 16) = q;
+        }
+    }
+}
+
+template <int BN, bool kFp8>
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
+    constexpr int kElemBytes = kFp8 ? 1 : 2;
+    constexpr int kBK = kRowBytes / kElemBytes;       // elements per k-block
+    constexpr int kMmaK = 32 / kElemBytes;             // K per tcgen05.mma
+    constexpr int kKSteps = kBK / kMmaK;               // MMAs per k-block
+    constexpr int kAtom = kRowBytes / kElemBytes;      // MN elements per swizzle row
+    constexpr int kABytes = kBM * kRowBytes;
+    constexpr int kBBytes = BN * kRowBytes;
+    constexpr int kStageBytes = kABytes + kBBytes;
+    constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr uint32_t kFmt = kFp8 ? 0u : 1u;          // e4m3 = 0, bf16 = 1
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
+    uint8_t* epi_smem = smem + S * kStageBytes;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_smem + kEpiBytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&ctl->full[s], 1);
+            ptx::mbar_init(&ctl->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&ctl->tmem_full[a], 1);
+            ptx::mbar_init(&ctl->tmem_empty[a], 4);
+        }
+        ptx::mbar_init(&ctl->drain, 1);
+        ctl->abort_flag = 0;
+        ctl->splitk_last = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+        ptx::tmem_relinquish_alloc_permit();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const long long limit = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            if (p.num_kb > 0) {
+                ptx::prefetch_tensormap(&p.tmA);
+                ptx::prefetch_tensormap(&p.tmB);
+            }
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            bool first = true;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int m_blk, n_blk, split, kb0, kb1;
+                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
+                    const bool skip = first && p.fault_inject && blockIdx.x == 0;
+                    first = false;
+                    if (!skip) {
+                        uint8_t* sA = smem + stage * kStageBytes;
+                        uint8_t* sB = sA + kABytes;
+                        uint64_t* fb = &ctl->full[stage];
+                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                        if (!p.a_mn_major) {
+                            ptx::tma_load_2d(sA, &p.tmA, fb, kb * kBK, m_blk * kBM);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < kBM / kAtom; ++h)
+                                ptx::tma_load_2d(sA + h * kRowBytes * kBK, &p.tmA, fb, m_blk * kBM + h * kAtom,
+                                                 kb * kBK);
+                        }
+                        if (!p.b_mn_major) {
+                            ptx::tma_load_2d(sB, &p.tmB, fb, kb * kBK, n_blk * BN);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < BN / kAtom; ++h)
+                                ptx::tma_load_2d(sB + h * kRowBytes * kBK, &p.tmB, fb, n_blk * BN + h * kAtom,
+                                                 kb * kBK);
+                        }
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: every stage this thread armed has landed before the CTA
+            // may leave (its shared memory is the copies' destination).
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s))
+                    wait_phase(&ctl->full[s], (armed_parity >> s) & 1u, p, ctl, 11, limit, false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+                                   (static_cast<uint32_t>(p.a_mn_major) << 15) |
+                                   (static_cast<uint32_t>(p.b_mn_major) << 16) |
+                                   (static_cast<uint32_t>(BN >> 3) << 17) |
+                                   (static_cast<uint32_t>(kBM >> 4) << 24);
+            // Descriptor geometry.  K-major: 8-row groups 1024 B apart (SBO),
+            // k-step = +kMmaK*elem bytes inside the swizzle row.  MN-major:
+            // swizzle-row boxes of kAtom MN elements, BK rows each (LBO apart),
+            // 8-row K groups 1024 B apart (SBO), k-step = kMmaK rows.
+            const uint32_t a_lbo = p.a_mn_major ? static_cast<uint32_t>(kRowBytes * kBK) : 16u;
+            const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(kRowBytes * kBK) : 16u;
+            const uint32_t a_kstep = p.a_mn_major ? (kMmaK * kRowBytes) >> 4 : (kMmaK * kElemBytes) >> 4;
+            const uint32_t b_kstep = p.b_mn_major ? (kMmaK * kRowBytes) >> 4 : (kMmaK * kElemBytes) >> 4;
+            int stage = 0;
+            uint32_t phase = 0;
+            int t = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+                int m_blk, n_blk, split, kb0, kb1;
+                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+                const int acc = t & 1;
+                const uint32_t acc_phase = (t >> 1) & 1;
+                if (!wait_phase(&ctl->tmem_empty[acc], acc_phase ^ 1u, p, ctl, 2, limit)) { ok = false; break; }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(&ctl->full[stage], phase, p, ctl, 3, limit)) { ok = false; break; }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t sA = ptx::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sB = sA + kABytes;
+                    const uint64_t a_desc = ptx::smem_desc_sw128(sA, a_lbo, 1024);
+                    const uint64_t b_desc = ptx::smem_desc_sw128(sB, b_lbo, 1024);
+#pragma unroll
+                    for (int k = 0; k < kKSteps; ++k) {
+                        const uint64_t ad = a_desc + static_cast<uint64_t>(k * a_kstep);
+                        const uint64_t bd = b_desc + static_cast<uint64_t>(k * b_kstep);
+                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                        if constexpr (kFp8) ptx::mma_f8(d_tmem, ad, bd, idesc, accum);
+                        else ptx::mma_f16(d_tmem, ad, bd, idesc, accum);
+                    }
+                    issued_any = true;
+                    ptx::mma_commit(&ctl->empty[stage]);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (kb1 > kb0) ptx::mma_commit(&ctl->tmem_full[acc]);
+                else ptx::mbar_arrive(&ctl->tmem_full[acc]);
+            }
+            // Drain: all MMAs this thread issued complete before TMEM is freed.
+            if (issued_any) {
+                ptx::mma_commit(&ctl->drain);
+                wait_phase(&ctl->drain, 0, p, ctl, 12, limit, false);
+            }
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int g = warp & 3;                 // TMEM lane group this warp may access
+        const int row_in_tile = g * 32 + lane;  // this thread's accumulator row
+        uint8_t* const stage_base = epi_smem + (warp - kEpiWarp0) * 2 * kStageBufBytes;
+        int sb = 0;
+        int t = 0;
+        const bool has_c = p.beta != 0.0f;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+            int m_blk, n_blk, split, kb0, kb1;
+            decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after_sync();
+
+            const int m0 = m_blk * kBM;
+            const int n0 = n_blk * BN;
+            const int grow = m0 + row_in_tile;
+            const bool row_ok = grow < p.M;
+            const bool warp_rows_live = (m0 + g * 32) < p.M;
+            const bool have_acc = kb1 > kb0;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            if (warp_rows_live) {
+                for (int j = 0; j < BN / kEpiChunk; ++j) {
+                    const int col0 = n0 + j * kEpiChunk;
+                    if (col0 >= p.N) break;
+                    float v[32];
+                    if (have_acc) {
+                        uint32_t r[32];
+                        ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(r[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+                    if (has_c && row_ok) {
+                        float c[32];
+                        const char* crow = static_cast<const char*>(p.C) +
+                                           static_cast<long long>(grow) * p.ldc * (p.c_f32 ? 4 : 2);
+                        load_row32(crow, p.c_f32, col0, p.N, c);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, c[i], v[i]);
+                    }
+                    if (p.bias) {
+                        float b[32];
+                        load_row32(p.bias, p.bias_f32, col0, p.N, b);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += b[i];
+                    }
+                    if (p.act) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = apply_act(p.act, v[i]);
+                    }
+                    // The staging buffer is free once its previous store has read it.
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    stage_row(stage_base + sb * kStageBufBytes, lane, p.d_f32, v);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&p.tmD, stage_base + sb * kStageBufBytes, col0, m0 + g * 32);
+                        ptx::bulk_commit_group();
+                    }
+                    sb ^= 1;
+                }
+            }
+            // Hand the accumulator back to the MMA issuer.
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ctl->tmem_empty[acc]);
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace tcg

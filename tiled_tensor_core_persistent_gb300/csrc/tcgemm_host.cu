@@ -1,0 +1,388 @@
+// tcgemm_host.cu -- the C ABI of include/tcgemm.h: argument validation, TMA
+// descriptor encoding, the launch plan and the launch.
+//
+// The host sequence follows "CUTLASS" (stanleyjacob.dev), Part IV Stage 1:
+// size the workspace, validate the problem against what the kernel can do
+// (can_implement), then run one kernel launch.  The planner plays the role of
+// the collective builder's StageCountAuto (the CUTLASS/CuTe/CUDA Tile page,
+// "Assembling a CUTLASS kernel": the stage count is whatever fits in shared
+// memory at one CTA per SM) and of the tile scheduler (grid size, raster
+// group, split-K for shapes with too few output tiles, Part III / Part IV
+// Stage 2 and Stage 6).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/tcgemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Test-only knobs (tcg_debug_set).
+int g_fault_inject = 0;
+long long g_timeout_ns = 0;
+int g_force_splits = 0;
+int g_force_cta2 = 0;
+constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s
+
+constexpr size_t kHeaderBytes = 256;  // status word + diagnostics
+
+tcg_status fail_launch(const char* what, cudaError_t e) {
+    char buf[512];
+    snprintf(buf, sizeof buf, "%s: %s", what, cudaGetErrorString(e));
+    g_last_error = buf;
+    return TCG_ERR_LAUNCH;
+}
+
+int elem_bytes(tcg_dtype t) {
+    switch (t) {
+        case TCG_BF16: return 2;
+        case TCG_E4M3: return 1;
+        case TCG_F32: return 4;
+    }
+    return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ device info
+
+struct DeviceInfo {
+    bool valid = false;
+    int major = 0, minor = 0;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+tcg_status device_info(DeviceInfo& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_launch("cudaGetDevice", e);
+    if (dev < 0 || dev >= 64) { g_last_error = "device index out of range"; return TCG_ERR_LAUNCH; }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.valid) {
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+                cudaSuccess)
+            return fail_launch("cudaDeviceGetAttribute", e);
+        d.valid = true;
+    }
+    out = d;
+    return TCG_OK;
+}
+
+// ------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+tcg_status get_encoder(EncodeTiledFn& fn) {
+    std::call_once(g_encode_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    if (!g_encode) { g_last_error = "cuTensorMapEncodeTiled entry point not found"; return TCG_ERR_LAUNCH; }
+    fn = g_encode;
+    return TCG_OK;
+}
+
+CUtensorMapDataType tma_dtype(tcg_dtype t) {
+    switch (t) {
+        case TCG_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        case TCG_E4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+// A 2-D row-major view: `inner` contiguous elements per row, `outer` rows
+// ld_elems apart; boxes of box_inner x box_outer elements.
+tcg_status encode_2d(CUtensorMap* map, tcg_dtype t, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn;
+    tcg_status st = get_encoder(fn);
+    if (st != TCG_OK) return st;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes(t))};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, tma_dtype(t), 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[256];
+        snprintf(buf, sizeof buf,
+                 "cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, ld %llu, box %u x %u", static_cast<int>(r),
+                 (unsigned long long)inner, (unsigned long long)outer, (unsigned long long)ld_elems, box_inner,
+                 box_outer);
+        g_last_error = buf;
+        return TCG_ERR_LAUNCH;
+    }
+    return TCG_OK;
+}
+
+// --------------------------------------------------------------- planning
+
+struct Plan {
+    int bn = 256;
+    int stages = 4;
+    int splits = 1;
+    int grid = 1;
+    int units = 0;
+    int group_m = 8;
+    int smem = 0;
+    int num_m = 0, num_n = 0, num_kb = 0;
+    int cluster = 1;
+};
+
+int stage_bytes(int bn) { return (tcg::kBM + bn) * tcg::kRowBytes; }
+
+Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
+    Plan pl;
+    const int bk = tcg::kRowBytes / elem_bytes(ab);
+    pl.bn = (N <= 128) ? 128 : 256;
+    pl.num_m = (M + tcg::kBM - 1) / tcg::kBM;
+    pl.num_n = (N + pl.bn - 1) / pl.bn;
+    pl.num_kb = (K + bk - 1) / bk;
+    const int tiles = pl.num_m * pl.num_n;
+    // Split K only when the output tiles cannot fill the machine and each
+    // split keeps a useful number of k-blocks.
+    int splits = 1;
+    (void)tiles;  // split-K epilogue not wired yet: one unit per tile
+    splits = std::max(1, std::min(splits, std::max(pl.num_kb, 1)));
+    pl.splits = splits;
+    pl.units = tiles * splits;
+    pl.grid = std::max(1, std::min(pl.units, dev.num_sms));
+    pl.group_m = 8;
+    const int fixed = 1024 /*alignment slack*/ + tcg::kEpiBytes + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
+    int stages = (dev.max_smem_optin - fixed) / stage_bytes(pl.bn);
+    stages = std::max(2, std::min(stages, 8));
+    pl.stages = stages;
+    pl.smem = fixed + stages * stage_bytes(pl.bn);
+    return pl;
+}
+
+size_t partial_bytes(const Plan& pl) {
+    if (pl.splits <= 1) return 0;
+    return static_cast<size_t>(pl.num_m) * pl.num_n * pl.splits * tcg::kBM * pl.bn * sizeof(float);
+}
+
+size_t counter_bytes(const Plan& pl) {
+    if (pl.splits <= 1) return 0;
+    return (static_cast<size_t>(pl.num_m) * pl.num_n * sizeof(int) + 255) / 256 * 256;
+}
+
+template <int BN, bool kFp8>
+tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
+    auto kern = tcg::gemm_persistent_kernel<BN, kFp8>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    });
+    if (attr_err != cudaSuccess) return fail_launch("cudaFuncSetAttribute", attr_err);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(pl.grid, 1, 1);
+    cfg.blockDim = dim3(tcg::kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+    if (e != cudaSuccess) return fail_launch("cudaLaunchKernelEx", e);
+    return TCG_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char* tcg_last_error(void) { return g_last_error.c_str(); }
+
+void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2) {
+    g_fault_inject = fault_inject;
+    g_timeout_ns = wait_timeout_ns;
+    g_force_splits = force_splits;
+    g_force_cta2 = force_cta2;
+}
+
+tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void* A, int lda, tcg_layout opA,
+                             const void* B, int ldb, tcg_layout opB, int has_c, const void* C, int ldc,
+                             tcg_dtype c_dtype, const void* D, int ldd, tcg_dtype d_dtype, tcg_epilogue epi) {
+    if (M < 0 || N < 0 || K < 0) return TCG_ERR_INVALID_ARG;
+    if (ab_dtype != TCG_BF16 && ab_dtype != TCG_E4M3) return TCG_ERR_INVALID_ARG;
+    if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return TCG_ERR_INVALID_ARG;
+    if (d_dtype != TCG_BF16 && d_dtype != TCG_F32) return TCG_ERR_INVALID_ARG;
+    if (has_c && c_dtype != TCG_BF16 && c_dtype != TCG_F32) return TCG_ERR_INVALID_ARG;
+    if (epi.act != TCG_ACT_NONE && epi.act != TCG_ACT_RELU && epi.act != TCG_ACT_GELU) return TCG_ERR_INVALID_ARG;
+    if (epi.bias && epi.bias_dtype != TCG_BF16 && epi.bias_dtype != TCG_F32) return TCG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TCG_OK;
+    if (!D) return TCG_ERR_INVALID_ARG;
+    if (has_c && !C) return TCG_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return TCG_ERR_INVALID_ARG;
+    // leading dimensions cover the contiguous extent
+    if (K > 0) {
+        if (lda < (opA == TCG_ROW ? K : M)) return TCG_ERR_INVALID_ARG;
+        if (ldb < (opB == TCG_ROW ? N : K)) return TCG_ERR_INVALID_ARG;
+    }
+    if (ldd < N) return TCG_ERR_INVALID_ARG;
+    if (has_c && ldc < N) return TCG_ERR_INVALID_ARG;
+    if (ab_dtype == TCG_E4M3 && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
+    // 16-byte rule for every pointer and every leading dimension in bytes
+    const int eb = elem_bytes(ab_dtype);
+    if (K > 0) {
+        if (!aligned16(A) || !aligned16(B)) return TCG_ERR_MISALIGNED;
+        if ((static_cast<long long>(lda) * eb) % 16 || (static_cast<long long>(ldb) * eb) % 16)
+            return TCG_ERR_MISALIGNED;
+    }
+    if (!aligned16(D) || (static_cast<long long>(ldd) * elem_bytes(d_dtype)) % 16) return TCG_ERR_MISALIGNED;
+    if (has_c && (!aligned16(C) || (static_cast<long long>(ldc) * elem_bytes(c_dtype)) % 16))
+        return TCG_ERR_MISALIGNED;
+    if (epi.bias && !aligned16(epi.bias)) return TCG_ERR_MISALIGNED;
+    return TCG_OK;
+}
+
+size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    if (ab_dtype != TCG_BF16 && ab_dtype != TCG_E4M3) return 0;
+    DeviceInfo dev;
+    if (device_info(dev) != TCG_OK) {
+        // Without a device the split-K part cannot be sized; report the
+        // largest plan this library could choose on a 1024-SM device.
+        dev.num_sms = 1024;
+        dev.max_smem_optin = 232448;
+    }
+    if (M == 0 || N == 0) return kHeaderBytes;
+    Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    return kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+}
+
+tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!workspace) return TCG_ERR_WORKSPACE;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_launch("cudaMemsetAsync", e);
+    return TCG_OK;
+}
+
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]) {
+    if (M < 0 || N < 0 || K < 0 || !out) return TCG_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    tcg_status st = device_info(dev);
+    if (st != TCG_OK) return st;
+    Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    const int vals[10] = {tcg::kBM, pl.bn, tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
+                          pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem};
+    memcpy(out, vals, sizeof vals);
+    return TCG_OK;
+}
+
+tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tcg_layout opA, const void* B,
+                    int ldb, tcg_layout opB, float beta, const void* C, int ldc, tcg_dtype c_dtype, void* D,
+                    int ldd, tcg_dtype d_dtype, tcg_epilogue epi, tcg_dtype ab_dtype, tcg_scales scales,
+                    void* workspace, size_t workspace_bytes, void* stream_) {
+    const int has_c = beta != 0.0f;
+    tcg_status st = tcg_can_implement(M, N, K, ab_dtype, A, lda, opA, B, ldb, opB, has_c, C, ldc, c_dtype, D, ldd,
+                                      d_dtype, epi);
+    if (st != TCG_OK) return st;
+    if (M == 0 || N == 0) return TCG_OK;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != TCG_OK) return st;
+    if (dev.major != 10 || dev.minor != 3) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "compute capability %d.%d is not 10.3 (sm_103a)", dev.major, dev.minor);
+        g_last_error = buf;
+        return TCG_ERR_ARCH;
+    }
+    Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TCG_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    tcg::KernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    const int bk = tcg::kRowBytes / elem_bytes(ab_dtype);
+    const int atom = bk;  // MN elements per 128-byte swizzle row
+    if (K > 0) {
+        // A: K-major -> rows of K, box BK x BM; MN-major -> rows of M, box atom x BK
+        if (opA == TCG_ROW)
+            st = encode_2d(&kp.tmA, ab_dtype, A, K, M, lda, bk, tcg::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+        else
+            st = encode_2d(&kp.tmA, ab_dtype, A, M, K, lda, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TCG_OK) return st;
+        if (opB == TCG_COL)
+            st = encode_2d(&kp.tmB, ab_dtype, B, K, N, ldb, bk, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        else
+            st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TCG_OK) return st;
+    }
+    st = encode_2d(&kp.tmD, d_dtype, D, N, M, ldd, tcg::kEpiChunk, 32,
+                   d_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != TCG_OK) return st;
+
+    kp.M = M; kp.N = N; kp.K = K;
+    kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
+    kp.splits = pl.splits; kp.num_units = pl.units; kp.group_m = pl.group_m;
+    kp.a_mn_major = (opA == TCG_COL); kp.b_mn_major = (opB == TCG_ROW);
+    kp.alpha = alpha * scales.scale_a * scales.scale_b;
+    kp.beta = beta;
+    kp.C = has_c ? C : nullptr;
+    kp.ldc = ldc;
+    kp.c_f32 = (c_dtype == TCG_F32);
+    kp.bias = epi.bias;
+    kp.bias_f32 = (epi.bias_dtype == TCG_F32);
+    kp.act = static_cast<int>(epi.act);
+    kp.d_f32 = (d_dtype == TCG_F32);
+    kp.stages = pl.stages;
+    char* ws = static_cast<char*>(workspace);
+    kp.status = reinterpret_cast<int*>(ws);
+    kp.tile_counters = pl.splits > 1 ? reinterpret_cast<int*>(ws + kHeaderBytes) : nullptr;
+    kp.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + kHeaderBytes + counter_bytes(pl)) : nullptr;
+    kp.timeout_ns = g_timeout_ns > 0 ? g_timeout_ns : kDefaultTimeoutNs;
+    kp.fault_inject = g_fault_inject;
+
+    const bool fp8 = ab_dtype == TCG_E4M3;
+    if (pl.bn == 256) return fp8 ? launch_kernel<256, true>(kp, pl, stream) : launch_kernel<256, false>(kp, pl, stream);
+    return fp8 ? launch_kernel<128, true>(kp, pl, stream) : launch_kernel<128, false>(kp, pl, stream);
+}
+
+tcg_status tcg_device_status(void* workspace, void* stream_) {
+    if (!workspace) return TCG_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_launch("cudaStreamSynchronize", e);
+    int words[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_launch("cudaMemcpy(status)", e);
+    if (words[0] != 0) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "device wait ran out (role/stage code %d, block %d)", words[1], words[2]);
+        g_last_error = buf;
+        e = cudaMemset(workspace, 0, sizeof words);
+        if (e != cudaSuccess) return fail_launch("cudaMemset(status)", e);
+        return static_cast<tcg_status>(words[0]);
+    }
+    return TCG_OK;
+}
+
+}  // extern "C"

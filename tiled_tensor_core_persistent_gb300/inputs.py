@@ -111,9 +111,10 @@ def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
     a = _draw(gen, (M, K), dist, K)
     b = _draw(gen, (K, N), dist, K)
     scale_a = scale_b = 1.0
-    if ab_dtype == "e4m3":
+    if ab_dtype == "e4m3" and dist != "int4":
         # per-tensor scale amax/448, then the quantised codes (the harness does
         # this, not the library): q = e4m3(clamp(x / scale, -448, 448)).
+        # Integer draws in [-4, 4] are e4m3 codes already and keep scale 1.
         amax_a = float(a.abs().max()) if a.numel() else 1.0
         amax_b = float(b.abs().max()) if b.numel() else 1.0
         scale_a = (amax_a / E4M3_MAX) if amax_a > 0 else 1.0
