@@ -184,3 +184,37 @@ def test_config_ragged(shape_idx, combo_idx):
 @pytest.mark.slow
 def test_config_fp8_8192_bias_relu():
     check_sampled(inputs.fp8_8192_relu(), nrows=64, ncols=64)
+
+
+# ----------------------------------------------------------------- split-K
+
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_forced_split_k_integer_exact(splits):
+    try:
+        tcg.debug_set(force_splits=splits)
+        case = inputs.make_case(f"split{splits}", 300, 520, 1100, seed=121 + splits, dist="int4",
+                                d_dtype="f32", opA="col", opB="row")
+        assert tcg.plan(case.M, case.N, case.K)["splits"] == splits
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()
+
+
+def test_forced_split_k_epilogue_and_determinism():
+    try:
+        tcg.debug_set(force_splits=4)
+        case = inputs.make_case("split_epi", 250, 300, 2048, seed=131, dist="uniform", beta=0.5,
+                                c_dist="uniform", bias_std=0.1, act="gelu")
+        dc = check_full(case)
+        first = dc.D_view.clone()
+        for _ in range(3):
+            dc.run()
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), dc.D_view.view(torch.int16)), "split-K not deterministic"
+    finally:
+        tcg.debug_set()
+
+
+def test_skinny_shapes_plan_split_k():
+    for (M, N, K) in [(16, 8192, 8192), (8192, 128, 8192)]:
+        assert tcg.plan(M, N, K)["splits"] > 1

@@ -61,6 +61,9 @@ struct KernelParams {
     int bias_f32;
     int act;
     int d_f32;
+    void* D;              // row-major output, for the ragged column tail
+    long long ldd;
+    int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
     int stages;
     float* partials;      // split-K partial tiles [tile][split][kBM][BN]
     int* tile_counters;   // split-K arrival counters [tile]
@@ -113,8 +116,8 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const Ke
 }
 
 __device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& m_blk, int& n_blk,
-                                            int& split, int& kb0, int& kb1) {
-    const int tile = u / p.splits;
+                                            int& split, int& kb0, int& kb1, int& tile) {
+    tile = u / p.splits;
     split = u - tile * p.splits;
     const int span = p.group_m * p.num_n_blk;
     const int gid = tile / span;
@@ -212,6 +215,21 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int row, int d_f32, cons
     }
 }
 
+// Element-wise guarded store of one thread's 32 results (columns >= N skipped).
+__device__ __forceinline__ void store_row_tail(const KernelParams& p, int row, int col0, const float (&v)[32]) {
+    if (p.d_f32) {
+        float* dst = static_cast<float*>(p.D) + static_cast<long long>(row) * p.ldd + col0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) dst[i] = v[i];
+    } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.D) + static_cast<long long>(row) * p.ldd + col0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) dst[i] = __float2bfloat16_rn(v[i]);
+    }
+}
+
 template <int BN, bool kFp8>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
@@ -271,8 +289,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool first = true;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                int m_blk, n_blk, split, kb0, kb1;
-                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+                int m_blk, n_blk, split, kb0, kb1, tile;
+                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
                     const bool skip = first && p.fault_inject && blockIdx.x == 0;
@@ -332,8 +350,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool ok = true;
             bool issued_any = false;
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
-                int m_blk, n_blk, split, kb0, kb1;
-                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+                int m_blk, n_blk, split, kb0, kb1, tile;
+                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
                 const int acc = t & 1;
                 const uint32_t acc_phase = (t >> 1) & 1;
                 if (!wait_phase(&ctl->tmem_empty[acc], acc_phase ^ 1u, p, ctl, 2, limit)) { ok = false; break; }
@@ -376,13 +394,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         int sb = 0;
         int t = 0;
         const bool has_c = p.beta != 0.0f;
+        const bool split_mode = p.splits > 1;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
-            int m_blk, n_blk, split, kb0, kb1;
-            decode_unit(p, u, m_blk, n_blk, split, kb0, kb1);
+            int m_blk, n_blk, split, kb0, kb1, tile;
+            decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
             bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
-            ok = __all_sync(0xffffffffu, ok);
+            // All four epilogue warps take the same branch (the split-K named
+            // barriers below must be reached by all 128 threads or by none).
+            ok = ptx::named_barrier_and(1, kEpiThreads, ok);
             if (!ok) break;
             ptx::tc_fence_after_sync();
 
@@ -394,16 +415,79 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const bool have_acc = kb1 > kb0;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if (warp_rows_live) {
+
+            bool finish = true;
+            if (split_mode) {
+                // Pass 1: this split's raw fp32 partial (valid rows only).
+                float* slot = p.partials +
+                              (static_cast<size_t>(tile) * p.splits + split) * (kBM * BN) +
+                              static_cast<size_t>(row_in_tile) * BN;
+                if (warp_rows_live && have_acc) {
+                    for (int j = 0; j < BN / kEpiChunk; ++j) {
+                        if (n0 + j * kEpiChunk >= p.N) break;
+                        uint32_t r[32];
+                        ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
+                        if (row_ok) {
+                            float4* dst = reinterpret_cast<float4*>(slot + j * kEpiChunk);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        }
+                    }
+                }
+                // Arrive on the tile; the last of its splits finishes it.
+                __threadfence();
+                ptx::named_barrier_sync(1, kEpiThreads);
+                if (threadIdx.x == kEpiWarp0 * 32) {
+                    const int old = atomicAdd(p.tile_counters + tile, 1);
+                    const int last = (old == p.splits - 1) ? 1 : 0;
+                    if (last) atomicExch(p.tile_counters + tile, 0);  // ready for the next launch
+                    ctl->splitk_last = last;
+                }
+                ptx::named_barrier_sync(1, kEpiThreads);
+                finish = ctl->splitk_last != 0;
+                __threadfence();
+            }
+
+            if (finish && warp_rows_live) {
                 for (int j = 0; j < BN / kEpiChunk; ++j) {
                     const int col0 = n0 + j * kEpiChunk;
                     if (col0 >= p.N) break;
                     float v[32];
-                    if (have_acc) {
+                    if (have_acc || split_mode) {
+                        float s[32];
                         uint32_t r[32];
-                        ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
+                        if (have_acc) ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
+                        if (!split_mode) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(r[i]);
+                            for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+                        } else {
+                            // Fixed order over the splits: the sum does not
+                            // depend on which split arrived last.
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) s[i] = 0.0f;
+                            for (int q = 0; q < p.splits; ++q) {
+                                if (q == split) {
+                                    if (have_acc) {
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) s[i] += __uint_as_float(r[i]);
+                                    }
+                                } else if (row_ok) {
+                                    const float4* src = reinterpret_cast<const float4*>(
+                                        p.partials + (static_cast<size_t>(tile) * p.splits + q) * (kBM * BN) +
+                                        static_cast<size_t>(row_in_tile) * BN + j * kEpiChunk);
+#pragma unroll
+                                    for (int c4 = 0; c4 < 8; ++c4) {
+                                        const float4 w = __ldcg(src + c4);
+                                        s[4 * c4 + 0] += w.x; s[4 * c4 + 1] += w.y;
+                                        s[4 * c4 + 2] += w.z; s[4 * c4 + 3] += w.w;
+                                    }
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = p.alpha * s[i];
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
@@ -426,17 +510,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = apply_act(p.act, v[i]);
                     }
-                    // The staging buffer is free once its previous store has read it.
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();
-                    __syncwarp();
-                    stage_row(stage_base + sb * kStageBufBytes, lane, p.d_f32, v);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&p.tmD, stage_base + sb * kStageBufBytes, col0, m0 + g * 32);
-                        ptx::bulk_commit_group();
+                    if (col0 + kEpiChunk <= p.N || p.d_inner_aligned) {
+                        // The staging buffer is free once its previous store has read it.
+                        if (lane == 0) ptx::bulk_wait_group_read<1>();
+                        __syncwarp();
+                        stage_row(stage_base + sb * kStageBufBytes, lane, p.d_f32, v);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmD, stage_base + sb * kStageBufBytes, col0, m0 + g * 32);
+                            ptx::bulk_commit_group();
+                        }
+                        sb ^= 1;
+                    } else if (row_ok) {
+                        // Ragged last chunk with N not a multiple of 16 bytes:
+                        // the TMA store clips the inner dimension only to 16-byte
+                        // granularity, so write the valid columns one by one.
+                        store_row_tail(p, grow, col0, v);
                     }
-                    sb ^= 1;
                 }
             }
             // Hand the accumulator back to the MMA issuer.

@@ -78,6 +78,20 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier over `nthreads` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred P, Q;\n\t"
+        "setp.ne.u32 Q, %1, 0;\n\t"
+        "bar.red.and.pred P, %2, %3, Q;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

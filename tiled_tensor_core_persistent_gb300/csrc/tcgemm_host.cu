@@ -168,7 +168,12 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     // Split K only when the output tiles cannot fill the machine and each
     // split keeps a useful number of k-blocks.
     int splits = 1;
-    (void)tiles;  // split-K epilogue not wired yet: one unit per tile
+    if (g_force_splits > 0) {
+        splits = g_force_splits;
+    } else if (tiles * 2 <= dev.num_sms && pl.num_kb >= 16) {
+        splits = std::min(dev.num_sms / tiles, pl.num_kb / 8);
+        splits = std::max(1, std::min(splits, 16));
+    }
     splits = std::max(1, std::min(splits, std::max(pl.num_kb, 1)));
     pl.splits = splits;
     pl.units = tiles * splits;
@@ -353,6 +358,9 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.bias_f32 = (epi.bias_dtype == TCG_F32);
     kp.act = static_cast<int>(epi.act);
     kp.d_f32 = (d_dtype == TCG_F32);
+    kp.D = D;
+    kp.ldd = ldd;
+    kp.d_inner_aligned = (static_cast<long long>(N) * elem_bytes(d_dtype)) % 16 == 0;
     kp.stages = pl.stages;
     char* ws = static_cast<char*>(workspace);
     kp.status = reinterpret_cast<int*>(ws);
