@@ -218,3 +218,47 @@ def test_forced_split_k_epilogue_and_determinism():
 def test_skinny_shapes_plan_split_k():
     for (M, N, K) in [(16, 8192, 8192), (8192, 128, 8192)]:
         assert tcg.plan(M, N, K)["splits"] > 1
+
+
+# ------------------------------------------------ 2-CTA pair tiles (cta_group::2)
+
+PAIR_SHAPES = [(256, 256, 64), (300, 520, 384), (513, 700, 129), (1024, 1536, 512), (130, 258, 70)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("combo", inputs.LAYOUT_COMBOS, ids=lambda c: c[0] + c[1])
+def test_pair_tiles_integer_exact(shape, combo):
+    M, N, K = shape
+    try:
+        tcg.debug_set(force_cta2=1)
+        assert tcg.plan(M, N, K)["cluster"] == 2
+        case = inputs.make_case(f"pair{M}x{N}x{K}", M, N, K, seed=M + 5 * N + 11 * K, dist="int4",
+                                opA=combo[0], opB=combo[1], d_dtype="f32")
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()
+
+
+def test_pair_tiles_many_units_epilogue():
+    try:
+        tcg.debug_set(force_cta2=1)
+        case = inputs.make_case("pair_epi", 2304, 2816, 640, seed=151, dist="uniform", beta=0.5,
+                                c_dist="uniform", bias_std=0.1, act="gelu")
+        check_full(case)
+    finally:
+        tcg.debug_set()
+
+
+def test_pair_tiles_fp8():
+    try:
+        tcg.debug_set(force_cta2=1)
+        case = inputs.make_case("pair_f8", 768, 1024, 1024, seed=161, dist="int4", ab_dtype="e4m3",
+                                d_dtype="f32")
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()
+
+
+def test_planner_picks_pairs_for_large_square():
+    pl = tcg.plan(8192, 8192, 8192)
+    assert pl["cluster"] == 2 and pl["grid"] % 2 == 0 and pl["stages"] >= 5

@@ -230,16 +230,27 @@ __device__ __forceinline__ void store_row_tail(const KernelParams& p, int row, i
     }
 }
 
-template <int BN, bool kFp8>
+// kCta2 = false: one CTA per 128 x BN tile.
+// kCta2 = true : a cluster of two CTAs per 256 x BN tile (tcgen05 cta_group::2).
+//   Each CTA loads its own 128 rows of A and its own BN/2 rows of B (no
+//   multicast); the TMA completions of both CTAs are counted on the even
+//   (leader) CTA's full barrier; the leader's single thread issues the pair
+//   MMA, whose result rows 0-127 land in the leader's TMEM and rows 128-255 in
+//   the peer's; commits are multicast to the barriers of both CTAs; the peer's
+//   epilogue hands accumulators back through the leader's tmem_empty barrier.
+template <int BN, bool kFp8, bool kCta2>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
     constexpr int kBK = kRowBytes / kElemBytes;       // elements per k-block
     constexpr int kMmaK = 32 / kElemBytes;             // K per tcgen05.mma
     constexpr int kKSteps = kBK / kMmaK;               // MMAs per k-block
     constexpr int kAtom = kRowBytes / kElemBytes;      // MN elements per swizzle row
+    constexpr int kBRows = kCta2 ? BN / 2 : BN;        // B rows (N) this CTA loads
+    constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
     constexpr int kABytes = kBM * kRowBytes;
-    constexpr int kBBytes = BN * kRowBytes;
+    constexpr int kBBytes = kBRows * kRowBytes;
     constexpr int kStageBytes = kABytes + kBBytes;
+    constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
     constexpr uint32_t kTmemCols = 2 * BN;
     constexpr uint32_t kFmt = kFp8 ? 0u : 1u;          // e4m3 = 0, bf16 = 1
 
@@ -251,6 +262,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kCta2 ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int first_unit = kCta2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int unit_stride = kCta2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&ctl->tmem_full[a], 1);
-            ptx::mbar_init(&ctl->tmem_empty[a], 4);
+            ptx::mbar_init(&ctl->tmem_empty[a], kCta2 ? 8 : 4);
         }
         ptx::mbar_init(&ctl->drain, 1);
         ctl->abort_flag = 0;
@@ -267,11 +282,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
-        ptx::tmem_relinquish_alloc_permit();
+        if constexpr (kCta2) {
+            ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+            ptx::tmem_relinquish_alloc_permit_pair();
+        } else {
+            ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+            ptx::tmem_relinquish_alloc_permit();
+        }
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kCta2) ptx::cluster_sync();  // peer barriers exist before anyone signals them
+    else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const long long limit = p.timeout_ns;
@@ -288,9 +309,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             uint32_t armed = 0, armed_parity = 0;
             bool first = true;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int u = first_unit; ok && u < p.num_units; u += unit_stride) {
                 int m_blk, n_blk, split, kb0, kb1, tile;
                 decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
+                const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
+                const int b_row = n_blk * BN + static_cast<int>(rank) * kBRows;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
                     const bool skip = first && p.fault_inject && blockIdx.x == 0;
@@ -299,22 +322,42 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         uint8_t* sA = smem + stage * kStageBytes;
                         uint8_t* sB = sA + kABytes;
                         uint64_t* fb = &ctl->full[stage];
-                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                        if (!p.a_mn_major) {
-                            ptx::tma_load_2d(sA, &p.tmA, fb, kb * kBK, m_blk * kBM);
-                        } else {
+                        if (leader) ptx::mbar_arrive_expect_tx(fb, kTxBytes);
+                        if constexpr (kCta2) {
+                            const uint32_t fbc = ptx::map_to_cta(ptx::smem_u32(fb), 0);
+                            if (!p.a_mn_major) {
+                                ptx::tma_load_2d_pair(sA, &p.tmA, fbc, kb * kBK, a_row);
+                            } else {
 #pragma unroll
-                            for (int h = 0; h < kBM / kAtom; ++h)
-                                ptx::tma_load_2d(sA + h * kRowBytes * kBK, &p.tmA, fb, m_blk * kBM + h * kAtom,
-                                                 kb * kBK);
-                        }
-                        if (!p.b_mn_major) {
-                            ptx::tma_load_2d(sB, &p.tmB, fb, kb * kBK, n_blk * BN);
-                        } else {
+                                for (int h = 0; h < kBM / kAtom; ++h)
+                                    ptx::tma_load_2d_pair(sA + h * kRowBytes * kBK, &p.tmA, fbc, a_row + h * kAtom,
+                                                          kb * kBK);
+                            }
+                            if (!p.b_mn_major) {
+                                ptx::tma_load_2d_pair(sB, &p.tmB, fbc, kb * kBK, b_row);
+                            } else {
 #pragma unroll
-                            for (int h = 0; h < BN / kAtom; ++h)
-                                ptx::tma_load_2d(sB + h * kRowBytes * kBK, &p.tmB, fb, n_blk * BN + h * kAtom,
-                                                 kb * kBK);
+                                for (int h = 0; h < kBRows / kAtom; ++h)
+                                    ptx::tma_load_2d_pair(sB + h * kRowBytes * kBK, &p.tmB, fbc, b_row + h * kAtom,
+                                                          kb * kBK);
+                            }
+                        } else {
+                            if (!p.a_mn_major) {
+                                ptx::tma_load_2d(sA, &p.tmA, fb, kb * kBK, a_row);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < kBM / kAtom; ++h)
+                                    ptx::tma_load_2d(sA + h * kRowBytes * kBK, &p.tmA, fb, a_row + h * kAtom,
+                                                     kb * kBK);
+                            }
+                            if (!p.b_mn_major) {
+                                ptx::tma_load_2d(sB, &p.tmB, fb, kb * kBK, b_row);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < kBRows / kAtom; ++h)
+                                    ptx::tma_load_2d(sB + h * kRowBytes * kBK, &p.tmB, fb, b_row + h * kAtom,
+                                                     kb * kBK);
+                            }
                         }
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -322,20 +365,25 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
             }
-            // Drain: every stage this thread armed has landed before the CTA
-            // may leave (its shared memory is the copies' destination).
-            for (int s = 0; s < S; ++s)
-                if (armed & (1u << s))
-                    wait_phase(&ctl->full[s], (armed_parity >> s) & 1u, p, ctl, 11, limit, false);
+            // Drain: every stage this thread filled has landed before the CTA
+            // may leave (its shared memory is the copies' destination).  The
+            // leader sees its fills complete on its own full barriers; the
+            // peer sees them consumed through its empty barriers.
+            for (int s = 0; s < S; ++s) {
+                if (!(armed & (1u << s))) continue;
+                const uint32_t par = (armed_parity >> s) & 1u;
+                if (leader) wait_phase(&ctl->full[s], par, p, ctl, 11, limit, false);
+                else wait_phase(&ctl->empty[s], par, p, ctl, 13, limit, false);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             const uint32_t idesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
                                    (static_cast<uint32_t>(p.a_mn_major) << 15) |
                                    (static_cast<uint32_t>(p.b_mn_major) << 16) |
                                    (static_cast<uint32_t>(BN >> 3) << 17) |
-                                   (static_cast<uint32_t>(kBM >> 4) << 24);
+                                   (static_cast<uint32_t>(kTileM >> 4) << 24);
             // Descriptor geometry.  K-major: 8-row groups 1024 B apart (SBO),
             // k-step = +kMmaK*elem bytes inside the swizzle row.  MN-major:
             // swizzle-row boxes of kAtom MN elements, BK rows each (LBO apart),
@@ -349,7 +397,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             int t = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+            for (int u = first_unit; ok && u < p.num_units; u += unit_stride, ++t) {
                 int m_blk, n_blk, split, kb0, kb1, tile;
                 decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
                 const int acc = t & 1;
@@ -369,20 +417,36 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         const uint64_t ad = a_desc + static_cast<uint64_t>(k * a_kstep);
                         const uint64_t bd = b_desc + static_cast<uint64_t>(k * b_kstep);
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if constexpr (kFp8) ptx::mma_f8(d_tmem, ad, bd, idesc, accum);
-                        else ptx::mma_f16(d_tmem, ad, bd, idesc, accum);
+                        if constexpr (kCta2) {
+                            if constexpr (kFp8) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);
+                            else ptx::mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                        } else {
+                            if constexpr (kFp8) ptx::mma_f8(d_tmem, ad, bd, idesc, accum);
+                            else ptx::mma_f16(d_tmem, ad, bd, idesc, accum);
+                        }
                     }
                     issued_any = true;
-                    ptx::mma_commit(&ctl->empty[stage]);
+                    if constexpr (kCta2) ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
+                    else ptx::mma_commit(&ctl->empty[stage]);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (kb1 > kb0) ptx::mma_commit(&ctl->tmem_full[acc]);
-                else ptx::mbar_arrive(&ctl->tmem_full[acc]);
+                if (kb1 > kb0) {
+                    if constexpr (kCta2) ptx::mma_commit_pair(&ctl->tmem_full[acc], 0x3);
+                    else ptx::mma_commit(&ctl->tmem_full[acc]);
+                } else {
+                    if constexpr (kCta2) {
+                        ptx::mbar_arrive(&ctl->tmem_full[acc]);
+                        ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_u32(&ctl->tmem_full[acc]), 1));
+                    } else {
+                        ptx::mbar_arrive(&ctl->tmem_full[acc]);
+                    }
+                }
             }
             // Drain: all MMAs this thread issued complete before TMEM is freed.
             if (issued_any) {
-                ptx::mma_commit(&ctl->drain);
+                if constexpr (kCta2) ptx::mma_commit_pair(&ctl->drain, 0x1);
+                else ptx::mma_commit(&ctl->drain);
                 wait_phase(&ctl->drain, 0, p, ctl, 12, limit, false);
             }
         }
@@ -395,7 +459,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         int t = 0;
         const bool has_c = p.beta != 0.0f;
         const bool split_mode = p.splits > 1;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++t) {
+        for (int u = first_unit; u < p.num_units; u += unit_stride, ++t) {
             int m_blk, n_blk, split, kb0, kb1, tile;
             decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
             const int acc = t & 1;
@@ -407,7 +471,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             if (!ok) break;
             ptx::tc_fence_after_sync();
 
-            const int m0 = m_blk * kBM;
+            const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
             const int n0 = n_blk * BN;
             const int grow = m0 + row_in_tile;
             const bool row_ok = grow < p.M;
@@ -533,17 +597,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             // Hand the accumulator back to the MMA issuer.
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ctl->tmem_empty[acc]);
+            if (lane == 0) {
+                if (kCta2 && !leader)
+                    ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_u32(&ctl->tmem_empty[acc]), 0));
+                else
+                    ptx::mbar_arrive(&ctl->tmem_empty[acc]);
+            }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
     }
 
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kCta2) ptx::cluster_sync();  // the leader's MMAs into the peer's TMEM are done
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (kCta2) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 

@@ -15,7 +15,9 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <string>
 
 #include "../../include/tcgemm.h"
@@ -155,35 +157,57 @@ struct Plan {
     int cluster = 1;
 };
 
-int stage_bytes(int bn) { return (tcg::kBM + bn) * tcg::kRowBytes; }
+int stage_bytes(int bn, bool cta2) { return (tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes; }
+
+int fixed_smem_bytes() {
+    return 1024 /*alignment slack*/ + tcg::kEpiBytes + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
+}
+
+int max_active_pairs(int bn, bool fp8, int smem);
 
 Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     Plan pl;
     const int bk = tcg::kRowBytes / elem_bytes(ab);
     pl.bn = (N <= 128) ? 128 : 256;
-    pl.num_m = (M + tcg::kBM - 1) / tcg::kBM;
-    pl.num_n = (N + pl.bn - 1) / pl.bn;
     pl.num_kb = (K + bk - 1) / bk;
-    const int tiles = pl.num_m * pl.num_n;
+    const int num_m1 = (M + tcg::kBM - 1) / tcg::kBM;
+    const int num_n = (N + pl.bn - 1) / pl.bn;
+    const int tiles1 = num_m1 * num_n;
     // Split K only when the output tiles cannot fill the machine and each
     // split keeps a useful number of k-blocks.
     int splits = 1;
     if (g_force_splits > 0) {
         splits = g_force_splits;
-    } else if (tiles * 2 <= dev.num_sms && pl.num_kb >= 16) {
-        splits = std::min(dev.num_sms / tiles, pl.num_kb / 8);
+    } else if (tiles1 * 2 <= dev.num_sms && pl.num_kb >= 16) {
+        splits = std::min(dev.num_sms / tiles1, pl.num_kb / 8);
         splits = std::max(1, std::min(splits, 16));
     }
     splits = std::max(1, std::min(splits, std::max(pl.num_kb, 1)));
+    // 2-CTA pair tiles (256 x BN) when K is not split and there is at least
+    // one full wave of pairs; they halve the operand bytes each SM streams.
+    const int num_m2 = (M + 2 * tcg::kBM - 1) / (2 * tcg::kBM);
+    bool cta2 = splits == 1 && pl.bn == 256 && M > tcg::kBM && num_m2 * num_n * 2 >= dev.num_sms;
+    if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
+    if (g_force_cta2 == 2) cta2 = false;
+    pl.cluster = cta2 ? 2 : 1;
+    pl.num_m = cta2 ? num_m2 : num_m1;
+    pl.num_n = num_n;
     pl.splits = splits;
-    pl.units = tiles * splits;
-    pl.grid = std::max(1, std::min(pl.units, dev.num_sms));
-    pl.group_m = 8;
-    const int fixed = 1024 /*alignment slack*/ + tcg::kEpiBytes + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
-    int stages = (dev.max_smem_optin - fixed) / stage_bytes(pl.bn);
+    pl.units = pl.num_m * pl.num_n * splits;
+    // Raster group (in M blocks) that keeps one wave's footprint of A rows
+    // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
+    pl.group_m = cta2 ? 8 : 16;
+    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2);
     stages = std::max(2, std::min(stages, 8));
     pl.stages = stages;
-    pl.smem = fixed + stages * stage_bytes(pl.bn);
+    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2);
+    if (cta2) {
+        int pairs = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.smem);
+        if (pairs <= 0) pairs = dev.num_sms / 2;
+        pl.grid = 2 * std::max(1, std::min(pl.units, pairs));
+    } else {
+        pl.grid = std::max(1, std::min(pl.units, dev.num_sms));
+    }
     return pl;
 }
 
@@ -197,22 +221,79 @@ size_t counter_bytes(const Plan& pl) {
     return (static_cast<size_t>(pl.num_m) * pl.num_n * sizeof(int) + 255) / 256 * 256;
 }
 
-template <int BN, bool kFp8>
-tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
-    auto kern = tcg::gemm_persistent_kernel<BN, kFp8>;
+template <int BN, bool kFp8, bool kCta2>
+cudaError_t set_smem_attr() {
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (err == cudaSuccess && kCta2)
+            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     });
-    if (attr_err != cudaSuccess) return fail_launch("cudaFuncSetAttribute", attr_err);
+    return err;
+}
+
+template <int BN, bool kFp8>
+int active_pairs_for(int smem) {
+    if (set_smem_attr<BN, kFp8, true>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(tcg::kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tcg::gemm_persistent_kernel<BN, kFp8, true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Pairs of CTAs that fit on the device at once, per (BN, dtype, smem), cached.
+int max_active_pairs(int bn, bool fp8, int smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, bn, fp8 ? 1 : 0, smem);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (bn == 256) n = fp8 ? active_pairs_for<256, true>(smem) : active_pairs_for<256, false>(smem);
+    cache[key] = n;
+    return n;
+}
+
+template <int BN, bool kFp8, bool kCta2>
+tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
+    cudaError_t e = set_smem_attr<BN, kFp8, kCta2>();
+    if (e != cudaSuccess) return fail_launch("cudaFuncSetAttribute", e);
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(pl.grid, 1, 1);
     cfg.blockDim = dim3(tcg::kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = stream;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+    if (kCta2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2>, kp);
     if (e != cudaSuccess) return fail_launch("cudaLaunchKernelEx", e);
     return TCG_OK;
 }
@@ -335,8 +416,9 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         else
             st = encode_2d(&kp.tmA, ab_dtype, A, M, K, lda, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
+        const int b_rows = pl.cluster == 2 ? pl.bn / 2 : pl.bn;  // B rows one CTA loads
         if (opB == TCG_COL)
-            st = encode_2d(&kp.tmB, ab_dtype, B, K, N, ldb, bk, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+            st = encode_2d(&kp.tmB, ab_dtype, B, K, N, ldb, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
         else
             st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
@@ -370,8 +452,11 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.fault_inject = g_fault_inject;
 
     const bool fp8 = ab_dtype == TCG_E4M3;
-    if (pl.bn == 256) return fp8 ? launch_kernel<256, true>(kp, pl, stream) : launch_kernel<256, false>(kp, pl, stream);
-    return fp8 ? launch_kernel<128, true>(kp, pl, stream) : launch_kernel<128, false>(kp, pl, stream);
+    if (pl.cluster == 2)
+        return fp8 ? launch_kernel<256, true, true>(kp, pl, stream) : launch_kernel<256, false, true>(kp, pl, stream);
+    if (pl.bn == 256)
+        return fp8 ? launch_kernel<256, true, false>(kp, pl, stream) : launch_kernel<256, false, false>(kp, pl, stream);
+    return fp8 ? launch_kernel<128, true, false>(kp, pl, stream) : launch_kernel<128, false, false>(kp, pl, stream);
 }
 
 tcg_status tcg_device_status(void* workspace, void* stream_) {
