@@ -70,6 +70,20 @@ struct KernelParams {
     int* status;          // [0] status, [1] where, [2] block
     long long timeout_ns;
     int fault_inject;
+    unsigned long long* stats;  // optional cycle accounting (nullptr = off), see kStat*
+};
+
+
+// Cycle accounting slots (summed over CTAs) when KernelParams::stats is set.
+enum : int {
+    kStatMmaWaitFull = 0,     // MMA issuer waiting for loaded stages
+    kStatMmaWaitAcc = 1,      // MMA issuer waiting for a free accumulator
+    kStatProdWaitEmpty = 2,   // producer waiting for a free stage
+    kStatEpiWaitFull = 3,     // epilogue (warp 2) waiting for a finished accumulator
+    kStatEpiBusy = 4,         // epilogue (warp 2) from accumulator ready to hand-back
+    kStatMmaTotal = 5,        // MMA issuer loop, first wait to last commit
+    kStatCtas = 6,
+    kNumStats = 8
 };
 
 // Shared-memory bookkeeping that lives after the operand stages.
@@ -115,6 +129,15 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const Ke
     }
 }
 
+// The whole warp waits (converged), then agrees on the outcome.  Role warps
+// run their loops with all 32 lanes and let lane 0 issue, so no lane of a
+// role warp ever sits at a CTA-wide barrier while its siblings spin.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const KernelParams& p, SmemCtl* ctl,
+                                          int where, long long limit_ns, bool honor_abort = true) {
+    const bool ok = wait_phase(bar, parity, p, ctl, where, limit_ns, honor_abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& m_blk, int& n_blk,
                                             int& split, int& kb0, int& kb1, int& tile) {
     tile = u / p.splits;
@@ -129,6 +152,7 @@ __device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& m
     kb0 = static_cast<int>((static_cast<long long>(split) * p.num_kb) / p.splits);
     kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.num_kb) / p.splits);
 }
+
 
 __device__ __forceinline__ float gelu_erf(float x) {
     return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
@@ -299,14 +323,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            if (p.num_kb > 0) {
+        {
+            const bool issuer = lane == 0;
+            if (issuer && p.num_kb > 0) {
                 ptx::prefetch_tensormap(&p.tmA);
                 ptx::prefetch_tensormap(&p.tmB);
             }
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
+            long long st_wait = 0;
             bool first = true;
             bool ok = true;
             for (int u = first_unit; ok && u < p.num_units; u += unit_stride) {
@@ -315,10 +341,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
                 const int b_row = n_blk * BN + static_cast<int>(rank) * kBRows;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
+                    const long long tw = p.stats ? clock64() : 0;
+                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
+                    if (p.stats) st_wait += clock64() - tw;
                     const bool skip = first && p.fault_inject && blockIdx.x == 0;
                     first = false;
-                    if (!skip) {
+                    if (!skip && issuer) {
                         uint8_t* sA = smem + stage * kStageBytes;
                         uint8_t* sB = sA + kABytes;
                         uint64_t* fb = &ctl->full[stage];
@@ -359,12 +387,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                                      kb * kBK);
                             }
                         }
+                    }
+                    if (!skip) {
                         armed |= 1u << stage;
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
+                    __syncwarp();
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
             }
+            if (p.stats && issuer) atomicAdd(p.stats + kStatProdWaitEmpty, static_cast<unsigned long long>(st_wait));
             // Drain: every stage this thread filled has landed before the CTA
             // may leave (its shared memory is the copies' destination).  The
             // leader sees its fills complete on its own full barriers; the
@@ -372,13 +404,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             for (int s = 0; s < S; ++s) {
                 if (!(armed & (1u << s))) continue;
                 const uint32_t par = (armed_parity >> s) & 1u;
-                if (leader) wait_phase(&ctl->full[s], par, p, ctl, 11, limit, false);
-                else wait_phase(&ctl->empty[s], par, p, ctl, 13, limit, false);
+                if (leader) warp_wait(&ctl->full[s], par, p, ctl, 11, limit, false);
+                else warp_wait(&ctl->empty[s], par, p, ctl, 13, limit, false);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && leader) {
+        if (leader) {
+            const bool issuer = lane == 0;
             const uint32_t idesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
                                    (static_cast<uint32_t>(p.a_mn_major) << 15) |
                                    (static_cast<uint32_t>(p.b_mn_major) << 16) |
@@ -397,17 +430,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             int t = 0;
             bool ok = true;
             bool issued_any = false;
+            long long st_full = 0, st_acc = 0;
+            const long long st_t0 = p.stats ? clock64() : 0;
             for (int u = first_unit; ok && u < p.num_units; u += unit_stride, ++t) {
                 int m_blk, n_blk, split, kb0, kb1, tile;
                 decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
                 const int acc = t & 1;
                 const uint32_t acc_phase = (t >> 1) & 1;
-                if (!wait_phase(&ctl->tmem_empty[acc], acc_phase ^ 1u, p, ctl, 2, limit)) { ok = false; break; }
+                const long long ta = p.stats ? clock64() : 0;
+                if (!warp_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, p, ctl, 2, limit)) { ok = false; break; }
+                if (p.stats) st_acc += clock64() - ta;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(&ctl->full[stage], phase, p, ctl, 3, limit)) { ok = false; break; }
+                    const long long tf = p.stats ? clock64() : 0;
+                    if (!warp_wait(&ctl->full[stage], phase, p, ctl, 3, limit)) { ok = false; break; }
+                    if (p.stats) st_full += clock64() - tf;
                     ptx::tc_fence_after_sync();
+                    if (issuer) {
                     const uint32_t sA = ptx::smem_u32(smem + stage * kStageBytes);
                     const uint32_t sB = sA + kABytes;
                     const uint64_t a_desc = ptx::smem_desc_sw128(sA, a_lbo, 1024);
@@ -425,13 +465,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             else ptx::mma_f16(d_tmem, ad, bd, idesc, accum);
                         }
                     }
-                    issued_any = true;
                     if constexpr (kCta2) ptx::mma_commit_pair(&ctl->empty[stage], 0x3);
                     else ptx::mma_commit(&ctl->empty[stage]);
+                    }
+                    __syncwarp();
+                    issued_any = true;
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (kb1 > kb0) {
+                if (!issuer) {
+                } else if (kb1 > kb0) {
                     if constexpr (kCta2) ptx::mma_commit_pair(&ctl->tmem_full[acc], 0x3);
                     else ptx::mma_commit(&ctl->tmem_full[acc]);
                 } else {
@@ -443,11 +486,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     }
                 }
             }
-            // Drain: all MMAs this thread issued complete before TMEM is freed.
+            if (p.stats && issuer) {
+                atomicAdd(p.stats + kStatMmaWaitFull, static_cast<unsigned long long>(st_full));
+                atomicAdd(p.stats + kStatMmaWaitAcc, static_cast<unsigned long long>(st_acc));
+                atomicAdd(p.stats + kStatMmaTotal, static_cast<unsigned long long>(clock64() - st_t0));
+                atomicAdd(p.stats + kStatCtas, 1ull);
+            }
+            // Drain: all MMAs lane 0 issued complete before TMEM is freed.
             if (issued_any) {
-                if constexpr (kCta2) ptx::mma_commit_pair(&ctl->drain, 0x1);
-                else ptx::mma_commit(&ctl->drain);
-                wait_phase(&ctl->drain, 0, p, ctl, 12, limit, false);
+                if (issuer) {
+                    if constexpr (kCta2) ptx::mma_commit_pair(&ctl->drain, 0x1);
+                    else ptx::mma_commit(&ctl->drain);
+                }
+                __syncwarp();
+                warp_wait(&ctl->drain, 0, p, ctl, 12, limit, false);
             }
         }
     } else {
@@ -459,12 +511,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         int t = 0;
         const bool has_c = p.beta != 0.0f;
         const bool split_mode = p.splits > 1;
+        long long st_ewait = 0, st_ebusy = 0;
         for (int u = first_unit; u < p.num_units; u += unit_stride, ++t) {
             int m_blk, n_blk, split, kb0, kb1, tile;
             decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
+            const long long te = p.stats ? clock64() : 0;
             bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
+            const long long te1 = p.stats ? clock64() : 0;
+            if (p.stats) st_ewait += te1 - te;
             // All four epilogue warps take the same branch (the split-K named
             // barriers below must be reached by all 128 threads or by none).
             ok = ptx::named_barrier_and(1, kEpiThreads, ok);
@@ -597,6 +653,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             // Hand the accumulator back to the MMA issuer.
             ptx::tc_fence_before_sync();
             __syncwarp();
+            if (p.stats) st_ebusy += clock64() - te1;
             if (lane == 0) {
                 if (kCta2 && !leader)
                     ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_u32(&ctl->tmem_empty[acc]), 0));
@@ -605,6 +662,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
+        if (p.stats && warp == kEpiWarp0 && lane == 0) {
+            atomicAdd(p.stats + kStatEpiWaitFull, static_cast<unsigned long long>(st_ewait));
+            atomicAdd(p.stats + kStatEpiBusy, static_cast<unsigned long long>(st_ebusy));
+        }
     }
 
     ptx::tc_fence_before_sync();

@@ -14,6 +14,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -35,6 +36,17 @@ int g_force_cta2 = 0;
 constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s
 
 constexpr size_t kHeaderBytes = 256;  // status word + diagnostics
+
+// Planner overrides for tuning experiments (environment, read once):
+// TCG_GROUP_M = raster group in M blocks, TCG_STAGES = pipeline depth cap.
+int env_int(const char* name) {
+    const char* v = getenv(name);
+    return v ? atoi(v) : 0;
+}
+const int g_env_group_m = env_int("TCG_GROUP_M");
+const int g_env_stages = env_int("TCG_STAGES");
+// TCG_STATS=1: accumulate per-role cycle counts into workspace bytes 64..127.
+const int g_env_stats = env_int("TCG_STATS");
 
 tcg_status fail_launch(const char* what, cudaError_t e) {
     char buf[512];
@@ -197,8 +209,10 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     // Raster group (in M blocks) that keeps one wave's footprint of A rows
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
+    if (g_env_group_m > 0) pl.group_m = g_env_group_m;
     int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2);
     stages = std::max(2, std::min(stages, 8));
+    if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
     pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2);
     if (cta2) {
@@ -450,6 +464,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + kHeaderBytes + counter_bytes(pl)) : nullptr;
     kp.timeout_ns = g_timeout_ns > 0 ? g_timeout_ns : kDefaultTimeoutNs;
     kp.fault_inject = g_fault_inject;
+    kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = ab_dtype == TCG_E4M3;
     if (pl.cluster == 2)
