@@ -262,17 +262,22 @@ __device__ __forceinline__ void store_row_tail(const KernelParams& p, int row, i
 //   MMA, whose result rows 0-127 land in the leader's TMEM and rows 128-255 in
 //   the peer's; commits are multicast to the barriers of both CTAs; the peer's
 //   epilogue hands accumulators back through the leader's tmem_empty barrier.
-template <int BN, bool kFp8, bool kCta2>
+//
+// kKAtoms = 128-byte K atoms per pipeline stage (1 or 2).  Two atoms put
+// twice the MMAs behind each stage handshake (wait, commit), which is what
+// keeps the tensor pipe busy with pair tiles.
+template <int BN, bool kFp8, bool kCta2, int kKAtoms>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
-    constexpr int kBK = kRowBytes / kElemBytes;       // elements per k-block
+    constexpr int kBK = kRowBytes / kElemBytes;       // K elements per 128-byte atom
+    constexpr int kStageK = kKAtoms * kBK;             // K elements per pipeline stage
     constexpr int kMmaK = 32 / kElemBytes;             // K per tcgen05.mma
-    constexpr int kKSteps = kBK / kMmaK;               // MMAs per k-block
+    constexpr int kKSteps = kBK / kMmaK;               // MMAs per atom
     constexpr int kAtom = kRowBytes / kElemBytes;      // MN elements per swizzle row
     constexpr int kBRows = kCta2 ? BN / 2 : BN;        // B rows (N) this CTA loads
     constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
-    constexpr int kABytes = kBM * kRowBytes;
-    constexpr int kBBytes = kBRows * kRowBytes;
+    constexpr int kABytes = kKAtoms * kBM * kRowBytes;
+    constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
     constexpr int kStageBytes = kABytes + kBBytes;
     constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
     constexpr uint32_t kTmemCols = 2 * BN;
@@ -351,41 +356,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         uint8_t* sB = sA + kABytes;
                         uint64_t* fb = &ctl->full[stage];
                         if (leader) ptx::mbar_arrive_expect_tx(fb, kTxBytes);
-                        if constexpr (kCta2) {
-                            const uint32_t fbc = ptx::map_to_cta(ptx::smem_u32(fb), 0);
-                            if (!p.a_mn_major) {
-                                ptx::tma_load_2d_pair(sA, &p.tmA, fbc, kb * kBK, a_row);
-                            } else {
+                        const uint32_t fbc = kCta2 ? ptx::map_to_cta(ptx::smem_u32(fb), 0) : 0u;
+                        auto load = [&](void* dst, const CUtensorMap* map, int x, int y) {
+                            if constexpr (kCta2) ptx::tma_load_2d_pair(dst, map, fbc, x, y);
+                            else ptx::tma_load_2d(dst, map, fb, x, y);
+                        };
+                        const int k0 = kb * kStageK;
+                        // K-major: one box of BK x rows per atom, atoms stacked;
+                        // MN-major: one box of kAtom x kStageK per MN atom.
+                        if (!p.a_mn_major) {
 #pragma unroll
-                                for (int h = 0; h < kBM / kAtom; ++h)
-                                    ptx::tma_load_2d_pair(sA + h * kRowBytes * kBK, &p.tmA, fbc, a_row + h * kAtom,
-                                                          kb * kBK);
-                            }
-                            if (!p.b_mn_major) {
-                                ptx::tma_load_2d_pair(sB, &p.tmB, fbc, kb * kBK, b_row);
-                            } else {
-#pragma unroll
-                                for (int h = 0; h < kBRows / kAtom; ++h)
-                                    ptx::tma_load_2d_pair(sB + h * kRowBytes * kBK, &p.tmB, fbc, b_row + h * kAtom,
-                                                          kb * kBK);
-                            }
+                            for (int at = 0; at < kKAtoms; ++at)
+                                load(sA + at * kBM * kRowBytes, &p.tmA, k0 + at * kBK, a_row);
                         } else {
-                            if (!p.a_mn_major) {
-                                ptx::tma_load_2d(sA, &p.tmA, fb, kb * kBK, a_row);
-                            } else {
 #pragma unroll
-                                for (int h = 0; h < kBM / kAtom; ++h)
-                                    ptx::tma_load_2d(sA + h * kRowBytes * kBK, &p.tmA, fb, a_row + h * kAtom,
-                                                     kb * kBK);
-                            }
-                            if (!p.b_mn_major) {
-                                ptx::tma_load_2d(sB, &p.tmB, fb, kb * kBK, b_row);
-                            } else {
+                            for (int h = 0; h < kBM / kAtom; ++h)
+                                load(sA + h * kRowBytes * kStageK, &p.tmA, a_row + h * kAtom, k0);
+                        }
+                        if (!p.b_mn_major) {
 #pragma unroll
-                                for (int h = 0; h < kBRows / kAtom; ++h)
-                                    ptx::tma_load_2d(sB + h * kRowBytes * kBK, &p.tmB, fb, b_row + h * kAtom,
-                                                     kb * kBK);
-                            }
+                            for (int at = 0; at < kKAtoms; ++at)
+                                load(sB + at * kBRows * kRowBytes, &p.tmB, k0 + at * kBK, b_row);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < kBRows / kAtom; ++h)
+                                load(sB + h * kRowBytes * kStageK, &p.tmB, b_row + h * kAtom, k0);
                         }
                     }
                     if (!skip) {
@@ -421,10 +416,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             // k-step = +kMmaK*elem bytes inside the swizzle row.  MN-major:
             // swizzle-row boxes of kAtom MN elements, BK rows each (LBO apart),
             // 8-row K groups 1024 B apart (SBO), k-step = kMmaK rows.
-            const uint32_t a_lbo = p.a_mn_major ? static_cast<uint32_t>(kRowBytes * kBK) : 16u;
-            const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(kRowBytes * kBK) : 16u;
-            const uint32_t a_kstep = p.a_mn_major ? (kMmaK * kRowBytes) >> 4 : (kMmaK * kElemBytes) >> 4;
-            const uint32_t b_kstep = p.b_mn_major ? (kMmaK * kRowBytes) >> 4 : (kMmaK * kElemBytes) >> 4;
+            const uint32_t a_lbo = p.a_mn_major ? static_cast<uint32_t>(kRowBytes * kStageK) : 16u;
+            const uint32_t b_lbo = p.b_mn_major ? static_cast<uint32_t>(kRowBytes * kStageK) : 16u;
+            // start-address advance (16-byte units) of MMA kk within a stage
+            auto a_off = [&](int kk) -> uint32_t {
+                return p.a_mn_major ? static_cast<uint32_t>(kk * kMmaK * kRowBytes) >> 4
+                                    : static_cast<uint32_t>((kk / kKSteps) * kBM * kRowBytes +
+                                                            (kk % kKSteps) * kMmaK * kElemBytes) >> 4;
+            };
+            auto b_off = [&](int kk) -> uint32_t {
+                return p.b_mn_major ? static_cast<uint32_t>(kk * kMmaK * kRowBytes) >> 4
+                                    : static_cast<uint32_t>((kk / kKSteps) * kBRows * kRowBytes +
+                                                            (kk % kKSteps) * kMmaK * kElemBytes) >> 4;
+            };
             int stage = 0;
             uint32_t phase = 0;
             int t = 0;
@@ -453,9 +457,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     const uint64_t a_desc = ptx::smem_desc_sw128(sA, a_lbo, 1024);
                     const uint64_t b_desc = ptx::smem_desc_sw128(sB, b_lbo, 1024);
 #pragma unroll
-                    for (int k = 0; k < kKSteps; ++k) {
-                        const uint64_t ad = a_desc + static_cast<uint64_t>(k * a_kstep);
-                        const uint64_t bd = b_desc + static_cast<uint64_t>(k * b_kstep);
+                    for (int k = 0; k < kKAtoms * kKSteps; ++k) {
+                        const uint64_t ad = a_desc + static_cast<uint64_t>(a_off(k));
+                        const uint64_t bd = b_desc + static_cast<uint64_t>(b_off(k));
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
                         if constexpr (kCta2) {
                             if constexpr (kFp8) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);

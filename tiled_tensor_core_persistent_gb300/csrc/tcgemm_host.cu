@@ -47,6 +47,8 @@ const int g_env_group_m = env_int("TCG_GROUP_M");
 const int g_env_stages = env_int("TCG_STAGES");
 // TCG_STATS=1: accumulate per-role cycle counts into workspace bytes 64..127.
 const int g_env_stats = env_int("TCG_STATS");
+// TCG_KATOMS = K atoms per stage for pair tiles (1 or 2; default 2).
+const int g_env_katoms = env_int("TCG_KATOMS");
 
 tcg_status fail_launch(const char* what, cudaError_t e) {
     char buf[512];
@@ -167,20 +169,25 @@ struct Plan {
     int smem = 0;
     int num_m = 0, num_n = 0, num_kb = 0;
     int cluster = 1;
+    int katoms = 1;  // 128-byte K atoms per pipeline stage
 };
 
-int stage_bytes(int bn, bool cta2) { return (tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes; }
+int stage_bytes(int bn, bool cta2, int katoms) {
+    return katoms * (tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes;
+}
 
 int fixed_smem_bytes() {
     return 1024 /*alignment slack*/ + tcg::kEpiBytes + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
 }
 
-int max_active_pairs(int bn, bool fp8, int smem);
+int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 
 Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     Plan pl;
     const int bk = tcg::kRowBytes / elem_bytes(ab);
     pl.bn = (N <= 128) ? 128 : 256;
+    // K atoms per stage are decided with the tile shape below; the split-K
+    // heuristic works on single-atom k-blocks.
     pl.num_kb = (K + bk - 1) / bk;
     const int num_m1 = (M + tcg::kBM - 1) / tcg::kBM;
     const int num_n = (N + pl.bn - 1) / pl.bn;
@@ -202,6 +209,8 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
     if (g_force_cta2 == 2) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
+    pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : 1;
+    pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
     pl.splits = splits;
@@ -210,13 +219,13 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
-    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2);
+    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms);
     stages = std::max(2, std::min(stages, 8));
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
-    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2);
+    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms);
     if (cta2) {
-        int pairs = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.smem);
+        int pairs = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.katoms, pl.smem);
         if (pairs <= 0) pairs = dev.num_sms / 2;
         pl.grid = 2 * std::max(1, std::min(pl.units, pairs));
     } else {
@@ -235,23 +244,23 @@ size_t counter_bytes(const Plan& pl) {
     return (static_cast<size_t>(pl.num_m) * pl.num_n * sizeof(int) + 255) / 256 * 256;
 }
 
-template <int BN, bool kFp8, bool kCta2>
+template <int BN, bool kFp8, bool kCta2, int KA>
 cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2>,
+        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (err == cudaSuccess && kCta2)
-            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2>,
+            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     });
     return err;
 }
 
-template <int BN, bool kFp8>
+template <int BN, bool kFp8, int KA>
 int active_pairs_for(int smem) {
-    if (set_smem_attr<BN, kFp8, true>() != cudaSuccess) return 0;
+    if (set_smem_attr<BN, kFp8, true, KA>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr[1];
@@ -265,7 +274,7 @@ int active_pairs_for(int smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tcg::gemm_persistent_kernel<BN, kFp8, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tcg::gemm_persistent_kernel<BN, kFp8, true, KA>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -273,24 +282,25 @@ int active_pairs_for(int smem) {
 }
 
 // Pairs of CTAs that fit on the device at once, per (BN, dtype, smem), cached.
-int max_active_pairs(int bn, bool fp8, int smem) {
+int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, bn, fp8 ? 1 : 0, smem);
+    const auto key = std::make_tuple(dev, bn, (fp8 ? 1 : 0) + 2 * katoms, smem);
     std::lock_guard<std::mutex> lk(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (bn == 256) n = fp8 ? active_pairs_for<256, true>(smem) : active_pairs_for<256, false>(smem);
+    if (bn == 256 && katoms == 2) n = fp8 ? active_pairs_for<256, true, 2>(smem) : active_pairs_for<256, false, 2>(smem);
+    if (bn == 256 && katoms == 1) n = fp8 ? active_pairs_for<256, true, 1>(smem) : active_pairs_for<256, false, 1>(smem);
     cache[key] = n;
     return n;
 }
 
-template <int BN, bool kFp8, bool kCta2>
+template <int BN, bool kFp8, bool kCta2, int KA>
 tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<BN, kFp8, kCta2>();
+    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA>();
     if (e != cudaSuccess) return fail_launch("cudaFuncSetAttribute", e);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -307,7 +317,7 @@ tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2>, kp);
+    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>, kp);
     if (e != cudaSuccess) return fail_launch("cudaLaunchKernelEx", e);
     return TCG_OK;
 }
@@ -391,7 +401,7 @@ tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]) {
     tcg_status st = device_info(dev);
     if (st != TCG_OK) return st;
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
-    const int vals[10] = {tcg::kBM, pl.bn, tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
+    const int vals[10] = {tcg::kBM, pl.bn, pl.katoms * tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
                           pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem};
     memcpy(out, vals, sizeof vals);
     return TCG_OK;
@@ -428,13 +438,13 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         if (opA == TCG_ROW)
             st = encode_2d(&kp.tmA, ab_dtype, A, K, M, lda, bk, tcg::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
         else
-            st = encode_2d(&kp.tmA, ab_dtype, A, M, K, lda, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
+            st = encode_2d(&kp.tmA, ab_dtype, A, M, K, lda, atom, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
         const int b_rows = pl.cluster == 2 ? pl.bn / 2 : pl.bn;  // B rows one CTA loads
         if (opB == TCG_COL)
             st = encode_2d(&kp.tmB, ab_dtype, B, K, N, ldb, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
         else
-            st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B);
+            st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
     }
     st = encode_2d(&kp.tmD, d_dtype, D, N, M, ldd, tcg::kEpiChunk, 32,
@@ -467,11 +477,16 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = ab_dtype == TCG_E4M3;
+    if (pl.cluster == 2 && pl.katoms == 2)
+        return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)
+                   : launch_kernel<256, false, true, 2>(kp, pl, stream);
     if (pl.cluster == 2)
-        return fp8 ? launch_kernel<256, true, true>(kp, pl, stream) : launch_kernel<256, false, true>(kp, pl, stream);
+        return fp8 ? launch_kernel<256, true, true, 1>(kp, pl, stream)
+                   : launch_kernel<256, false, true, 1>(kp, pl, stream);
     if (pl.bn == 256)
-        return fp8 ? launch_kernel<256, true, false>(kp, pl, stream) : launch_kernel<256, false, false>(kp, pl, stream);
-    return fp8 ? launch_kernel<128, true, false>(kp, pl, stream) : launch_kernel<128, false, false>(kp, pl, stream);
+        return fp8 ? launch_kernel<256, true, false, 1>(kp, pl, stream)
+                   : launch_kernel<256, false, false, 1>(kp, pl, stream);
+    return fp8 ? launch_kernel<128, true, false, 1>(kp, pl, stream) : launch_kernel<128, false, false, 1>(kp, pl, stream);
 }
 
 tcg_status tcg_device_status(void* workspace, void* stream_) {
