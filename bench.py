@@ -229,7 +229,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     import tiled_tensor_core_persistent_gb300 as tcg
-    from tiled_tensor_core_persistent_gb300 import _build, harness, inputs
+    from tiled_tensor_core_persistent_gb300 import _build, analysis, harness, inputs
     if rank == 0:
         _build.build()
     barrier(pg, device)
@@ -284,7 +284,11 @@ def run_ours(args):
             "peak_kind": f"{peak_kind} bf16 burst (cuBLAS 8192^3)",
             "peak_sustained": peaks.get("bf16_tflops_sustained"),
             "frac_of_nominal_2250": per_launch_tflops / 2250.0,
-            "algorithmic": "2*M*N*K flop per launch"}
+            "algorithmic": "2*M*N*K flop per launch",
+            "model": {"intensity_flop_per_byte": analysis.boundary_intensity(case.M, case.N, case.K, 2),
+                      "roofline_tflops": analysis.roofline(2250.0, analysis.boundary_intensity(case.M, case.N, case.K, 2),
+                                                           float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)) * 1e-3),
+                      "algorithmic_bytes": analysis.gemm_bytes(case.M, case.N, case.K, 2, 2, 0, 2)}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
