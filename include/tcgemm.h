@@ -155,6 +155,34 @@ tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);
  */
 void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2);
 
+/*
+ * tcg_gemm_noalloc -- the same GEMM as tcg_gemm for callers that cannot
+ * allocate device memory, so cannot pass a workspace: e.g. plugins that only
+ * receive input/output pointers from an engine that owns all device memory,
+ * or latency-critical loops where cudaMalloc/cudaFree are not allowed.
+ * The reference pages have no counterpart; this is a property of the library.
+ *   Arguments: as tcg_gemm, without the workspace.  It allocates nothing.
+ *   Scratch: a 32 MiB file-scope device array held by every GPU that loads
+ *     the library until the process exits.  Problems whose workspace
+ *     (tcg_workspace_size) exceeds 32 MiB return TCG_ERR_WORKSPACE with a
+ *     message in tcg_last_error.
+ *   Set-up: the first call on each device (with that device current) looks
+ *     up the array's device address; make that first call before any stream
+ *     capture.
+ *   Concurrency: all calls on a device share the one array; calls that
+ *     overlap on the GPU (different streams, unordered) race and give wrong
+ *     results.  Each call clears the status word and split-K counters first.
+ *   Device-side wait timeouts still end the kernel but are not reported (no
+ *     workspace is visible to the caller).
+ */
+tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha,
+                            const void* A, int lda, tcg_layout opA,
+                            const void* B, int ldb, tcg_layout opB,
+                            float beta, const void* C, int ldc, tcg_dtype c_dtype,
+                            void* D, int ldd, tcg_dtype d_dtype,
+                            tcg_epilogue epi, tcg_dtype ab_dtype, tcg_scales scales,
+                            void* stream);
+
 #ifdef __cplusplus
 }
 #endif

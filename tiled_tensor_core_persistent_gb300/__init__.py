@@ -32,7 +32,7 @@ STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "T
           4: "TCG_ERR_ARCH", 5: "TCG_ERR_WORKSPACE", 6: "TCG_ERR_LAUNCH", 7: "TCG_ERR_TIMEOUT"}
 
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_init", "tcg_gemm",
-            "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set"]
+            "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc"]
 
 
 class TcgError(RuntimeError):
@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
         L.tcg_gemm.argtypes = [i32, i32, i32, f32, P, i32, i32, P, i32, i32, f32, P, i32, i32, P, i32, i32,
                                Epilogue, i32, Scales, P, sz, P]
         L.tcg_gemm.restype = i32
+        L.tcg_gemm_noalloc.argtypes = [i32, i32, i32, f32, P, i32, i32, P, i32, i32, f32, P, i32, i32, P, i32,
+                                       i32, Epilogue, i32, Scales, P]
+        L.tcg_gemm_noalloc.restype = i32
         L.tcg_device_status.argtypes = [P, P]
         L.tcg_device_status.restype = i32
         L.tcg_last_error.argtypes = []
@@ -148,6 +151,19 @@ def gemm(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd
                         _addr(workspace), int(workspace_bytes), _stream(stream))
     if st != 0:
         raise TcgError(st, "tcg_gemm", last_error())
+
+
+def gemm_noalloc(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd, d_dtype, *,
+                 bias=None, bias_dtype="bf16", act="none", ab_dtype="bf16", scale_a=1.0, scale_b=1.0,
+                 stream=None) -> None:
+    """tcg_gemm_noalloc: the same GEMM with the library's built-in device scratch (see tcgemm.h)."""
+    epi = Epilogue(_addr(bias), _enum(bias_dtype, DTYPES), _enum(act, ACTS))
+    st = lib().tcg_gemm_noalloc(M, N, K, alpha, _addr(A), lda, _enum(opA, LAYOUTS), _addr(B), ldb,
+                                _enum(opB, LAYOUTS), beta, _addr(C), ldc, _enum(c_dtype, DTYPES), _addr(D),
+                                ldd, _enum(d_dtype, DTYPES), epi, _enum(ab_dtype, DTYPES),
+                                Scales(scale_a, scale_b), _stream(stream))
+    if st != 0:
+        raise TcgError(st, "tcg_gemm_noalloc", last_error())
 
 
 def device_status(workspace, stream=None) -> int:

@@ -509,3 +509,76 @@ tcg_status tcg_device_status(void* workspace, void* stream_) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- no-allocation entry point
+//
+// Some callers cannot allocate device memory: plugins that receive only
+// input and output pointers from a host engine that owns every byte of device
+// memory (and hands out no allocator or workspace), and latency-critical loops
+// where cudaMalloc/cudaFree are not allowed because of their cost and implicit
+// synchronisation.  tcg_gemm itself allocates nothing, but it needs a
+// caller-provided workspace, which such callers cannot supply.
+// tcg_gemm_noalloc runs the same GEMM with its workspace taken from this
+// file-scope device array instead.  Every GPU that loads the library holds
+// the array until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+
+// Device-side scratch.  In host code this name is only a stand-in for the
+// symbol, never a device address: the address is taken once per device with
+// cudaGetSymbolAddress and passed to the kernel.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+}  // namespace
+
+extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const void* A, int lda, tcg_layout opA,
+                                       const void* B, int ldb, tcg_layout opB, float beta, const void* C, int ldc,
+                                       tcg_dtype c_dtype, void* D, int ldd, tcg_dtype d_dtype, tcg_epilogue epi,
+                                       tcg_dtype ab_dtype, tcg_scales scales, void* stream_) {
+    const int has_c = beta != 0.0f;
+    tcg_status st = tcg_can_implement(M, N, K, ab_dtype, A, lda, opA, B, ldb, opB, has_c, C, ldc, c_dtype, D, ldd,
+                                      d_dtype, epi);
+    if (st != TCG_OK) return st;
+    if (M == 0 || N == 0) return TCG_OK;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != TCG_OK) return st;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return fail_launch("cudaGetDevice", e);
+    if (device < 0 || device >= 64) { g_last_error = "device index out of range"; return TCG_ERR_LAUNCH; }
+    void* scratch = nullptr;
+    {
+        // Set-up, once per device, on the first call made with that device current.
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[device]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr) return fail_launch("cudaGetSymbolAddress(scratch)", e);
+            g_noalloc_ptr[device] = ptr;
+        }
+        scratch = g_noalloc_ptr[device];
+    }
+    const Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    if (need > kNoAllocScratchBytes) {
+        char buf[200];
+        snprintf(buf, sizeof buf,
+                 "tcg_gemm_noalloc: this problem needs %zu bytes of scratch, more than the %zu-byte maximum; "
+                 "use tcg_gemm with a workspace",
+                 need, kNoAllocScratchBytes);
+        g_last_error = buf;
+        return TCG_ERR_WORKSPACE;
+    }
+    // The array keeps the previous call's contents: the status word and the
+    // split-K arrival counters must start at zero.
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    e = cudaMemsetAsync(scratch, 0, kHeaderBytes + counter_bytes(pl), stream);
+    if (e != cudaSuccess) return fail_launch("cudaMemsetAsync(scratch)", e);
+    return tcg_gemm(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd, d_dtype, epi, ab_dtype,
+                    scales, scratch, kNoAllocScratchBytes, stream_);
+}
