@@ -141,6 +141,8 @@ const char* tcg_last_error(void);
  * tcg_plan -- the launch plan tcg_gemm would use (for tests and tools).
  * out[0..9] = {BM, BN, BK, stages, splits, grid CTAs, cluster size,
  *              units of work, raster group, dynamic smem bytes}.
+ * units of work > tiles x splits when the last tiles are split over K to
+ * fill the last wave.
  * Needs the current device (queries SM count and shared-memory limit).
  */
 tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);

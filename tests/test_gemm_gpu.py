@@ -5,6 +5,8 @@ full-size workloads are compared on sampled full rows and full columns
 (edges, tile boundaries and random positions), which the oracle computes one
 element at a time.  Integer-valued inputs with fp32 D must match bit for bit.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -263,3 +265,35 @@ def test_planner_picks_pairs_for_large_square():
     pl = tcg.plan(8192, 8192, 8192)
     # at least 384 elements of K (six 128-byte atoms) in flight per CTA
     assert pl["cluster"] == 2 and pl["grid"] % 2 == 0 and pl["stages"] * pl["BK"] >= 384
+
+
+# ------------------------------------- tail split (last wave split over K)
+
+@pytest.mark.parametrize("force_cta2", [1, 2], ids=["pair", "one_cta"])
+def test_tail_split_integer_exact_and_deterministic(force_cta2):
+    # the tail split is opt-in (TCG_TAIL=1 in the environment of this process)
+    if os.environ.get("TCG_TAIL") != "1":
+        pytest.skip("tail split is enabled by TCG_TAIL=1 (read when the library loads)")
+    try:
+        tcg.debug_set(force_cta2=force_cta2)
+        M, N, K = 2048 + 17, 2560, 1024 + 40
+        pl = tcg.plan(M, N, K)
+        per = 256 if force_cta2 == 1 else 128
+        tiles = -(-M // per) * -(-N // 256)
+        if pl["units"] == tiles:
+            pytest.skip(f"planner did not split the tail on this device: {pl}")
+        case = inputs.make_case("tail", M, N, K, seed=191 + force_cta2, dist="int4", d_dtype="f32",
+                                opA="col", opB="col")
+        dc = check_full(case, exact=True)
+        first = dc.D_view.clone()
+        dc.run()
+        torch.cuda.synchronize()
+        assert torch.equal(first, dc.D_view)
+    finally:
+        tcg.debug_set()
+
+
+def test_tail_split_epilogue_bf16():
+    case = inputs.make_case("tail_epi", 2048, 2560 + 256, 1024, seed=201, dist="uniform", beta=0.5,
+                            c_dist="uniform", bias_std=0.1, act="gelu")
+    check_full(case)

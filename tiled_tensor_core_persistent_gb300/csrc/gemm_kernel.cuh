@@ -51,7 +51,11 @@ struct KernelParams {
     CUtensorMap tmD;
     int M, N, K;
     int num_m_blk, num_n_blk, num_kb;
+    // Units of work: phase A = units_a units over tiles [0, units_a / splits_a),
+    // each tile split into splits_a K ranges; phase B (the tail that would
+    // leave the last wave half empty) = the remaining tiles, split_b ways.
     int splits, num_units, group_m;
+    int units_a, splits_b;
     int a_mn_major, b_mn_major;
     float alpha, beta;
     const void* C;
@@ -65,8 +69,8 @@ struct KernelParams {
     long long ldd;
     int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
     int stages;
-    float* partials;      // split-K partial tiles [tile][split][kBM][BN]
-    int* tile_counters;   // split-K arrival counters [tile]
+    float* partials;      // split-K partials: [slot][kBM][BN], slot = (slot_tile + split) * ranks + rank
+    int* tile_counters;   // split-K arrival counters [tile * ranks + rank]
     int* status;          // [0] status, [1] where, [2] block
     long long timeout_ns;
     int fault_inject;
@@ -138,24 +142,58 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& m_blk, int& n_blk,
-                                            int& split, int& kb0, int& kb1, int& tile) {
-    tile = u / p.splits;
-    split = u - tile * p.splits;
+// Unit u -> output tile (m_blk, n_blk), K range [kb0, kb1) of its split out
+// of nsplit, and slot_tile, the first partial slot of the tile's splits.
+struct Unit {
+    int m_blk, n_blk, tile, split, nsplit, kb0, kb1, slot_tile;
+};
+
+__device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
+    Unit w;
+    if (u < p.units_a) {
+        w.tile = u / p.splits;
+        w.split = u - w.tile * p.splits;
+        w.nsplit = p.splits;
+        w.slot_tile = w.tile * p.splits;
+    } else {
+        const int v = u - p.units_a;
+        const int tiles_a = p.units_a / p.splits;
+        w.tile = tiles_a + v / p.splits_b;
+        w.split = v - (v / p.splits_b) * p.splits_b;
+        w.nsplit = p.splits_b;
+        w.slot_tile = (p.splits > 1 ? p.units_a : 0) + (v / p.splits_b) * p.splits_b;
+    }
     const int span = p.group_m * p.num_n_blk;
-    const int gid = tile / span;
+    const int gid = w.tile / span;
     const int first_m = gid * p.group_m;
     const int gsz = min(p.num_m_blk - first_m, p.group_m);
-    const int local = tile - gid * span;
-    m_blk = first_m + local % gsz;
-    n_blk = local / gsz;
-    kb0 = static_cast<int>((static_cast<long long>(split) * p.num_kb) / p.splits);
-    kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.num_kb) / p.splits);
+    const int local = w.tile - gid * span;
+    w.m_blk = first_m + local % gsz;
+    w.n_blk = local / gsz;
+    w.kb0 = static_cast<int>((static_cast<long long>(w.split) * p.num_kb) / w.nsplit);
+    w.kb1 = static_cast<int>((static_cast<long long>(w.split + 1) * p.num_kb) / w.nsplit);
+    return w;
 }
 
 
+// erf(z) for z >= 0 by Abramowitz & Stegun, Handbook of Mathematical
+// Functions, formula 7.1.26: 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
+// exp(-z^2), t = 1 / (1 + p z), |error| <= 1.5e-7; odd extension for z < 0.
+// Exact-erf GELU = 0.5 x (1 + erf(x / sqrt 2)).
 __device__ __forceinline__ float gelu_erf(float x) {
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+    const float z = x * 0.70710678118654752f;
+    const float a = fabsf(z);
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, a, 1.0f));
+    float q = fmaf(1.061405429f, t, -1.453152027f);
+    q = fmaf(q, t, 1.421413741f);
+    q = fmaf(q, t, -0.284496736f);
+    q = fmaf(q, t, 0.254829592f);
+    q *= t;
+    float e;  // exp(-a^2) = 2^(-a^2 log2 e)
+    asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-a * a * 1.44269504088896341f));
+    const float erf_z = copysignf(fmaf(-q, e, 1.0f), z);
+    const float hx = 0.5f * x;
+    return fmaf(hx, erf_z, hx);
 }
 
 __device__ __forceinline__ float apply_act(int act, float x) {
@@ -341,8 +379,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool first = true;
             bool ok = true;
             for (int u = first_unit; ok && u < p.num_units; u += unit_stride) {
-                int m_blk, n_blk, split, kb0, kb1, tile;
-                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
+                const Unit w = decode_unit(p, u);
+                const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1;
                 const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
                 const int b_row = n_blk * BN + static_cast<int>(rank) * kBRows;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -437,8 +475,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             long long st_full = 0, st_acc = 0;
             const long long st_t0 = p.stats ? clock64() : 0;
             for (int u = first_unit; ok && u < p.num_units; u += unit_stride, ++t) {
-                int m_blk, n_blk, split, kb0, kb1, tile;
-                decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
+                const Unit w = decode_unit(p, u);
+                const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1;
                 const int acc = t & 1;
                 const uint32_t acc_phase = (t >> 1) & 1;
                 const long long ta = p.stats ? clock64() : 0;
@@ -514,11 +552,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         int sb = 0;
         int t = 0;
         const bool has_c = p.beta != 0.0f;
-        const bool split_mode = p.splits > 1;
         long long st_ewait = 0, st_ebusy = 0;
         for (int u = first_unit; u < p.num_units; u += unit_stride, ++t) {
-            int m_blk, n_blk, split, kb0, kb1, tile;
-            decode_unit(p, u, m_blk, n_blk, split, kb0, kb1, tile);
+            const Unit w = decode_unit(p, u);
+            const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1, split = w.split;
+            const bool split_mode = w.nsplit > 1;
+            constexpr int kRanks = kCta2 ? 2 : 1;
+            const int counter = w.tile * kRanks + static_cast<int>(rank);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
             const long long te = p.stats ? clock64() : 0;
@@ -544,7 +584,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             if (split_mode) {
                 // Pass 1: this split's raw fp32 partial (valid rows only).
                 float* slot = p.partials +
-                              (static_cast<size_t>(tile) * p.splits + split) * (kBM * BN) +
+                              (static_cast<size_t>(w.slot_tile + split) * kRanks + rank) * (kBM * BN) +
                               static_cast<size_t>(row_in_tile) * BN;
                 if (warp_rows_live && have_acc) {
                     for (int j = 0; j < BN / kEpiChunk; ++j) {
@@ -564,9 +604,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 __threadfence();
                 ptx::named_barrier_sync(1, kEpiThreads);
                 if (threadIdx.x == kEpiWarp0 * 32) {
-                    const int old = atomicAdd(p.tile_counters + tile, 1);
-                    const int last = (old == p.splits - 1) ? 1 : 0;
-                    if (last) atomicExch(p.tile_counters + tile, 0);  // ready for the next launch
+                    const int old = atomicAdd(p.tile_counters + counter, 1);
+                    const int last = (old == w.nsplit - 1) ? 1 : 0;
+                    if (last) atomicExch(p.tile_counters + counter, 0);  // ready for the next launch
                     ctl->splitk_last = last;
                 }
                 ptx::named_barrier_sync(1, kEpiThreads);
@@ -591,7 +631,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             // depend on which split arrived last.
 #pragma unroll
                             for (int i = 0; i < 32; ++i) s[i] = 0.0f;
-                            for (int q = 0; q < p.splits; ++q) {
+                            for (int q = 0; q < w.nsplit; ++q) {
                                 if (q == split) {
                                     if (have_acc) {
 #pragma unroll
@@ -599,7 +639,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                     }
                                 } else if (row_ok) {
                                     const float4* src = reinterpret_cast<const float4*>(
-                                        p.partials + (static_cast<size_t>(tile) * p.splits + q) * (kBM * BN) +
+                                        p.partials + (static_cast<size_t>(w.slot_tile + q) * kRanks + rank) * (kBM * BN) +
                                         static_cast<size_t>(row_in_tile) * BN + j * kEpiChunk);
 #pragma unroll
                                     for (int c4 = 0; c4 < 8; ++c4) {

@@ -49,6 +49,9 @@ const int g_env_stages = env_int("TCG_STAGES");
 const int g_env_stats = env_int("TCG_STATS");
 // TCG_KATOMS = K atoms per stage for pair tiles (1 or 2; default 2).
 const int g_env_katoms = env_int("TCG_KATOMS");
+// TCG_TAIL=1 splits the tiles of a half-empty last wave over K.  Off by
+// default: measured slower on GB300 (4096^3: 102 -> 112 us).
+const int g_env_tail = env_int("TCG_TAIL");
 
 tcg_status fail_launch(const char* what, cudaError_t e) {
     char buf[512];
@@ -169,7 +172,10 @@ struct Plan {
     int smem = 0;
     int num_m = 0, num_n = 0, num_kb = 0;
     int cluster = 1;
-    int katoms = 1;  // 128-byte K atoms per pipeline stage
+    int katoms = 1;     // 128-byte K atoms per pipeline stage
+    int units_a = 0;    // units of the data-parallel phase (tiles x splits)
+    int tail_tiles = 0; // last tiles, split splits_b ways over K to fill the last wave
+    int splits_b = 1;
 };
 
 int stage_bytes(int bn, bool cta2, int katoms) {
@@ -214,7 +220,9 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
     pl.splits = splits;
-    pl.units = pl.num_m * pl.num_n * splits;
+    const int tiles = pl.num_m * pl.num_n;
+    pl.units_a = tiles * splits;
+    pl.units = pl.units_a;
     // Raster group (in M blocks) that keeps one wave's footprint of A rows
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
@@ -224,24 +232,44 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
     pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms);
+    int slots = dev.num_sms;  // units that run at once
     if (cta2) {
-        int pairs = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.katoms, pl.smem);
-        if (pairs <= 0) pairs = dev.num_sms / 2;
-        pl.grid = 2 * std::max(1, std::min(pl.units, pairs));
-    } else {
-        pl.grid = std::max(1, std::min(pl.units, dev.num_sms));
+        slots = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.katoms, pl.smem);
+        if (slots <= 0) slots = dev.num_sms / 2;
     }
+    // When the tiles leave the last wave at most half full, split those last
+    // tiles over K so their pieces fill it (the rest stays data-parallel).
+    if (splits == 1 && g_env_tail && g_force_splits == 0 && tiles > slots) {
+        const int rem = tiles % slots;
+        if (rem > 0 && 2 * rem <= slots) {
+            const int sb = std::min(std::min(slots / rem, 4), pl.num_kb / 2);
+            if (sb >= 2) {
+                pl.tail_tiles = rem;
+                pl.splits_b = sb;
+                pl.units_a = tiles - rem;
+                pl.units = pl.units_a + rem * sb;
+            }
+        }
+    }
+    pl.grid = (cta2 ? 2 : 1) * std::max(1, std::min(pl.units, slots));
     return pl;
 }
 
+size_t partial_slots(const Plan& pl) {
+    const size_t a = pl.splits > 1 ? static_cast<size_t>(pl.units_a) : 0;
+    const size_t b = pl.splits_b > 1 ? static_cast<size_t>(pl.tail_tiles) * pl.splits_b : 0;
+    return (a + b) * static_cast<size_t>(pl.cluster);
+}
+
+bool any_split(const Plan& pl) { return pl.splits > 1 || pl.splits_b > 1; }
+
 size_t partial_bytes(const Plan& pl) {
-    if (pl.splits <= 1) return 0;
-    return static_cast<size_t>(pl.num_m) * pl.num_n * pl.splits * tcg::kBM * pl.bn * sizeof(float);
+    return partial_slots(pl) * tcg::kBM * pl.bn * sizeof(float);
 }
 
 size_t counter_bytes(const Plan& pl) {
-    if (pl.splits <= 1) return 0;
-    return (static_cast<size_t>(pl.num_m) * pl.num_n * sizeof(int) + 255) / 256 * 256;
+    if (!any_split(pl)) return 0;
+    return (static_cast<size_t>(pl.num_m) * pl.num_n * pl.cluster * sizeof(int) + 255) / 256 * 256;
 }
 
 template <int BN, bool kFp8, bool kCta2, int KA>
@@ -454,6 +482,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.M = M; kp.N = N; kp.K = K;
     kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
     kp.splits = pl.splits; kp.num_units = pl.units; kp.group_m = pl.group_m;
+    kp.units_a = pl.units_a; kp.splits_b = pl.splits_b;
     kp.a_mn_major = (opA == TCG_COL); kp.b_mn_major = (opB == TCG_ROW);
     kp.alpha = alpha * scales.scale_a * scales.scale_b;
     kp.beta = beta;
@@ -470,8 +499,8 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stages = pl.stages;
     char* ws = static_cast<char*>(workspace);
     kp.status = reinterpret_cast<int*>(ws);
-    kp.tile_counters = pl.splits > 1 ? reinterpret_cast<int*>(ws + kHeaderBytes) : nullptr;
-    kp.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + kHeaderBytes + counter_bytes(pl)) : nullptr;
+    kp.tile_counters = any_split(pl) ? reinterpret_cast<int*>(ws + kHeaderBytes) : nullptr;
+    kp.partials = any_split(pl) ? reinterpret_cast<float*>(ws + kHeaderBytes + counter_bytes(pl)) : nullptr;
     kp.timeout_ns = g_timeout_ns > 0 ? g_timeout_ns : kDefaultTimeoutNs;
     kp.fault_inject = g_fault_inject;
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
