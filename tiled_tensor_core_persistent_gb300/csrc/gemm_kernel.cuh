@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const long long st_t0 = p.stats ? clock64() : 0;
             for (int u = first_unit; ok && u < p.num_units; u += unit_stride, ++t) {
                 const Unit w = decode_unit(p, u);
-                const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1;
+                const int kb0 = w.kb0, kb1 = w.kb1;
                 const int acc = t & 1;
                 const uint32_t acc_phase = (t >> 1) & 1;
                 const long long ta = p.stats ? clock64() : 0;
