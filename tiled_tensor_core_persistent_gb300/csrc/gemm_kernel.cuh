@@ -69,7 +69,7 @@ struct KernelParams {
     long long ldd;
     int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
     int stages;
-    float* partials;      // split-K partials: [slot][kBM][BN], slot = (slot_tile + split) * ranks + rank
+    float* partials;      // split-K partials: [slot][BN][kBM] (row fastest), slot = (slot_tile + split) * ranks + rank
     int* tile_counters;   // split-K arrival counters [tile * ranks + rank]
     int* status;          // [0] status, [1] where, [2] block
     long long timeout_ns;
@@ -583,20 +583,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool finish = true;
             if (split_mode) {
                 // Pass 1: this split's raw fp32 partial (valid rows only).
+                // Column-major within the tile: the 32 rows of a warp form one
+                // contiguous 128-byte line per column (coalesced stores/loads).
                 float* slot = p.partials +
                               (static_cast<size_t>(w.slot_tile + split) * kRanks + rank) * (kBM * BN) +
-                              static_cast<size_t>(row_in_tile) * BN;
+                              row_in_tile;
                 if (warp_rows_live && have_acc) {
                     for (int j = 0; j < BN / kEpiChunk; ++j) {
                         if (n0 + j * kEpiChunk >= p.N) break;
                         uint32_t r[32];
                         ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
                         if (row_ok) {
-                            float4* dst = reinterpret_cast<float4*>(slot + j * kEpiChunk);
+                            float* dst = slot + static_cast<size_t>(j * kEpiChunk) * kBM;
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                            for (int i = 0; i < 32; ++i) dst[i * kBM] = __uint_as_float(r[i]);
                         }
                     }
                 }
@@ -638,15 +638,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                         for (int i = 0; i < 32; ++i) s[i] += __uint_as_float(r[i]);
                                     }
                                 } else if (row_ok) {
-                                    const float4* src = reinterpret_cast<const float4*>(
+                                    const float* src =
                                         p.partials + (static_cast<size_t>(w.slot_tile + q) * kRanks + rank) * (kBM * BN) +
-                                        static_cast<size_t>(row_in_tile) * BN + j * kEpiChunk);
+                                        static_cast<size_t>(j * kEpiChunk) * kBM + row_in_tile;
+                                    float pv[32];
 #pragma unroll
-                                    for (int c4 = 0; c4 < 8; ++c4) {
-                                        const float4 w = __ldcg(src + c4);
-                                        s[4 * c4 + 0] += w.x; s[4 * c4 + 1] += w.y;
-                                        s[4 * c4 + 2] += w.z; s[4 * c4 + 3] += w.w;
-                                    }
+                                    for (int i = 0; i < 32; ++i) pv[i] = __ldcg(src + i * kBM);
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) s[i] += pv[i];
                                 }
                             }
                         }
