@@ -244,6 +244,50 @@ __device__ __forceinline__ void load_row32(const void* base, int is_f32, int col
     }
 }
 
+// C prefetch: the raw 16-byte vectors of one thread's 32-column C chunk are
+// loaded one chunk ahead (and the first chunk before the accumulator is
+// ready), so the load latency hides behind the TMEM read and the math.
+// Full chunks only; a ragged last chunk is loaded element-wise when used.
+__device__ __forceinline__ void c_prefetch(const KernelParams& p, int row, int col0, uint4 (&q)[8]) {
+    if (col0 + 32 > p.N) return;
+    const int eb = p.c_f32 ? 4 : 2;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.C) +
+                                                      (static_cast<long long>(row) * p.ldc + col0) * eb);
+    if (p.c_f32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = src[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = src[i];
+    }
+}
+
+__device__ __forceinline__ void c_values(const KernelParams& p, int row, int col0, const uint4 (&q)[8],
+                                         float (&c)[32]) {
+    if (col0 + 32 > p.N) {
+        const char* crow = static_cast<const char*>(p.C) + static_cast<long long>(row) * p.ldc * (p.c_f32 ? 4 : 2);
+        load_row32(crow, p.c_f32, col0, p.N, c);
+        return;
+    }
+    if (p.c_f32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[4 * i + 0] = __uint_as_float(q[i].x); c[4 * i + 1] = __uint_as_float(q[i].y);
+            c[4 * i + 2] = __uint_as_float(q[i].z); c[4 * i + 3] = __uint_as_float(q[i].w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t wv[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                c[8 * i + 2 * h + 0] = bf16_bits_to_float(wv[h] & 0xFFFFu);
+                c[8 * i + 2 * h + 1] = bf16_bits_to_float(wv[h] >> 16);
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -561,6 +605,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const int counter = w.tile * kRanks + static_cast<int>(rank);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
+            uint4 cq[8];
+            {
+                const int pre_row = m_blk * kTileM + static_cast<int>(rank) * kBM + (warp & 3) * 32 + lane;
+                if (has_c && pre_row < p.M && n_blk * BN < p.N) c_prefetch(p, pre_row, n_blk * BN, cq);
+            }
             const long long te = p.stats ? clock64() : 0;
             bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
             const long long te1 = p.stats ? clock64() : 0;
@@ -657,9 +706,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     }
                     if (has_c && row_ok) {
                         float c[32];
-                        const char* crow = static_cast<const char*>(p.C) +
-                                           static_cast<long long>(grow) * p.ldc * (p.c_f32 ? 4 : 2);
-                        load_row32(crow, p.c_f32, col0, p.N, c);
+                        c_values(p, grow, col0, cq, c);
+                        if (col0 + kEpiChunk < p.N && j + 1 < BN / kEpiChunk) c_prefetch(p, grow, col0 + kEpiChunk, cq);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, c[i], v[i]);
                     }
