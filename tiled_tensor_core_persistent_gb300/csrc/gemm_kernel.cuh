@@ -357,6 +357,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kKSteps = kBK / kMmaK;               // MMAs per atom
     constexpr int kAtom = kRowBytes / kElemBytes;      // MN elements per swizzle row
     constexpr int kBRows = kCta2 ? BN / 2 : BN;        // B rows (N) this CTA loads
+    // MN-major B boxes are whole 128-byte MN atoms (e4m3 operands are K-major only)
+    static_assert(kFp8 || kBRows % kAtom == 0, "B rows per CTA must be whole 128-byte MN atoms");
     constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;

@@ -52,6 +52,8 @@ const int g_env_katoms = env_int("TCG_KATOMS");
 // TCG_TAIL=1 splits the tiles of a half-empty last wave over K.  Off by
 // default: measured slower on GB300 (4096^3: 102 -> 112 us).
 const int g_env_tail = env_int("TCG_TAIL");
+// TCG_NARROW=0 keeps 128/256-wide tiles for small problems (default: narrow them).
+const int g_env_narrow = getenv("TCG_NARROW") ? env_int("TCG_NARROW") : 1;
 
 tcg_status fail_launch(const char* what, cudaError_t e) {
     char buf[512];
@@ -196,6 +198,14 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     // heuristic works on single-atom k-blocks.
     pl.num_kb = (K + bk - 1) / bk;
     const int num_m1 = (M + tcg::kBM - 1) / tcg::kBM;
+    // Short K (too short to split): narrower tiles (down to 128 x 64, one full
+    // 128-byte MN atom, so an MN-major B box still fits its stage) while the
+    // tiles would fill less than half of the SMs.  Measured on GB300: 512^3
+    // 12.4 -> 10.3 us; for long K, split-K beats narrowing (16x8192x8192:
+    // 49 vs 60 us).
+    if (g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && pl.num_kb < 16) {
+        while (pl.bn > 64 && num_m1 * ((N + pl.bn - 1) / pl.bn) * 2 < dev.num_sms) pl.bn /= 2;
+    }
     const int num_n = (N + pl.bn - 1) / pl.bn;
     const int tiles1 = num_m1 * num_n;
     // Split K only when the output tiles cannot fill the machine and each
@@ -512,10 +522,17 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     if (pl.cluster == 2)
         return fp8 ? launch_kernel<256, true, true, 1>(kp, pl, stream)
                    : launch_kernel<256, false, true, 1>(kp, pl, stream);
-    if (pl.bn == 256)
-        return fp8 ? launch_kernel<256, true, false, 1>(kp, pl, stream)
-                   : launch_kernel<256, false, false, 1>(kp, pl, stream);
-    return fp8 ? launch_kernel<128, true, false, 1>(kp, pl, stream) : launch_kernel<128, false, false, 1>(kp, pl, stream);
+    switch (pl.bn) {
+        case 256:
+            return fp8 ? launch_kernel<256, true, false, 1>(kp, pl, stream)
+                       : launch_kernel<256, false, false, 1>(kp, pl, stream);
+        case 128:
+            return fp8 ? launch_kernel<128, true, false, 1>(kp, pl, stream)
+                       : launch_kernel<128, false, false, 1>(kp, pl, stream);
+        default:
+            return fp8 ? launch_kernel<64, true, false, 1>(kp, pl, stream)
+                       : launch_kernel<64, false, false, 1>(kp, pl, stream);
+    }
 }
 
 tcg_status tcg_device_status(void* workspace, void* stream_) {
