@@ -196,6 +196,30 @@ __device__ __forceinline__ float gelu_erf(float x) {
     return fmaf(hx, erf_z, hx);
 }
 
+// The same GELU on a packed pair of fp32 values: the polynomial and the
+// linear steps run as f32x2 instructions, the reciprocal and 2^x per lane.
+__device__ __forceinline__ uint64_t gelu_erf2(uint64_t x) {
+    constexpr uint64_t kSign = 0x8000000080000000ull;
+    auto splat = [](float f) { return ptx::pack2(f, f); };
+    const uint64_t z = ptx::mul2(x, splat(0.70710678118654752f));
+    const uint64_t a = z & ~kSign;
+    float d0, d1;
+    ptx::unpack2(ptx::fma2(splat(0.3275911f), a, splat(1.0f)), d0, d1);
+    const uint64_t t = ptx::pack2(ptx::rcp_approx(d0), ptx::rcp_approx(d1));
+    uint64_t q = ptx::fma2(splat(1.061405429f), t, splat(-1.453152027f));
+    q = ptx::fma2(q, t, splat(1.421413741f));
+    q = ptx::fma2(q, t, splat(-0.284496736f));
+    q = ptx::fma2(q, t, splat(0.254829592f));
+    q = ptx::mul2(q, t);
+    float m0, m1;
+    ptx::unpack2(ptx::mul2(ptx::mul2(a, a), splat(-1.44269504088896341f)), m0, m1);
+    const uint64_t e = ptx::pack2(ptx::ex2_approx(m0), ptx::ex2_approx(m1));
+    const uint64_t erf_abs = ptx::fma2(q ^ kSign, e, splat(1.0f));
+    const uint64_t erf_z = erf_abs | (z & kSign);
+    const uint64_t hx = ptx::mul2(x, splat(0.5f));
+    return ptx::fma2(hx, erf_z, hx);
+}
+
 __device__ __forceinline__ float apply_act(int act, float x) {
     if (act == 1) return x > 0.0f ? x : 0.0f;
     if (act == 2) return gelu_erf(x);
@@ -701,27 +725,43 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             }
                         }
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = p.alpha * s[i];
+                        for (int i = 0; i < 32; ++i) v[i] = s[i];
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+                    // alpha, beta*C, bias and GELU on packed pairs (f32x2)
+                    uint64_t v2[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v2[i] = ptx::pack2(v[2 * i], v[2 * i + 1]);
+                    if (p.alpha != 1.0f) {
+                        const uint64_t al = ptx::pack2(p.alpha, p.alpha);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], al);
                     }
                     if (has_c && row_ok) {
                         float c[32];
                         c_values(p, grow, col0, cq, c);
                         if (col0 + kEpiChunk < p.N && j + 1 < BN / kEpiChunk) c_prefetch(p, grow, col0 + kEpiChunk, cq);
+                        const uint64_t be = ptx::pack2(p.beta, p.beta);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, c[i], v[i]);
+                        for (int i = 0; i < 16; ++i) v2[i] = ptx::fma2(be, ptx::pack2(c[2 * i], c[2 * i + 1]), v2[i]);
                     }
                     if (p.bias) {
                         float b[32];
                         load_row32(p.bias, p.bias_f32, col0, p.N, b);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += b[i];
+                        for (int i = 0; i < 16; ++i) v2[i] = ptx::add2(v2[i], ptx::pack2(b[2 * i], b[2 * i + 1]));
                     }
-                    if (p.act) {
+                    if (p.act == 2) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = apply_act(p.act, v[i]);
+                        for (int i = 0; i < 16; ++i) v2[i] = gelu_erf2(v2[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ptx::unpack2(v2[i], v[2 * i], v[2 * i + 1]);
+                    if (p.act == 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = apply_act(1, v[i]);
                     }
                     if (col0 + kEpiChunk <= p.N || p.d_inner_aligned) {
                         // The staging buffer is free once its previous store has read it.
