@@ -29,7 +29,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_OUT_DIR, "libgemm_oracle.so")
 
 ROW, COL = 0, 1
-BF16, E4M3, F32 = 0, 1, 2
+BF16, E4M3, F32, F16, E5M2 = 0, 1, 2, 3, 4
 ACT = {"none": 0, "relu": 1, "gelu": 2}
 
 _lock = threading.Lock()
@@ -65,6 +65,10 @@ def _load():
         lib.oracle_gemm_full.restype = i64
         lib.oracle_decode_bf16_array.argtypes = [P, P, i64]
         lib.oracle_decode_e4m3_array.argtypes = [P, P, i64]
+        lib.oracle_decode_f16_array.argtypes = [P, P, i64]
+        lib.oracle_decode_e5m2_array.argtypes = [P, P, i64]
+        lib.oracle_set_channel_scales.argtypes = [P, P]
+        lib.oracle_set_channel_scales.restype = None
         lib.oracle_act_array.argtypes = [i32, P, P, i64]
         _lib = lib
         return lib
@@ -74,11 +78,14 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _storage(x):
-    """Raw storage of an operand: uint16 (bf16 bits), uint8 (e4m3 bits) or float32."""
+def _storage(x, dtype=None):
+    """Raw storage of an operand: uint16 (bf16 bits), uint8 (e4m3 bits) or float32;
+    `dtype` (BF16 / E4M3 / F32 / F16 / E5M2) overrides the guess from the array type."""
     if x is None:
         return None, None
     x = np.ascontiguousarray(x)
+    if dtype is not None:
+        return x, int(dtype)
     if x.dtype == np.uint16:
         return x, BF16
     if x.dtype == np.uint8:
@@ -98,18 +105,21 @@ class Problem:
     """
 
     def __init__(self, M, N, K, A, lda, opA, B, ldb, opB, alpha=1.0, beta=0.0,
-                 C=None, ldc=0, bias=None, act="none", scale_a=1.0, scale_b=1.0):
+                 C=None, ldc=0, bias=None, act="none", scale_a=1.0, scale_b=1.0,
+                 ab_dtype=None, c_dtype=None, bias_dtype=None, row_scale=None, col_scale=None):
         self.M, self.N, self.K = int(M), int(N), int(K)
-        self.A, ab = _storage(A)
-        self.B, ab2 = _storage(B)
+        self.A, ab = _storage(A, ab_dtype)
+        self.B, ab2 = _storage(B, ab_dtype)
         if ab is not None and ab2 is not None and ab != ab2:
             raise TypeError("A and B must share a storage type")
         self.ab_dtype = ab if ab is not None else BF16
         self.lda, self.ldb, self.opA, self.opB = int(lda), int(ldb), int(opA), int(opB)
         self.alpha, self.beta = float(alpha), float(beta)
-        self.C, self.c_dtype = _storage(C)
+        self.C, self.c_dtype = _storage(C, c_dtype)
         self.ldc = int(ldc)
-        self.bias, self.bias_dtype = _storage(bias)
+        self.bias, self.bias_dtype = _storage(bias, bias_dtype)
+        self.row_scale = None if row_scale is None else np.ascontiguousarray(row_scale, dtype=np.float32)
+        self.col_scale = None if col_scale is None else np.ascontiguousarray(col_scale, dtype=np.float32)
         self.act = ACT[act] if isinstance(act, str) else int(act)
         self.scale_a, self.scale_b = float(scale_a), float(scale_b)
 
@@ -120,8 +130,12 @@ class Problem:
                 _ptr(self.bias), self.bias_dtype if self.bias_dtype is not None else BF16,
                 self.act, self.scale_a, self.scale_b)
 
+    def _scales(self):
+        _load().oracle_set_channel_scales(_ptr(self.row_scale), _ptr(self.col_scale))
+
     def full(self, nthreads: int = 0) -> np.ndarray:
         out = np.empty((self.M, self.N), dtype=np.float64)
+        self._scales()
         n = _load().oracle_gemm_full(*self._args(), _ptr(out), int(nthreads), 0, None, None)
         if n < 0:
             raise MemoryError("oracle allocation failed")
@@ -131,6 +145,7 @@ class Problem:
         """Run the full GEMM single-threaded with the per-operation counter on."""
         out = np.empty((self.M, self.N), dtype=np.float64)
         n_mul, n_add = ctypes.c_longlong(0), ctypes.c_longlong(0)
+        self._scales()
         _load().oracle_gemm_full(*self._args(), _ptr(out), 1, 1,
                                  ctypes.byref(n_mul), ctypes.byref(n_add))
         return out, n_mul.value, n_add.value
@@ -139,6 +154,7 @@ class Problem:
         rows = np.ascontiguousarray(rows, dtype=np.int32)
         cols = np.ascontiguousarray(cols, dtype=np.int32)
         out = np.empty((rows.size, cols.size), dtype=np.float64)
+        self._scales()
         n = _load().oracle_gemm_select(*self._args(), _ptr(rows), int(rows.size),
                                        _ptr(cols), int(cols.size), _ptr(out), int(nthreads))
         if n < 0:
@@ -157,6 +173,20 @@ def decode_e4m3(bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint8)
     out = np.empty(bits.shape, dtype=np.float64)
     _load().oracle_decode_e4m3_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def decode_f16(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode_f16_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def decode_e5m2(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode_e5m2_array(_ptr(bits), _ptr(out), bits.size)
     return out
 
 

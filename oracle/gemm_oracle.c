@@ -20,6 +20,10 @@
  *     fused into the epilogue): the bias is added before the activation, and
  *     the FP8 per-tensor scales sA, sB multiply the raw sum.
  *
+ * The FP8 per-tensor scales may be refined by optional per-row (i) and
+ * per-column (j) fp32 scale vectors, multiplying the raw sum the same way
+ * (the per-channel dequantisation scale of the same Stage 5 paragraph).
+ *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - bias is indexed by the output column j and added before act;
  *   - GELU is the exact erf form 0.5*x*(1+erf(x/sqrt(2)));
@@ -42,7 +46,7 @@
 #include <unistd.h>
 
 enum { OR_ROW = 0, OR_COL = 1 };
-enum { OR_BF16 = 0, OR_E4M3 = 1, OR_F32 = 2 };
+enum { OR_BF16 = 0, OR_E4M3 = 1, OR_F32 = 2, OR_F16 = 3, OR_E5M2 = 4 };
 enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_GELU = 2 };
 
 /* ------------------------------------------------------------------------ */
@@ -86,6 +90,42 @@ double oracle_decode_e4m3(uint8_t bits) {
     return s ? -v : v;
 }
 
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal: (-1)^s 2^(e-15) (1 + f/1024); subnormal: (-1)^s 2^(-14) (f/1024);
+ * e = 31: infinity (f = 0) or NaN. */
+double oracle_decode_f16(uint16_t bits) {
+    int s = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1F;
+    int f = bits & 0x3FF;
+    double v;
+    if (e == 0x1F) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f / 1024.0, -14);
+    } else {
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
+/* float8 e5m2 (FP8 formats paper): 1 sign, 5 exponent bits (bias 15), 2
+ * fraction bits, IEEE-like specials: e = 31 is infinity (f = 0) or NaN;
+ * subnormal (e = 0): (-1)^s 2^(-14) (f/4); largest finite value 57344. */
+double oracle_decode_e5m2(uint8_t bits) {
+    int s = (bits >> 7) & 1;
+    int e = (bits >> 2) & 0x1F;
+    int f = bits & 0x3;
+    double v;
+    if (e == 0x1F) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f / 4.0, -14);
+    } else {
+        v = ldexp(1.0 + (double)f / 4.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
 /* IEEE binary32, decoded through its bits for the same reason. */
 static double decode_f32(const void* p) {
     float x;
@@ -94,12 +134,16 @@ static double decode_f32(const void* p) {
 }
 
 static double g_bf16_table[65536];
+static double g_f16_table[65536];
 static double g_e4m3_table[256];
+static double g_e5m2_table[256];
 static pthread_once_t g_tables_once = PTHREAD_ONCE_INIT;
 
 static void build_tables(void) {
     for (int i = 0; i < 65536; ++i) g_bf16_table[i] = oracle_decode_bf16((uint16_t)i);
+    for (int i = 0; i < 65536; ++i) g_f16_table[i] = oracle_decode_f16((uint16_t)i);
     for (int i = 0; i < 256; ++i) g_e4m3_table[i] = oracle_decode_e4m3((uint8_t)i);
+    for (int i = 0; i < 256; ++i) g_e5m2_table[i] = oracle_decode_e5m2((uint8_t)i);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -130,18 +174,26 @@ typedef struct {
     const void* C; long long ldc; int c_dtype;
     const void* bias; int bias_dtype;
     int act;
+    /* optional per-row (length M) and per-column (length N) fp32 scales */
+    const float* row_scale;
+    const float* col_scale;
     /* optional instrumented operation counter (tiny problems only) */
     int count_ops;
 } oracle_problem;
 
 static double load_ab(const void* base, int dtype, long long idx) {
-    if (dtype == OR_E4M3) return g_e4m3_table[((const uint8_t*)base)[idx]];
-    if (dtype == OR_F32) return decode_f32((const float*)base + idx);
-    return g_bf16_table[((const uint16_t*)base)[idx]];
+    switch (dtype) {
+    case OR_E4M3: return g_e4m3_table[((const uint8_t*)base)[idx]];
+    case OR_E5M2: return g_e5m2_table[((const uint8_t*)base)[idx]];
+    case OR_F16: return g_f16_table[((const uint16_t*)base)[idx]];
+    case OR_F32: return decode_f32((const float*)base + idx);
+    default: return g_bf16_table[((const uint16_t*)base)[idx]];
+    }
 }
 
 static double load_vec(const void* base, int dtype, long long idx) {
     if (dtype == OR_F32) return decode_f32((const float*)base + idx);
+    if (dtype == OR_F16) return g_f16_table[((const uint16_t*)base)[idx]];
     return g_bf16_table[((const uint16_t*)base)[idx]];
 }
 
@@ -162,7 +214,10 @@ static double element(const oracle_problem* p, int i, int j, long long* n_mul, l
         s = s + a * b;
         if (p->count_ops) { ++*n_mul; ++*n_add; }
     }
-    double d = p->alpha * p->scale_a * p->scale_b * s;
+    double scale = p->alpha * p->scale_a * p->scale_b;
+    if (p->row_scale) scale *= decode_f32(p->row_scale + i);
+    if (p->col_scale) scale *= decode_f32(p->col_scale + j);
+    double d = scale * s;
     if (p->beta != 0.0) d += p->beta * load_vec(p->C, p->c_dtype, (long long)i * p->ldc + j);
     if (p->bias) d += load_vec(p->bias, p->bias_dtype, j);
     return oracle_act(p->act, d);
@@ -250,6 +305,15 @@ static oracle_problem make_problem(PROBLEM_ARGS) {
     return p;
 }
 
+/* Per-row / per-column dequantisation scales for the next oracle_gemm_*
+ * call on this thread (NULL = none).  The vectors are fp32, length M and N. */
+static _Thread_local const float* g_row_scale = NULL;
+static _Thread_local const float* g_col_scale = NULL;
+void oracle_set_channel_scales(const float* row_scale, const float* col_scale) {
+    g_row_scale = row_scale;
+    g_col_scale = col_scale;
+}
+
 /* Selected rows x selected columns of D_ref, written to out (nrows x ncols).
  * Returns the number of elements computed, or -1 on allocation failure. */
 long long oracle_gemm_select(PROBLEM_ARGS, const int* rows, int nrows,
@@ -257,6 +321,8 @@ long long oracle_gemm_select(PROBLEM_ARGS, const int* rows, int nrows,
     oracle_problem p = make_problem(M, N, K, alpha, A, lda, opA, B, ldb, opB, ab_dtype,
                                     beta, C, ldc, c_dtype, bias, bias_dtype, act,
                                     scale_a, scale_b);
+    p.row_scale = g_row_scale;
+    p.col_scale = g_col_scale;
     return run_positions(&p, rows, nrows, cols, ncols, out, nthreads, NULL, NULL);
 }
 
@@ -269,6 +335,8 @@ long long oracle_gemm_full(PROBLEM_ARGS, double* out, int nthreads, int count_op
                                     beta, C, ldc, c_dtype, bias, bias_dtype, act,
                                     scale_a, scale_b);
     p.count_ops = count_ops;
+    p.row_scale = g_row_scale;
+    p.col_scale = g_col_scale;
     int* rows = (int*)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
     int* cols = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
     if (!rows || !cols) { free(rows); free(cols); return -1; }
@@ -285,6 +353,12 @@ void oracle_decode_bf16_array(const uint16_t* in, double* out, long long n) {
 }
 void oracle_decode_e4m3_array(const uint8_t* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e4m3(in[i]);
+}
+void oracle_decode_f16_array(const uint16_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_f16(in[i]);
+}
+void oracle_decode_e5m2_array(const uint8_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e5m2(in[i]);
 }
 void oracle_act_array(int act, const double* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_act(act, in[i]);

@@ -288,3 +288,68 @@ def test_input_generator_recipes():
     f = inputs.make_case("f8", 8, 8, 32, seed=2, dist="normal", ab_dtype="e4m3")
     assert f.A.dtype == torch.float8_e4m3fn
     assert float(f.A.to(torch.float32)[:, :32].abs().max()) == 448.0
+
+
+# ------------------------------------------- fp16 / e5m2 and channel scales
+
+def test_f16_decoder_exhaustive_against_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.decode_f16(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.float16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e5m2_decoder_exhaustive_against_torch():
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ours = oracle.decode_e5m2(bits)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 6  # exponent 31 with a non-zero fraction, both signs
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.nanmax(ours[np.isfinite(ours)]) == 57344.0
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 4, 5), (6, 2, 7)])
+def test_f16_tiny_exact_rational(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a = torch.from_numpy(rng.uniform(-3, 3, (M, K)).astype(np.float32)).to(torch.float16)
+    b = torch.from_numpy(rng.uniform(-3, 3, (N, K)).astype(np.float32)).to(torch.float16)
+    a_bits = a.view(torch.int16).numpy().view(np.uint16)
+    b_bits = b.view(torch.int16).numpy().view(np.uint16)
+    got = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL, ab_dtype=oracle.F16).full(1)
+    av, bv = a.double().numpy(), b.double().numpy()
+    for i in range(M):
+        for j in range(N):
+            ref = sum((Fraction(av[i, k]) * Fraction(bv[j, k]) for k in range(K)), Fraction(0))
+            assert got[i, j] == float(ref)
+
+
+def test_e5m2_matches_numpy_on_decoded_values():
+    M, N, K = 9, 7, 64
+    rng = np.random.default_rng(12)
+    qa = torch.from_numpy(rng.uniform(-100, 100, (M, K)).astype(np.float32)).to(torch.float8_e5m2)
+    qb = torch.from_numpy(rng.uniform(-100, 100, (N, K)).astype(np.float32)).to(torch.float8_e5m2)
+    got = oracle.Problem(M, N, K, qa.view(torch.uint8).numpy(), K, oracle.ROW, qb.view(torch.uint8).numpy(), K,
+                         oracle.COL, ab_dtype=oracle.E5M2, scale_a=0.5, scale_b=0.25).full()
+    ref = 0.125 * (qa.double().numpy() @ qb.double().numpy().T)
+    np.testing.assert_allclose(got, ref, rtol=1e-13)
+
+
+def test_channel_scales_are_row_and_column_factors():
+    """Per-row and per-column scales multiply element (i, j) by r_i * c_j (indices not swapped)."""
+    M, N, K = 5, 8, 24
+    rng = np.random.default_rng(13)
+    a_bits = bf16_bits(rng.uniform(-1, 1, (M, K)))
+    b_bits = bf16_bits(rng.uniform(-1, 1, (N, K)))
+    r = np.arange(1, M + 1, dtype=np.float32) * 0.5
+    c = np.arange(1, N + 1, dtype=np.float32) * 0.25 + 1.0
+    base = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL).full()
+    scaled = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL,
+                            row_scale=r, col_scale=c).full()
+    np.testing.assert_allclose(scaled, base * r[:, None] * c[None, :], rtol=1e-13)
+    only_rows = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL, row_scale=r).full()
+    np.testing.assert_allclose(only_rows, base * r[:, None], rtol=1e-13)
