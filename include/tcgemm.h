@@ -56,7 +56,9 @@ typedef enum {
 
 typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
 
-typedef enum { TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2 } tcg_dtype;
+/* Operands A and B: BF16, F16, E4M3 or E5M2 (both the same).  C, D and bias:
+ * BF16 or F32.  E4M3 / E5M2 are the FP8 formats (e4m3 without infinities). */
+typedef enum { TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2, TCG_F16 = 3, TCG_E5M2 = 4 } tcg_dtype;
 
 typedef enum { TCG_ACT_NONE = 0, TCG_ACT_RELU = 1, TCG_ACT_GELU = 2 } tcg_act;
 
@@ -69,18 +71,25 @@ typedef struct {
     tcg_act act;
 } tcg_epilogue;
 
-/* Per-tensor dequantisation scales for e4m3 operands (use 1.0 for bf16):
- * the raw product sum is multiplied by alpha * scale_a * scale_b. */
+/* Dequantisation scales (CUTLASS page, Part IV Stage 5: a per-channel scale
+ * fused into the epilogue).  The raw product sum of element (i, j) is
+ * multiplied by alpha * scale_a * scale_b * row_scale[i] * col_scale[j].
+ * scale_a / scale_b: per-tensor (1.0 when unused).  row_scale: NULL or a
+ * device vector of M fp32 values (4-byte aligned); col_scale: NULL or a
+ * device vector of N fp32 values (16-byte aligned).  Any operand type. */
 typedef struct {
     float scale_a;
     float scale_b;
+    const float* row_scale;
+    const float* col_scale;
 } tcg_scales;
 
 /*
  * tcg_can_implement -- argument validation only (no GPU access, no launch).
  *   M, N, K        : problem size, >= 0.
- *   ab_dtype       : TCG_BF16 or TCG_E4M3 (A and B share it).  E4M3 requires
- *                    opA = TCG_ROW and opB = TCG_COL (both K-contiguous).
+ *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3 or TCG_E5M2 (A and B share
+ *                    it).  The 8-bit types require opA = TCG_ROW and
+ *                    opB = TCG_COL (both K-contiguous).
  *   A, lda, opA    : operand A; lda >= K (ROW) or >= M (COL).
  *   B, ldb, opB    : operand B; ldb >= N (ROW) or >= K (COL).
  *   has_c, C, ldc, c_dtype : has_c != 0 when beta != 0; then C row-major,

@@ -8,7 +8,10 @@ from tiled_tensor_core_persistent_gb300 import inputs
 
 # Tolerances of the comparison |D - D_ref| <= tol * max(1, |D_ref|):
 # 1e-2 for bf16 operands, 5e-2 for e4m3 operands with per-tensor scales.
-TOL = {"bf16": 1e-2, "e4m3": 5e-2}
+TOL = {"bf16": 1e-2, "f16": 1e-2, "e4m3": 5e-2, "e5m2": 5e-2}
+
+_AB = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+_VEC = {"bf16": oracle.BF16, "f32": oracle.F32}
 
 
 def oracle_for(case: inputs.GemmCase) -> oracle.Problem:
@@ -17,7 +20,11 @@ def oracle_for(case: inputs.GemmCase) -> oracle.Problem:
         oracle.ROW if case.opA == "row" else oracle.COL,
         inputs.raw_bits(case.B), case.ldb, oracle.ROW if case.opB == "row" else oracle.COL,
         alpha=case.alpha, beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
-        bias=inputs.raw_bits(case.bias), act=case.act, scale_a=case.scale_a, scale_b=case.scale_b)
+        bias=inputs.raw_bits(case.bias), act=case.act, scale_a=case.scale_a, scale_b=case.scale_b,
+        ab_dtype=_AB[case.ab_dtype], c_dtype=_VEC[case.c_dtype] if case.C is not None else None,
+        bias_dtype=_VEC[case.bias_dtype] if case.bias is not None else None,
+        row_scale=None if case.row_scale is None else case.row_scale.numpy(),
+        col_scale=None if case.col_scale is None else case.col_scale.numpy())
 
 
 def assert_within(got: np.ndarray, ref: np.ndarray, tol: float, what: str = "") -> float:

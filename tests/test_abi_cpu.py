@@ -58,6 +58,9 @@ def test_valid_problem_is_ok(lib):
     assert ci(opA="col", lda=304, opB="row", ldb=200) == 0
     assert ci(has_c=1, bias=BIAS, act="gelu") == 0
     assert ci(ab="e4m3", lda=128, ldb=128) == 0
+    assert ci(ab="f16") == 0
+    assert ci(ab="e5m2", lda=128, ldb=128) == 0
+    assert ci(ab="f16", opA="col", lda=304, opB="row", ldb=200) == 0
 
 
 def test_empty_problem_is_ok(lib):
@@ -91,6 +94,7 @@ def test_misaligned_lda_is_refused(lib):
 
 def test_unsupported_fp8_layouts(lib):
     assert ci(ab="e4m3", opA="col", lda=304) == 2
+    assert ci(ab="e5m2", opB="row", ldb=208) == 2
 
 
 def test_k_zero_needs_no_operands(lib):

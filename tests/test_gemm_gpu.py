@@ -298,3 +298,61 @@ def test_tail_split_epilogue_bf16():
     case = inputs.make_case("tail_epi", 2048, 2560 + 256, 1024, seed=201, dist="uniform", beta=0.5,
                             c_dist="uniform", bias_std=0.1, act="gelu")
     check_full(case)
+
+
+# -------------------------------------- fp16 / e5m2 operands, channel scales
+
+@pytest.mark.parametrize("combo", inputs.LAYOUT_COMBOS, ids=lambda c: c[0] + c[1])
+@pytest.mark.parametrize("force_cta2", [1, 2], ids=["pair", "one_cta"])
+def test_f16_integer_exact(combo, force_cta2):
+    try:
+        tcg.debug_set(force_cta2=force_cta2)
+        case = inputs.make_case("f16int", 300, 520, 384, seed=211, dist="int4", ab_dtype="f16",
+                                opA=combo[0], opB=combo[1], d_dtype="f32")
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()
+
+
+def test_f16_bias_gelu():
+    case = inputs.make_case("f16gelu", 640, 768, 512, seed=221, dist="normal_sqrtk", ab_dtype="f16",
+                            bias_std=0.1, act="gelu", beta=0.5, c_dist="uniform")
+    check_full(case)
+
+
+@pytest.mark.parametrize("force_cta2", [1, 2], ids=["pair", "one_cta"])
+def test_e5m2_integer_exact(force_cta2):
+    try:
+        tcg.debug_set(force_cta2=force_cta2)
+        case = inputs.make_case("e5m2int", 512, 768, 640, seed=231, dist="int4", ab_dtype="e5m2",
+                                d_dtype="f32")
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()
+
+
+def test_e5m2_scaled_bias_relu():
+    case = inputs.make_case("e5m2", 384, 640, 1024, seed=241, dist="normal", ab_dtype="e5m2",
+                            bias_std=0.1, act="relu")
+    check_full(case)
+
+
+@pytest.mark.parametrize("ab", ["bf16", "e4m3"])
+@pytest.mark.parametrize("force_cta2", [1, 2], ids=["pair", "one_cta"])
+def test_channel_scales(ab, force_cta2):
+    try:
+        tcg.debug_set(force_cta2=force_cta2)
+        case = inputs.make_case("chan", 520, 768, 512, seed=251, dist="uniform" if ab == "bf16" else "normal",
+                                ab_dtype=ab, beta=0.5, c_dist="uniform", bias_std=0.1, act="gelu",
+                                channel_scales=True)
+        check_full(case)
+    finally:
+        tcg.debug_set()
+
+
+def test_channel_scales_integer_exact():
+    """Power-of-two channel scales keep integer inputs exact."""
+    case = inputs.make_case("chanint", 256, 512, 256, seed=261, dist="int4", d_dtype="f32")
+    case.row_scale = torch.tensor([2.0 ** (i % 3) for i in range(case.M)], dtype=torch.float32)
+    case.col_scale = torch.tensor([0.5 ** (j % 2) for j in range(case.N)], dtype=torch.float32)
+    check_full(case, exact=True)

@@ -75,6 +75,9 @@ struct KernelParams {
     long long timeout_ns;
     int fault_inject;
     unsigned long long* stats;  // optional cycle accounting (nullptr = off), see kStat*
+    uint32_t ab_fmt;            // operand format field of the instruction descriptor
+    const float* row_scale;     // optional dequantisation scale per output row (M)
+    const float* col_scale;     // optional dequantisation scale per output column (N)
 };
 
 
@@ -389,7 +392,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kStageBytes = kABytes + kBBytes;
     constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
     constexpr uint32_t kTmemCols = 2 * BN;
-    constexpr uint32_t kFmt = kFp8 ? 0u : 1u;          // e4m3 = 0, bf16 = 1
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -515,7 +517,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         // ------------------------------------------------------- MMA issuer
         if (leader) {
             const bool issuer = lane == 0;
-            const uint32_t idesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+            const uint32_t idesc = (1u << 4) | (p.ab_fmt << 7) | (p.ab_fmt << 10) |
                                    (static_cast<uint32_t>(p.a_mn_major) << 15) |
                                    (static_cast<uint32_t>(p.b_mn_major) << 16) |
                                    (static_cast<uint32_t>(BN >> 3) << 17) |
@@ -734,10 +736,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     uint64_t v2[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v2[i] = ptx::pack2(v[2 * i], v[2 * i + 1]);
-                    if (p.alpha != 1.0f) {
-                        const uint64_t al = ptx::pack2(p.alpha, p.alpha);
+                    {
+                        // alpha * sA * sB, and the per-row / per-column scales
+                        float rs = p.alpha;
+                        if (p.row_scale && row_ok) rs *= p.row_scale[grow];
+                        if (rs != 1.0f) {
+                            const uint64_t al = ptx::pack2(rs, rs);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], al);
+                            for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], al);
+                        }
+                        if (p.col_scale) {
+                            float cs[32];
+                            load_row32(p.col_scale, 1, col0, p.N, cs);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], ptx::pack2(cs[2 * i], cs[2 * i + 1]));
+                        }
                     }
                     if (has_c && row_ok) {
                         float c[32];

@@ -65,11 +65,20 @@ tcg_status fail_launch(const char* what, cudaError_t e) {
 int elem_bytes(tcg_dtype t) {
     switch (t) {
         case TCG_BF16: return 2;
+        case TCG_F16: return 2;
         case TCG_E4M3: return 1;
+        case TCG_E5M2: return 1;
         case TCG_F32: return 4;
     }
     return 0;
 }
+
+bool is_fp8(tcg_dtype t) { return t == TCG_E4M3 || t == TCG_E5M2; }
+bool is_ab_type(tcg_dtype t) { return t == TCG_BF16 || t == TCG_F16 || is_fp8(t); }
+
+// Operand format field of the tcgen05 instruction descriptor: kind::f16
+// (F16 = 0, BF16 = 1) and kind::f8f6f4 (E4M3 = 0, E5M2 = 1).
+uint32_t mma_format(tcg_dtype t) { return (t == TCG_BF16 || t == TCG_E5M2) ? 1u : 0u; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -131,7 +140,9 @@ tcg_status get_encoder(EncodeTiledFn& fn) {
 CUtensorMapDataType tma_dtype(tcg_dtype t) {
     switch (t) {
         case TCG_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        case TCG_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         case TCG_E4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        case TCG_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -244,7 +255,7 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms);
     int slots = dev.num_sms;  // units that run at once
     if (cta2) {
-        slots = max_active_pairs(pl.bn, ab == TCG_E4M3, pl.katoms, pl.smem);
+        slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
         if (slots <= 0) slots = dev.num_sms / 2;
     }
     // When the tiles leave the last wave at most half full, split those last
@@ -379,7 +390,7 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
                              const void* B, int ldb, tcg_layout opB, int has_c, const void* C, int ldc,
                              tcg_dtype c_dtype, const void* D, int ldd, tcg_dtype d_dtype, tcg_epilogue epi) {
     if (M < 0 || N < 0 || K < 0) return TCG_ERR_INVALID_ARG;
-    if (ab_dtype != TCG_BF16 && ab_dtype != TCG_E4M3) return TCG_ERR_INVALID_ARG;
+    if (!is_ab_type(ab_dtype)) return TCG_ERR_INVALID_ARG;
     if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return TCG_ERR_INVALID_ARG;
     if (d_dtype != TCG_BF16 && d_dtype != TCG_F32) return TCG_ERR_INVALID_ARG;
     if (has_c && c_dtype != TCG_BF16 && c_dtype != TCG_F32) return TCG_ERR_INVALID_ARG;
@@ -396,7 +407,7 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
     }
     if (ldd < N) return TCG_ERR_INVALID_ARG;
     if (has_c && ldc < N) return TCG_ERR_INVALID_ARG;
-    if (ab_dtype == TCG_E4M3 && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
+    if (is_fp8(ab_dtype) && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
     // 16-byte rule for every pointer and every leading dimension in bytes
     const int eb = elem_bytes(ab_dtype);
     if (K > 0) {
@@ -413,7 +424,7 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
 
 size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
     if (M < 0 || N < 0 || K < 0) return 0;
-    if (ab_dtype != TCG_BF16 && ab_dtype != TCG_E4M3) return 0;
+    if (!is_ab_type(ab_dtype)) return 0;
     DeviceInfo dev;
     if (device_info(dev) != TCG_OK) {
         // Without a device the split-K part cannot be sized; report the
@@ -462,6 +473,8 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         g_last_error = buf;
         return TCG_ERR_ARCH;
     }
+    if (scales.col_scale && !aligned16(scales.col_scale)) return TCG_ERR_MISALIGNED;
+    if (scales.row_scale && (reinterpret_cast<uintptr_t>(scales.row_scale) & 3u)) return TCG_ERR_MISALIGNED;
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
     const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TCG_ERR_WORKSPACE;
@@ -495,6 +508,9 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.units_a = pl.units_a; kp.splits_b = pl.splits_b;
     kp.a_mn_major = (opA == TCG_COL); kp.b_mn_major = (opB == TCG_ROW);
     kp.alpha = alpha * scales.scale_a * scales.scale_b;
+    kp.ab_fmt = mma_format(ab_dtype);
+    kp.row_scale = scales.row_scale;
+    kp.col_scale = scales.col_scale;
     kp.beta = beta;
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
@@ -515,7 +531,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.fault_inject = g_fault_inject;
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
-    const bool fp8 = ab_dtype == TCG_E4M3;
+    const bool fp8 = is_fp8(ab_dtype);
     if (pl.cluster == 2 && pl.katoms == 2)
         return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)
                    : launch_kernel<256, false, true, 2>(kp, pl, stream);

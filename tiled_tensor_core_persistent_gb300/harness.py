@@ -33,6 +33,8 @@ class DeviceCase:
         self.B = case.B.to(dev)
         self.C = case.C.to(dev) if case.C is not None else None
         self.bias = case.bias.to(dev) if case.bias is not None else None
+        self.row_scale = case.row_scale.to(dev) if case.row_scale is not None else None
+        self.col_scale = case.col_scale.to(dev) if case.col_scale is not None else None
         ddt = _TORCH_DTYPE[case.d_dtype]
         self.guard_rows = guard_rows
         rows = max(case.M, 1) + 2 * guard_rows
@@ -47,7 +49,8 @@ class DeviceCase:
         gemm(c.M, c.N, c.K, c.alpha, self.A, c.lda, c.opA, self.B, c.ldb, c.opB, c.beta, self.C,
              c.ldc, c.c_dtype, self.D_view, c.ldd, c.d_dtype, bias=self.bias,
              bias_dtype=c.bias_dtype, act=c.act, ab_dtype=c.ab_dtype, scale_a=c.scale_a,
-             scale_b=c.scale_b, workspace=self.workspace, workspace_bytes=self.ws_bytes,
+             scale_b=c.scale_b, row_scale=self.row_scale, col_scale=self.col_scale,
+             workspace=self.workspace, workspace_bytes=self.ws_bytes,
              stream=stream if stream is not None else self.stream)
 
     def result(self) -> torch.Tensor:

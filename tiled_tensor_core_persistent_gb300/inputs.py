@@ -20,9 +20,12 @@ from typing import Optional
 import numpy as np
 import torch
 
-_ELEM_BYTES = {"bf16": 2, "e4m3": 1, "f32": 4}
-_TORCH = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "f32": torch.float32}
+_ELEM_BYTES = {"bf16": 2, "e4m3": 1, "f32": 4, "f16": 2, "e5m2": 1}
+_TORCH = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "f32": torch.float32, "f16": torch.float16,
+          "e5m2": torch.float8_e5m2}
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+FP8_MAX = {"e4m3": E4M3_MAX, "e5m2": E5M2_MAX}
 
 
 def padded_ld(extent: int, dtype: str) -> int:
@@ -49,9 +52,9 @@ def raw_bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
     """The raw storage bits of a CPU tensor as numpy (uint16 / uint8 / float32)."""
     if t is None:
         return None
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    if t.dtype == torch.float8_e4m3fn:
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
         return t.contiguous().view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.contiguous().numpy()
@@ -82,6 +85,8 @@ class GemmCase:
     act: str = "none"
     scale_a: float = 1.0
     scale_b: float = 1.0
+    row_scale: Optional[torch.Tensor] = None   # fp32 [M] dequantisation scale per row
+    col_scale: Optional[torch.Tensor] = None   # fp32 [N] dequantisation scale per column
     ldd: int = 0
     meta: dict = field(default_factory=dict)
 
@@ -105,22 +110,25 @@ def _draw(gen, shape, dist, K):
 def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
               ab_dtype="bf16", d_dtype="bf16", alpha=1.0, beta=0.0, c_dist=None,
               c_dtype="bf16", bias_std=None, bias_dtype="bf16", act="none",
-              lda=None, ldb=None, ldc=None, ldd=None) -> GemmCase:
-    """Draw one GEMM problem.  Order of draws: A, B, C, bias (all from `seed`)."""
+              lda=None, ldb=None, ldc=None, ldd=None, channel_scales=False) -> GemmCase:
+    """Draw one GEMM problem.  Order of draws: A, B, C, bias, channel scales
+    (all from `seed`).  channel_scales: fp32 row and column scales U[0.5, 2]."""
     gen = torch.Generator().manual_seed(int(seed))
     a = _draw(gen, (M, K), dist, K)
     b = _draw(gen, (K, N), dist, K)
     scale_a = scale_b = 1.0
-    if ab_dtype == "e4m3" and dist != "int4":
-        # per-tensor scale amax/448, then the quantised codes (the harness does
-        # this, not the library): q = e4m3(clamp(x / scale, -448, 448)).
-        # Integer draws in [-4, 4] are e4m3 codes already and keep scale 1.
+    if ab_dtype in FP8_MAX and dist != "int4":
+        # per-tensor scale amax/fmax, then the quantised codes (the harness does
+        # this, not the library): q = fp8(clamp(x / scale, -fmax, fmax)), fmax =
+        # 448 (e4m3) or 57344 (e5m2).  Integer draws in [-4, 4] are FP8 codes
+        # already and keep scale 1.
+        fmax = FP8_MAX[ab_dtype]
         amax_a = float(a.abs().max()) if a.numel() else 1.0
         amax_b = float(b.abs().max()) if b.numel() else 1.0
-        scale_a = (amax_a / E4M3_MAX) if amax_a > 0 else 1.0
-        scale_b = (amax_b / E4M3_MAX) if amax_b > 0 else 1.0
-        a = (a / scale_a).clamp(-E4M3_MAX, E4M3_MAX)
-        b = (b / scale_b).clamp(-E4M3_MAX, E4M3_MAX)
+        scale_a = (amax_a / fmax) if amax_a > 0 else 1.0
+        scale_b = (amax_b / fmax) if amax_b > 0 else 1.0
+        a = (a / scale_a).clamp(-fmax, fmax)
+        b = (b / scale_b).clamp(-fmax, fmax)
     A, lda = _store(a, opA, ab_dtype, lda)
     B, ldb = _store(b, opB, ab_dtype, ldb)
     C = None
@@ -132,12 +140,16 @@ def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
     bias = None
     if bias_std is not None:
         bias = (torch.randn((N,), generator=gen, dtype=torch.float32) * bias_std).to(_TORCH[bias_dtype])
+    row_scale = col_scale = None
+    if channel_scales:
+        row_scale = torch.rand((M,), generator=gen, dtype=torch.float32) * 1.5 + 0.5
+        col_scale = torch.rand((N,), generator=gen, dtype=torch.float32) * 1.5 + 0.5
     ldd = padded_ld(N, d_dtype) if ldd is None else ldd
     return GemmCase(name=name, M=M, N=N, K=K, opA=opA, opB=opB, ab_dtype=ab_dtype,
                     d_dtype=d_dtype, A=A, lda=lda, B=B, ldb=ldb, alpha=alpha, beta=beta,
                     C=C, ldc=ldc, c_dtype=c_dtype, bias=bias, bias_dtype=bias_dtype,
-                    act=act, scale_a=scale_a, scale_b=scale_b, ldd=ldd,
-                    meta={"seed": seed, "dist": dist})
+                    act=act, scale_a=scale_a, scale_b=scale_b, row_scale=row_scale,
+                    col_scale=col_scale, ldd=ldd, meta={"seed": seed, "dist": dist})
 
 
 # The workloads, with their sizes and value recipes.  Seeds are fixed per case.
