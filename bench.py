@@ -292,8 +292,10 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nrows = 96
-        t = cpu_oracle_rows(case, list(range(0, case.M, case.M // nrows))[:nrows])
+        # a bounded sample: about 15 s of oracle work on the host cores
+        t_probe = cpu_oracle_rows(case, list(range(0, case.M, case.M // 16))[:16])
+        nrows = int(min(case.M, max(16, 15.0 / max(t_probe / 16, 1e-6))))
+        t = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // nrows)))[:nrows])
         cpu = {"value": 2.0 * nrows * case.N * case.K / t / 1e12, "unit": UNIT,
                "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{nrows} full rows of D ({nrows}x{case.N}x{case.K}), {t:.1f} s wall"}
