@@ -3,6 +3,7 @@
 bias + GELU epilogue (A row-major, B column-major, bf16 D), 1 GPU per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
 
 One step = one tcg_gemm launch over the whole 8192^3 problem with inputs
 resident in HBM (A+B = 256 MiB > the 129 MB L2, so no flush is needed).  The
@@ -13,6 +14,12 @@ collective on the data path); the reported time is the max over ranks.
 
 --impl reference times the oracle (plain C, fp64, host cores) on bounded row
 samples of the same workload, reported in the same unit.
+
+--workload picks one of the other parity workloads (4096^3 beta*C, 512^3,
+the ragged and skinny shapes, 8192^3 e4m3); those whose inputs fit in L2 are
+timed one launch per event pair with a 512 MiB L2 flush in between.  The
+roofline object is then against HBM bandwidth (GB/s) when the pages'
+intensity 2MNK / (b (MK + KN + MN)) puts the shape below the ridge point.
 """
 from __future__ import annotations
 
@@ -43,15 +50,58 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
+                    help="the metric's workload (default) or one of the parity workloads, "
+                         "measured the same way for the per-workload roofline table")
     return ap.parse_args()
 
 
-def workload_config(case):
-    return {"workload": f"gemm {case.M}x{case.N}x{case.K} bf16, A row-major / B column-major, "
-                        f"D = GELU(A@B + bias[N]) bf16, bias N(0,0.1), A,B N(0,1)/sqrt(K)",
+# Workloads: name -> (case factory name in inputs, flush L2 between launches).
+# Inputs that do not exceed the 129 MB L2 by a wide margin are timed one launch
+# at a time with a 512 MiB L2 flush between launches (outside the timed events).
+DEFAULT_WORKLOAD = "gemm8192_bias_gelu"
+WORKLOADS = {
+    "gemm8192_bias_gelu": (lambda inputs: inputs.square_8192_gelu(), False),
+    "gemm4096_beta1": (lambda inputs: inputs.square_4096_beta(), True),
+    "gemm512_uniform": (lambda inputs: inputs.square_512(integer=False), True),
+    "ragged_4095x3001x1537": (lambda inputs: inputs.ragged(0, 1), True),
+    "ragged_tight_4095x3001x1537": (lambda inputs: inputs.ragged_tight(1), True),
+    "skinny_16x8192x8192": (lambda inputs: inputs.ragged(1, 1), True),
+    "skinny_8192x128x8192": (lambda inputs: inputs.ragged(2, 1), True),
+    "gemm8192_e4m3_bias_relu": (lambda inputs: inputs.fp8_8192_relu(), True),
+}
+
+def metric_name(workload):
+    return METRIC if workload == DEFAULT_WORKLOAD else f"GEMM TFLOP/s ({workload}), 1 GPU"
+
+
+_EB = {"bf16": 2, "f16": 2, "e4m3": 1, "e5m2": 1, "f32": 4}
+
+
+def case_bytes(case):
+    """Algorithmic bytes of one launch: A and B once, C once if beta != 0, D once, bias once."""
+    from tiled_tensor_core_persistent_gb300 import analysis
+    return analysis.gemm_bytes(case.M, case.N, case.K, _EB[case.ab_dtype], _EB[case.d_dtype],
+                               _EB[case.c_dtype] if case.C is not None else 0,
+                               _EB[case.bias_dtype] if case.bias is not None else 0)
+
+
+def workload_config(case, flush):
+    epi = []
+    if case.C is not None:
+        epi.append(f"beta*C ({case.c_dtype})")
+    if case.bias is not None:
+        epi.append(f"bias[N] ({case.bias_dtype})")
+    if case.act != "none":
+        epi.append(case.act + ("(erf)" if case.act == "gelu" else ""))
+    ab = sum(t.numel() * t.element_size() for t in (case.A, case.B))
+    return {"workload": f"gemm {case.M}x{case.N}x{case.K} {case.ab_dtype}, A {case.opA}-major / "
+                        f"B {case.opB}-major, D = {' + '.join(['alpha*A@B'] + epi)} -> {case.d_dtype} "
+                        f"({case.name}, seed {case.meta.get('seed')}, {case.meta.get('dist')})",
             "M": case.M, "N": case.N, "K": case.K, "ab_dtype": case.ab_dtype,
-            "d_dtype": case.d_dtype, "epilogue": "bias+gelu(erf)", "accumulate": "f32",
-            "l2": "inputs larger than L2 (A+B 256 MiB > 129 MB), no flush",
+            "d_dtype": case.d_dtype, "epilogue": "+".join(epi) or "none", "accumulate": "f32",
+            "l2": ("512 MiB L2 flush (write, then read back) between launches, outside the timed events" if flush else
+                   f"inputs larger than L2 (A+B {ab / 2**20:.0f} MiB > 129 MB), no flush"),
             "parallelism": "replicas (one independent GEMM per GPU)"}
 
 
@@ -175,14 +225,24 @@ def max_over_ranks(pg, value, device):
     return float(t.item())
 
 
-def cpu_oracle_rows(case, rows, nthreads=0):
-    import numpy as np
+def oracle_problem(case):
     import oracle
     from tiled_tensor_core_persistent_gb300 import inputs
-    prob = oracle.Problem(case.M, case.N, case.K, inputs.raw_bits(case.A), case.lda, oracle.ROW,
-                          inputs.raw_bits(case.B), case.ldb, oracle.COL, alpha=case.alpha,
-                          beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
-                          bias=inputs.raw_bits(case.bias), act=case.act)
+    ab = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+    vec = {"bf16": oracle.BF16, "f32": oracle.F32}
+    return oracle.Problem(
+        case.M, case.N, case.K, inputs.raw_bits(case.A), case.lda,
+        oracle.ROW if case.opA == "row" else oracle.COL,
+        inputs.raw_bits(case.B), case.ldb, oracle.ROW if case.opB == "row" else oracle.COL,
+        alpha=case.alpha, beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
+        bias=inputs.raw_bits(case.bias), act=case.act, scale_a=case.scale_a, scale_b=case.scale_b,
+        ab_dtype=ab[case.ab_dtype], c_dtype=vec[case.c_dtype] if case.C is not None else None,
+        bias_dtype=vec[case.bias_dtype] if case.bias is not None else None)
+
+
+def cpu_oracle_rows(case, rows, nthreads=0, prob=None):
+    import numpy as np
+    prob = prob if prob is not None else oracle_problem(case)
     cols = np.arange(case.N, dtype=np.int32)
     t0 = time.perf_counter()
     prob.select(np.asarray(rows, dtype=np.int32), cols, nthreads)
@@ -195,32 +255,63 @@ def run_reference(args):
     if rank != 0:
         return 0
     from tiled_tensor_core_persistent_gb300 import inputs
-    case = inputs.square_8192_gelu()
+    case = WORKLOADS[args.workload][0](inputs)
     cores = os.cpu_count() or 1
     # size each step so the whole run stays within about a minute
-    probe = cpu_oracle_rows(case, [0, 1])
+    prob = oracle_problem(case)
+    probe = cpu_oracle_rows(case, [0, 1], prob=prob)
     per_row = probe / 2
     budget_s = 60.0
     rows_per_step = max(1, int(budget_s / max(1, args.steps + args.warmup) / max(per_row, 1e-6)))
     rows_per_step = min(rows_per_step, 64)
     rng_rows = lambda i: [(i * rows_per_step + r) % case.M for r in range(rows_per_step)]
     for i in range(args.warmup):
-        cpu_oracle_rows(case, rng_rows(i))
+        cpu_oracle_rows(case, rng_rows(i), prob=prob)
     t = 0.0
     for i in range(args.steps):
-        t += cpu_oracle_rows(case, rng_rows(args.warmup + i))
+        t += cpu_oracle_rows(case, rng_rows(args.warmup + i), prob=prob)
     flops = 2.0 * rows_per_step * case.N * case.K * args.steps
     value = flops / t / 1e12
     sample = f"{rows_per_step} full rows of D (x {case.N} cols x K={case.K}) per step"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(case),
+            "data": "synthetic", "config": workload_config(case, WORKLOADS[args.workload][1]),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def timed_launches(args, dc, stream, device, flush):
+    """Milliseconds of args.steps launches: back to back between two events, or
+    (flush) one launch per event pair with an L2 flush outside each pair."""
+    import torch
+    if not flush:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            dc.run(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        return ev0.elapsed_time(ev1)
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            # write 512 MiB, then read it back: L2 ends up holding clean lines
+            # of the scrub buffer, so no write-back of the flush competes with
+            # the timed launch for DRAM bandwidth
+            scrub.fill_(i & 0xFF)
+            scrub.view(torch.int32).sum()
+            a.record(stream)
+            dc.run(stream)
+            b.record(stream)
+    torch.cuda.synchronize(device)
+    return sum(a.elapsed_time(b) for a, b in evs)
 
 
 def run_ours(args):
@@ -235,7 +326,8 @@ def run_ours(args):
     barrier(pg, device)
     tcg.lib()
 
-    case = inputs.square_8192_gelu()
+    factory, flush = WORKLOADS[args.workload]
+    case = factory(inputs)
     stream = torch.cuda.Stream(device=device)
     dc = harness.DeviceCase(case, device=device, stream=stream)
     torch.cuda.synchronize(device)
@@ -254,16 +346,10 @@ def run_ours(args):
     time.sleep(0.3)
     barrier(pg, device)
     torch.cuda.synchronize(device)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        dc.run(stream)
-    ev1.record(stream)
+    elapsed_ms = timed_launches(args, dc, stream, device, flush)
     torch.cuda.synchronize(device)
     barrier(pg, device)
     clocks = sampler.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
     elapsed_ms = max_over_ranks(pg, elapsed_ms, device)
     st = tcg.device_status(dc.workspace, stream)
     if st != 0:
@@ -278,34 +364,52 @@ def run_ours(args):
     e2e = run_e2e(args, case, dc, stream, device, tcg) if args.e2e_steps > 0 else None
 
     peaks, peak_kind = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
-    roof = {"bound": "tensor", "achieved": per_launch_tflops, "peak": peak, "unit": "TFLOP/s",
-            "frac": per_launch_tflops / peak, "traffic": recorded_traffic("gemm8192_bias_gelu"),
-            "peak_kind": f"{peak_kind} bf16 burst (cuBLAS 8192^3)",
-            "peak_sustained": peaks.get("bf16_tflops_sustained"),
-            "frac_of_nominal_2250": per_launch_tflops / 2250.0,
-            "algorithmic": "2*M*N*K flop per launch",
-            "model": {"intensity_flop_per_byte": analysis.boundary_intensity(case.M, case.N, case.K, 2),
-                      "roofline_tflops": analysis.roofline(2250.0, analysis.boundary_intensity(case.M, case.N, case.K, 2),
-                                                           float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)) * 1e-3),
-                      "algorithmic_bytes": analysis.gemm_bytes(case.M, case.N, case.K, 2, 2, 0, 2)}}
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    in_bytes = _EB[case.ab_dtype]
+    # dense tensor peak of the operand type: fp8 = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+    tensor_peak = bf16_peak * (2.0 if in_bytes == 1 else 1.0)
+    nominal = 2250.0 * (2.0 if in_bytes == 1 else 1.0)
+    alg_bytes = case_bytes(case)
+    intensity = analysis.boundary_intensity(case.M, case.N, case.K, in_bytes)
+    hbm_bound = intensity * hbm * 1e-3 < tensor_peak
+    gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
+    roof = {"bound": "hbm" if hbm_bound else "tensor",
+            "achieved": gbs if hbm_bound else per_launch_tflops,
+            "peak": hbm if hbm_bound else tensor_peak,
+            "unit": "GB/s" if hbm_bound else "TFLOP/s",
+            "frac": (gbs / hbm) if hbm_bound else (per_launch_tflops / tensor_peak),
+            "traffic": recorded_traffic(args.workload),
+            "peak_kind": (f"{peak_kind} copy bandwidth" if hbm_bound else
+                          f"{peak_kind} bf16 burst (cuBLAS 8192^3)" + (" x 2 for fp8" if in_bytes == 1 else "")),
+            "peak_sustained": None if hbm_bound else
+            peaks.get("bf16_tflops_sustained", 0) * (2.0 if in_bytes == 1 else 1.0) or None,
+            "tflops": per_launch_tflops, "gbs": gbs,
+            "frac_of_nominal_tensor": per_launch_tflops / nominal,
+            "algorithmic": "2*M*N*K flop per launch; bytes = A + B + D (+ C, bias) once",
+            "model": {"intensity_flop_per_byte": intensity,
+                      "roofline_tflops": analysis.roofline(nominal, intensity, hbm * 1e-3),
+                      "algorithmic_bytes": alg_bytes}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # a bounded sample: about 15 s of oracle work on the host cores
-        t_probe = cpu_oracle_rows(case, list(range(0, case.M, case.M // 16))[:16])
-        nrows = int(min(case.M, max(16, 15.0 / max(t_probe / 16, 1e-6))))
-        t = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // nrows)))[:nrows])
+        prob = oracle_problem(case)
+        n_probe = min(16, case.M)
+        t_probe = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // n_probe)))[:n_probe], prob=prob)
+        nrows = int(min(case.M, max(n_probe, 15.0 / max(t_probe / n_probe, 1e-6))))
+        t = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // nrows)))[:nrows], prob=prob)
         cpu = {"value": 2.0 * nrows * case.N * case.K / t / 1e12, "unit": UNIT,
                "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{nrows} full rows of D ({nrows}x{case.N}x{case.K}), {t:.1f} s wall"}
 
     plan = tcg.plan(case.M, case.N, case.K, case.ab_dtype)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        line = {"metric": metric_name(args.workload),
+                "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": dict(workload_config(case), plan=plan),
+                "scaling": "weak", "vs_baseline": None, "dtype": case.ab_dtype, "data": "synthetic",
+                "config": dict(workload_config(case, flush), plan=plan),
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": args.steps}
         print(json.dumps(line), flush=True)
@@ -319,9 +423,11 @@ def run_e2e(args, case, dc, stream, device, tcg):
     A_h = case.A.pin_memory()
     B_h = case.B.pin_memory()
     bias_h = case.bias.pin_memory() if case.bias is not None else None
+    C_h = case.C.pin_memory() if case.C is not None else None
     D_h = torch.empty(dc.D_view.shape, dtype=dc.D_view.dtype).pin_memory()
     h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size() + \
-        (bias_h.numel() * bias_h.element_size() if bias_h is not None else 0)
+        (bias_h.numel() * bias_h.element_size() if bias_h is not None else 0) + \
+        (C_h.numel() * C_h.element_size() if C_h is not None else 0)
     d2h = D_h.numel() * D_h.element_size()
 
     def step():
@@ -330,6 +436,8 @@ def run_e2e(args, case, dc, stream, device, tcg):
             dc.B.copy_(B_h, non_blocking=True)
             if bias_h is not None:
                 dc.bias.copy_(bias_h, non_blocking=True)
+            if C_h is not None:
+                dc.C.copy_(C_h, non_blocking=True)
             dc.run(stream)
             D_h.copy_(dc.D_view, non_blocking=True)
 
@@ -347,7 +455,7 @@ def run_e2e(args, case, dc, stream, device, tcg):
     ms = ev0.elapsed_time(ev1) / n
     return {"value": case.flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
-            "path": "pinned host A,B,bias -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
+            "path": "pinned host A, B, C, bias -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
 
 
 def main():

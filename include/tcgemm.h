@@ -23,9 +23,14 @@
  *   caller, are device memory of the current CUDA device, and must stay
  *   valid until the work queued on `stream` has finished.  The library keeps
  *   only a process-wide cache of TMA descriptors and launch attributes.
- * - Alignment: every pointer 16-byte aligned and every ld * sizeof(element)
- *   a multiple of 16 bytes, else TCG_ERR_MISALIGNED (the CUTLASS page, Part II,
- *   "ignoring alignment", and Lab 3: a misaligned lda must be refused).
+ * - Alignment ("CUTLASS" page, Part II, "ignoring alignment": a misaligned
+ *   tensor either falls back to a slow path or refuses to run).  Every
+ *   pointer must be aligned to its element size, else TCG_ERR_MISALIGNED.
+ *   The fast path wants each matrix 16-byte aligned with ld * sizeof(element)
+ *   a multiple of 16 bytes (the TMA rule).  Otherwise the call still runs:
+ *   A or B is first copied into 16-byte pitched rows of the workspace (size
+ *   it with tcg_workspace_size_for), and C, D and bias are read and written
+ *   element-wise in the epilogue.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  tcg_gemm is asynchronous: host-detectable errors return before
  *   anything is queued; device-side errors (a bounded wait that ran out) are
@@ -47,9 +52,9 @@ typedef enum {
     TCG_OK = 0,
     TCG_ERR_INVALID_ARG = 1,   /* negative size, NULL pointer that is needed, bad enum, ld too small */
     TCG_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. MN-major e4m3) */
-    TCG_ERR_MISALIGNED = 3,    /* pointer or ld * element size not a multiple of 16 bytes */
+    TCG_ERR_MISALIGNED = 3,    /* a pointer not aligned to its element size */
     TCG_ERR_ARCH = 4,          /* current device is not compute capability 10.3 */
-    TCG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than tcg_workspace_size */
+    TCG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than tcg_workspace_size_for */
     TCG_ERR_LAUNCH = 6,        /* a CUDA runtime/driver call failed (message: tcg_last_error) */
     TCG_ERR_TIMEOUT = 7        /* a bounded device-side wait ran out (reported by tcg_device_status) */
 } tcg_status;
@@ -75,8 +80,8 @@ typedef struct {
  * fused into the epilogue).  The raw product sum of element (i, j) is
  * multiplied by alpha * scale_a * scale_b * row_scale[i] * col_scale[j].
  * scale_a / scale_b: per-tensor (1.0 when unused).  row_scale: NULL or a
- * device vector of M fp32 values (4-byte aligned); col_scale: NULL or a
- * device vector of N fp32 values (16-byte aligned).  Any operand type. */
+ * device vector of M fp32 values; col_scale: NULL or a device vector of N
+ * fp32 values (both 4-byte aligned).  Any operand type. */
 typedef struct {
     float scale_a;
     float scale_b;
@@ -86,6 +91,7 @@ typedef struct {
 
 /*
  * tcg_can_implement -- argument validation only (no GPU access, no launch).
+ * TCG_OK also for unaligned leading dimensions (the slow path above).
  *   M, N, K        : problem size, >= 0.
  *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3 or TCG_E5M2 (A and B share
  *                    it).  The 8-bit types require opA = TCG_ROW and
@@ -95,7 +101,7 @@ typedef struct {
  *   has_c, C, ldc, c_dtype : has_c != 0 when beta != 0; then C row-major,
  *                    ldc >= N, c_dtype TCG_BF16 or TCG_F32.
  *   D, ldd, d_dtype: output, row-major, ldd >= N, TCG_BF16 or TCG_F32.
- *   epi            : bias pointer (16-byte aligned) / dtype / activation.
+ *   epi            : bias pointer (aligned to its element) / dtype / activation.
  * Returns TCG_OK or the first failing rule's code.  M == 0 or N == 0 is OK.
  */
 tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype,
@@ -115,6 +121,19 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype,
  */
 size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype);
 
+/*
+ * tcg_workspace_size_for -- tcg_workspace_size plus room for packed copies of
+ * A and/or B when the TMA cannot address them as stored (base not 16-byte
+ * aligned, or ld * sizeof(element) not a multiple of 16): outer x ld' elements
+ * per packed operand, ld' = the contiguous extent rounded up to 16 bytes,
+ * each copy 256-byte aligned.  Equal to tcg_workspace_size when both operands
+ * are TMA-addressable.  Arguments as in tcg_can_implement (pointers are only
+ * inspected, never dereferenced).  Returns 0 for invalid sizes or layouts.
+ */
+size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype,
+                              const void* A, int lda, tcg_layout opA,
+                              const void* B, int ldb, tcg_layout opB);
+
 /* Zero-fill `bytes` of workspace on `stream` (asynchronous). */
 tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream);
 
@@ -123,6 +142,9 @@ tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream);
  * `stream`.  Arguments as in tcg_can_implement; beta == 0 means C is never
  * read (C may be NULL and may hold NaN).  K == 0 gives act(beta*C + bias).
  * The result is rounded once from fp32 to d_dtype (round to nearest even).
+ * When A or B is not TMA-addressable, a copy kernel first packs it into the
+ * workspace on `stream` (workspace_bytes >= tcg_workspace_size_for, else
+ * TCG_ERR_WORKSPACE with a message in tcg_last_error).
  * D must not overlap A, B or bias; D == C (in-place update) is allowed when
  * ldc == ldd and c_dtype == d_dtype.
  * Returns TCG_OK when the kernel was queued.
@@ -175,8 +197,8 @@ void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits
  *   Arguments: as tcg_gemm, without the workspace.  It allocates nothing.
  *   Scratch: a 32 MiB file-scope device array held by every GPU that loads
  *     the library until the process exits.  Problems whose workspace
- *     (tcg_workspace_size) exceeds 32 MiB return TCG_ERR_WORKSPACE with a
- *     message in tcg_last_error.
+ *     (tcg_workspace_size_for) exceeds 32 MiB return TCG_ERR_WORKSPACE with
+ *     a message in tcg_last_error.
  *   Set-up: the first call on each device (with that device current) looks
  *     up the array's device address; make that first call before any stream
  *     capture.

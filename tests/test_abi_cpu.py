@@ -82,14 +82,42 @@ def test_invalid_arguments(lib):
     assert ci(act=9) == INVALID
 
 
-def test_misaligned_lda_is_refused(lib):
-    """The CUTLASS page's Lab 3: misalign lda by one and watch can_implement refuse."""
+def test_pointer_not_aligned_to_its_element_is_refused(lib):
+    """The refusing branch of the CUTLASS page's alignment rule (Part II): a pointer
+    that is not aligned to its element size cannot be served by any path."""
     MISALIGNED = 3
-    assert ci(lda=129) == MISALIGNED
-    assert ci(A_=A + 2) == MISALIGNED
-    assert ci(ldd=201) == MISALIGNED
-    assert ci(bias=BIAS + 4) == MISALIGNED
-    assert ci(has_c=1, ldc=204, c_dtype="bf16") == MISALIGNED
+    assert ci(A_=A + 1) == MISALIGNED
+    assert ci(B_=B + 1) == MISALIGNED
+    assert ci(D_=D + 1) == MISALIGNED
+    assert ci(D_=D + 2, d_dtype="f32") == MISALIGNED
+    assert ci(bias=BIAS + 1) == MISALIGNED
+    assert ci(bias=BIAS + 2, bias_dtype="f32") == MISALIGNED
+    assert ci(has_c=1, C_=C + 1) == MISALIGNED
+    assert ci(ab="e4m3", A_=A + 1, lda=128, ldb=128) == 0   # 1-byte elements: any address
+
+
+def test_unaligned_leading_dimensions_take_the_slow_path(lib):
+    """The other branch of the same rule: Lab 3's lda misaligned by one element is
+    accepted; the operand is packed into the workspace, which grows by its size."""
+    assert ci(lda=129) == 0
+    assert ci(A_=A + 2) == 0
+    assert ci(ldd=201) == 0
+    assert ci(bias=BIAS + 4) == 0
+    assert ci(has_c=1, ldc=201, c_dtype="bf16") == 0
+    base = tcg.workspace_size(300, 200, 128)
+    assert tcg.workspace_size_for(300, 200, 128, "bf16", A, 128, "row", B, 128, "col") == base
+    # A row-major 300 x 128 with lda 129: the copy holds 300 rows of K = 128 elements
+    pa = (300 * 128 * 2 + 255) // 256 * 256
+    assert tcg.workspace_size_for(300, 200, 128, "bf16", A, 129, "row", B, 128, "col") == base + pa
+    assert tcg.workspace_size_for(300, 200, 128, "bf16", A + 2, 128, "row", B, 128, "col") == base + pa
+    # B column-major 128 x 200 stored as 200 rows of K = 128, ldb 131 -> 200 x 128
+    pb = (200 * 128 * 2 + 255) // 256 * 256
+    assert tcg.workspace_size_for(300, 200, 128, "bf16", A, 129, "row", B, 131, "col") == base + pa + pb
+    # a ragged contiguous extent is padded to 16 bytes: K = 127 bf16 -> 128, e4m3 -> 128
+    assert tcg.workspace_size_for(300, 200, 127, "bf16", A, 127, "row", B, 128, "col") == \
+        tcg.workspace_size(300, 200, 127) + (300 * 128 * 2 + 255) // 256 * 256
+    assert tcg.workspace_size_for(300, 200, 100, "e4m3", A, 101, "row", B, 112, "col") == \
+        tcg.workspace_size(300, 200, 100, "e4m3") + (300 * 112 + 255) // 256 * 256
 
 
 def test_unsupported_fp8_layouts(lib):

@@ -31,7 +31,7 @@ ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
 STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "TCG_ERR_MISALIGNED",
           4: "TCG_ERR_ARCH", 5: "TCG_ERR_WORKSPACE", 6: "TCG_ERR_LAUNCH", 7: "TCG_ERR_TIMEOUT"}
 
-EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_init", "tcg_gemm",
+EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
             "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc"]
 
 
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.tcg_can_implement.restype = i32
         L.tcg_workspace_size.argtypes = [i32, i32, i32, i32]
         L.tcg_workspace_size.restype = sz
+        L.tcg_workspace_size_for.argtypes = [i32, i32, i32, i32, P, i32, i32, P, i32, i32]
+        L.tcg_workspace_size_for.restype = sz
         L.tcg_workspace_init.argtypes = [P, sz, P]
         L.tcg_workspace_init.restype = i32
         L.tcg_gemm.argtypes = [i32, i32, i32, f32, P, i32, i32, P, i32, i32, f32, P, i32, i32, P, i32, i32,
@@ -133,6 +135,12 @@ def can_implement(M, N, K, ab_dtype, A, lda, opA, B, ldb, opB, has_c, C, ldc, c_
 
 def workspace_size(M, N, K, ab_dtype="bf16") -> int:
     return int(lib().tcg_workspace_size(M, N, K, _enum(ab_dtype, DTYPES)))
+
+
+def workspace_size_for(M, N, K, ab_dtype, A, lda, opA, B, ldb, opB) -> int:
+    """Workspace bytes including packed copies of A/B that the TMA cannot address."""
+    return int(lib().tcg_workspace_size_for(M, N, K, _enum(ab_dtype, DTYPES), _addr(A), lda,
+                                            _enum(opA, LAYOUTS), _addr(B), ldb, _enum(opB, LAYOUTS)))
 
 
 def workspace_init(workspace, nbytes, stream=None) -> None:

@@ -68,6 +68,10 @@ struct KernelParams {
     void* D;              // row-major output, for the ragged column tail
     long long ldd;
     int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
+    int d_tma;            // D has a TMA store map (16-byte aligned base and row pitch)
+    int c_vec;            // C rows may be read with 16-byte vector loads
+    int bias_vec;         // bias may be read with 16-byte vector loads
+    int cs_vec;           // col_scale may be read with 16-byte vector loads
     int stages;
     float* partials;      // split-K partials: [slot][BN][kBM] (row fastest), slot = (slot_tile + split) * ranks + rank
     int* tile_counters;   // split-K arrival counters [tile * ranks + rank]
@@ -235,11 +239,12 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 
 // Load 32 consecutive elements of a row-major bf16/f32 row, columns
 // [col0, col0+32) clipped to n_valid, into fp32 registers (0 outside).
+// vec: the row start is 16-byte aligned, so whole chunks use 16-byte loads.
 __device__ __forceinline__ void load_row32(const void* base, int is_f32, int col0, int n_valid,
-                                           float (&out)[32]) {
+                                           float (&out)[32], bool vec = true) {
     if (is_f32) {
         const float* src = static_cast<const float*>(base) + col0;
-        if (col0 + 32 <= n_valid) {
+        if (vec && col0 + 32 <= n_valid) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 v = *reinterpret_cast<const float4*>(src + 4 * q);
@@ -252,7 +257,7 @@ __device__ __forceinline__ void load_row32(const void* base, int is_f32, int col
         }
     } else {
         const uint16_t* src = static_cast<const uint16_t*>(base) + col0;
-        if (col0 + 32 <= n_valid) {
+        if (vec && col0 + 32 <= n_valid) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * q);
@@ -271,46 +276,96 @@ __device__ __forceinline__ void load_row32(const void* base, int is_f32, int col
     }
 }
 
-// C prefetch: the raw 16-byte vectors of one thread's 32-column C chunk are
-// loaded one chunk ahead (and the first chunk before the accumulator is
-// ready), so the load latency hides behind the TMEM read and the math.
-// Full chunks only; a ragged last chunk is loaded element-wise when used.
-__device__ __forceinline__ void c_prefetch(const KernelParams& p, int row, int col0, uint4 (&q)[8]) {
+// C prefetch: the raw bytes of one thread's 32-column C chunk are loaded one
+// chunk ahead (and the first chunk before the accumulator is ready), so the
+// load latency hides behind the TMEM read and the math.  The loads are whole
+// aligned 16-byte blocks: the block holding the chunk's first byte and the
+// ones after it up to the block holding its last byte (4 or 5 blocks for
+// bf16, 8 or 9 for fp32; the extra block only when the row segment does not
+// start on a 16-byte boundary, i.e. when ldc * sizeof(C) is not a multiple of
+// 16).  Every block loaded holds at least one byte of the chunk.  Full chunks
+// only; a ragged last chunk is loaded element-wise when used.
+__device__ __forceinline__ uintptr_t c_chunk_addr(const KernelParams& p, int row, int col0) {
+    return reinterpret_cast<uintptr_t>(p.C) +
+           static_cast<uintptr_t>((static_cast<long long>(row) * p.ldc + col0) * (p.c_f32 ? 4 : 2));
+}
+
+__device__ __forceinline__ void c_prefetch(const KernelParams& p, int row, int col0, uint4 (&q)[9]) {
     if (col0 + 32 > p.N) return;
-    const int eb = p.c_f32 ? 4 : 2;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.C) +
-                                                      (static_cast<long long>(row) * p.ldc + col0) * eb);
+    const uintptr_t s = c_chunk_addr(p, row, col0);
+    const uint4* blk = reinterpret_cast<const uint4*>(s & ~static_cast<uintptr_t>(15));
+    const bool extra = !p.c_vec && (s & 15u) != 0;
     if (p.c_f32) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = src[i];
+        for (int i = 0; i < 8; ++i) q[i] = blk[i];
+        q[8] = extra ? blk[8] : make_uint4(0u, 0u, 0u, 0u);
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = src[i];
+        for (int i = 0; i < 4; ++i) q[i] = blk[i];
+        q[4] = extra ? blk[4] : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-__device__ __forceinline__ void c_values(const KernelParams& p, int row, int col0, const uint4 (&q)[8],
+// Bytes [off, off + 4 NW) of the word array w (NW + 4 words), off in 0..15:
+// a shift by 2 words, then by 1 word, then a funnel shift by the byte rest,
+// all branch-free so lanes with different offsets stay converged.
+template <int NW>
+__device__ __forceinline__ void shift_bytes(const uint32_t (&w)[NW + 4], uint32_t off, uint32_t (&o)[NW]) {
+    const bool s2 = (off & 8u) != 0, s1 = (off & 4u) != 0;
+    uint32_t u[NW + 2];
+#pragma unroll
+    for (int i = 0; i < NW + 2; ++i) u[i] = s2 ? w[i + 2] : w[i];
+    uint32_t v[NW + 1];
+#pragma unroll
+    for (int i = 0; i < NW + 1; ++i) v[i] = s1 ? u[i + 1] : u[i];
+    const uint32_t sh = (off & 3u) * 8u;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) o[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
+__device__ __forceinline__ void c_values(const KernelParams& p, int row, int col0, const uint4 (&q)[9],
                                          float (&c)[32]) {
     if (col0 + 32 > p.N) {
         const char* crow = static_cast<const char*>(p.C) + static_cast<long long>(row) * p.ldc * (p.c_f32 ? 4 : 2);
-        load_row32(crow, p.c_f32, col0, p.N, c);
+        load_row32(crow, p.c_f32, col0, p.N, c, p.c_vec != 0);
         return;
     }
     if (p.c_f32) {
+        uint32_t o[32];
+        if (p.c_vec) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            c[4 * i + 0] = __uint_as_float(q[i].x); c[4 * i + 1] = __uint_as_float(q[i].y);
-            c[4 * i + 2] = __uint_as_float(q[i].z); c[4 * i + 3] = __uint_as_float(q[i].w);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t wv[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                c[8 * i + 2 * h + 0] = bf16_bits_to_float(wv[h] & 0xFFFFu);
-                c[8 * i + 2 * h + 1] = bf16_bits_to_float(wv[h] >> 16);
+            for (int i = 0; i < 8; ++i) {
+                o[4 * i + 0] = q[i].x; o[4 * i + 1] = q[i].y; o[4 * i + 2] = q[i].z; o[4 * i + 3] = q[i].w;
             }
+        } else {
+            uint32_t w[36];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+                w[4 * i + 0] = q[i].x; w[4 * i + 1] = q[i].y; w[4 * i + 2] = q[i].z; w[4 * i + 3] = q[i].w;
+            }
+            shift_bytes<32>(w, static_cast<uint32_t>(c_chunk_addr(p, row, col0) & 15u), o);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) c[i] = __uint_as_float(o[i]);
+    } else {
+        uint32_t o[16];
+        if (p.c_vec) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o[4 * i + 0] = q[i].x; o[4 * i + 1] = q[i].y; o[4 * i + 2] = q[i].z; o[4 * i + 3] = q[i].w;
+            }
+        } else {
+            uint32_t w[20];
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                w[4 * i + 0] = q[i].x; w[4 * i + 1] = q[i].y; w[4 * i + 2] = q[i].z; w[4 * i + 3] = q[i].w;
+            }
+            shift_bytes<16>(w, static_cast<uint32_t>(c_chunk_addr(p, row, col0) & 15u), o);
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+            c[2 * h + 0] = bf16_bits_to_float(o[h] & 0xFFFFu);
+            c[2 * h + 1] = bf16_bits_to_float(o[h] >> 16);
         }
     }
 }
@@ -348,18 +403,32 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int row, int d_f32, cons
     }
 }
 
-// Element-wise guarded store of one thread's 32 results (columns >= N skipped).
-__device__ __forceinline__ void store_row_tail(const KernelParams& p, int row, int col0, const float (&v)[32]) {
+// Store a warp's staged 32 x 32 chunk (stage_row layout) without the TMA:
+// lane l writes column col0 + l of each of the 32 rows, so every store
+// instruction covers one contiguous run of a row.  Used when D has no TMA map
+// (unaligned base or row pitch) and for a ragged last chunk whose row end is
+// not on a 16-byte boundary (the TMA store clips the inner dimension only to
+// 16-byte granularity).  Rows >= M and columns >= N are skipped.
+__device__ __forceinline__ void store_chunk_direct(const KernelParams& p, const uint8_t* buf, int row0, int col0,
+                                                   int lane) {
+    const int col = col0 + lane;
+    if (col >= p.N) return;
+    const int nrows = min(32, p.M - row0);
     if (p.d_f32) {
-        float* dst = static_cast<float*>(p.D) + static_cast<long long>(row) * p.ldd + col0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) dst[i] = v[i];
+        float* dst = static_cast<float*>(p.D) + col;
+        const int in_row = (lane & 3) * 4, chunk = lane >> 2;
+        for (int r = 0; r < nrows; ++r) {
+            const float v = *reinterpret_cast<const float*>(buf + r * 128 + ((chunk ^ (r & 7)) << 4) + in_row);
+            dst[static_cast<long long>(row0 + r) * p.ldd] = v;
+        }
     } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.D) + static_cast<long long>(row) * p.ldd + col0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) dst[i] = __float2bfloat16_rn(v[i]);
+        uint16_t* dst = static_cast<uint16_t*>(p.D) + col;
+        const int in_row = (lane & 7) * 2, chunk = lane >> 3;
+        for (int r = 0; r < nrows; ++r) {
+            const uint16_t v =
+                *reinterpret_cast<const uint16_t*>(buf + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4) + in_row);
+            dst[static_cast<long long>(row0 + r) * p.ldd] = v;
+        }
     }
 }
 
@@ -633,7 +702,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const int counter = w.tile * kRanks + static_cast<int>(rank);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
-            uint4 cq[8];
+            uint4 cq[9];
             {
                 const int pre_row = m_blk * kTileM + static_cast<int>(rank) * kBM + (warp & 3) * 32 + lane;
                 if (has_c && pre_row < p.M && n_blk * BN < p.N) c_prefetch(p, pre_row, n_blk * BN, cq);
@@ -747,7 +816,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         }
                         if (p.col_scale) {
                             float cs[32];
-                            load_row32(p.col_scale, 1, col0, p.N, cs);
+                            load_row32(p.col_scale, 1, col0, p.N, cs, p.cs_vec != 0);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], ptx::pack2(cs[2 * i], cs[2 * i + 1]));
                         }
@@ -762,7 +831,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     }
                     if (p.bias) {
                         float b[32];
-                        load_row32(p.bias, p.bias_f32, col0, p.N, b);
+                        load_row32(p.bias, p.bias_f32, col0, p.N, b, p.bias_vec != 0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v2[i] = ptx::add2(v2[i], ptx::pack2(b[2 * i], b[2 * i + 1]));
                     }
@@ -776,24 +845,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = apply_act(1, v[i]);
                     }
-                    if (col0 + kEpiChunk <= p.N || p.d_inner_aligned) {
-                        // The staging buffer is free once its previous store has read it.
-                        if (lane == 0) ptx::bulk_wait_group_read<1>();
-                        __syncwarp();
-                        stage_row(stage_base + sb * kStageBufBytes, lane, p.d_f32, v);
+                    // The staging buffer is free once its previous TMA store has read it.
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint8_t* const buf = stage_base + sb * kStageBufBytes;
+                    stage_row(buf, lane, p.d_f32, v);
+                    if (p.d_tma && (col0 + kEpiChunk <= p.N || p.d_inner_aligned)) {
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmD, stage_base + sb * kStageBufBytes, col0, m0 + g * 32);
+                            ptx::tma_store_2d(&p.tmD, buf, col0, m0 + g * 32);
                             ptx::bulk_commit_group();
                         }
-                        sb ^= 1;
-                    } else if (row_ok) {
-                        // Ragged last chunk with N not a multiple of 16 bytes:
-                        // the TMA store clips the inner dimension only to 16-byte
-                        // granularity, so write the valid columns one by one.
-                        store_row_tail(p, grow, col0, v);
+                    } else {
+                        __syncwarp();
+                        store_chunk_direct(p, buf, m0 + g * 32, col0, lane);
+                        __syncwarp();
                     }
+                    sb ^= 1;
                 }
             }
             // Hand the accumulator back to the MMA issuer.

@@ -23,6 +23,7 @@
 
 #include "../../include/tcgemm.h"
 #include "gemm_kernel.cuh"
+#include "pack_kernel.cuh"
 
 namespace {
 
@@ -81,6 +82,36 @@ bool is_ab_type(tcg_dtype t) { return t == TCG_BF16 || t == TCG_F16 || is_fp8(t)
 uint32_t mma_format(tcg_dtype t) { return (t == TCG_BF16 || t == TCG_E5M2) ? 1u : 0u; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, int bytes) { return (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(bytes)) == 0; }
+
+// A matrix the TMA can stream as stored: 16-byte aligned base and row pitch.
+bool tma_addressable(const void* p, long long ld, int eb) { return aligned16(p) && (ld * eb) % 16 == 0; }
+
+// Operand storage as rows: `outer` rows of `inner` contiguous elements.
+struct Rows {
+    long long inner = 0, outer = 0;
+};
+Rows operand_rows(int rows, int cols, tcg_layout op) {  // logical rows x cols, stored per op
+    Rows r;
+    r.inner = op == TCG_ROW ? cols : rows;
+    r.outer = op == TCG_ROW ? rows : cols;
+    return r;
+}
+
+// Leading dimension (elements) of the packed copy: rows padded to 16 bytes.
+long long packed_ld(long long inner, int eb) {
+    const long long q = 16 / eb;
+    return std::max(q, (inner + q - 1) / q * q);
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace bytes of the packed copy of an operand the TMA cannot address (0 otherwise).
+size_t pack_bytes(int rows, int cols, tcg_layout op, const void* ptr, long long ld, int eb) {
+    if (rows <= 0 || cols <= 0 || tma_addressable(ptr, ld, eb)) return 0;
+    const Rows r = operand_rows(rows, cols, op);
+    return round256(static_cast<size_t>(r.outer) * static_cast<size_t>(packed_ld(r.inner, eb)) * eb);
+}
 
 // ------------------------------------------------------------ device info
 
@@ -408,17 +439,15 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
     if (ldd < N) return TCG_ERR_INVALID_ARG;
     if (has_c && ldc < N) return TCG_ERR_INVALID_ARG;
     if (is_fp8(ab_dtype) && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
-    // 16-byte rule for every pointer and every leading dimension in bytes
+    // Every pointer aligned to its element size.  Operands and outputs whose
+    // base or row pitch is not a multiple of 16 bytes are still implemented:
+    // A and B through a packed copy in the workspace, C, D and bias through
+    // element-wise loads and stores in the epilogue.
     const int eb = elem_bytes(ab_dtype);
-    if (K > 0) {
-        if (!aligned16(A) || !aligned16(B)) return TCG_ERR_MISALIGNED;
-        if ((static_cast<long long>(lda) * eb) % 16 || (static_cast<long long>(ldb) * eb) % 16)
-            return TCG_ERR_MISALIGNED;
-    }
-    if (!aligned16(D) || (static_cast<long long>(ldd) * elem_bytes(d_dtype)) % 16) return TCG_ERR_MISALIGNED;
-    if (has_c && (!aligned16(C) || (static_cast<long long>(ldc) * elem_bytes(c_dtype)) % 16))
-        return TCG_ERR_MISALIGNED;
-    if (epi.bias && !aligned16(epi.bias)) return TCG_ERR_MISALIGNED;
+    if (K > 0 && (!aligned_to(A, eb) || !aligned_to(B, eb))) return TCG_ERR_MISALIGNED;
+    if (!aligned_to(D, elem_bytes(d_dtype))) return TCG_ERR_MISALIGNED;
+    if (has_c && !aligned_to(C, elem_bytes(c_dtype))) return TCG_ERR_MISALIGNED;
+    if (epi.bias && !aligned_to(epi.bias, elem_bytes(epi.bias_dtype))) return TCG_ERR_MISALIGNED;
     return TCG_OK;
 }
 
@@ -435,6 +464,15 @@ size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
     if (M == 0 || N == 0) return kHeaderBytes;
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
     return kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+}
+
+size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const void* A, int lda, tcg_layout opA,
+                              const void* B, int ldb, tcg_layout opB) {
+    const size_t base = tcg_workspace_size(M, N, K, ab_dtype);
+    if (base == 0 || M == 0 || N == 0 || K == 0) return base;
+    if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return 0;
+    const int eb = elem_bytes(ab_dtype);
+    return base + pack_bytes(M, K, opA, A, lda, eb) + pack_bytes(K, N, opB, B, ldb, eb);
 }
 
 tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -473,12 +511,56 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         g_last_error = buf;
         return TCG_ERR_ARCH;
     }
-    if (scales.col_scale && !aligned16(scales.col_scale)) return TCG_ERR_MISALIGNED;
-    if (scales.row_scale && (reinterpret_cast<uintptr_t>(scales.row_scale) & 3u)) return TCG_ERR_MISALIGNED;
+    if (scales.col_scale && !aligned_to(scales.col_scale, 4)) return TCG_ERR_MISALIGNED;
+    if (scales.row_scale && !aligned_to(scales.row_scale, 4)) return TCG_ERR_MISALIGNED;
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
-    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TCG_ERR_WORKSPACE;
+    const int eb = elem_bytes(ab_dtype);
+    const size_t base_need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    const size_t pack_a = K > 0 ? pack_bytes(M, K, opA, A, lda, eb) : 0;
+    const size_t pack_b = K > 0 ? pack_bytes(K, N, opB, B, ldb, eb) : 0;
+    const size_t need = base_need + pack_a + pack_b;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) {
+        if (pack_a + pack_b > 0) {
+            char buf[200];
+            snprintf(buf, sizeof buf,
+                     "A or B is not 16-byte addressable: the packed copy needs a workspace of %zu bytes "
+                     "(tcg_workspace_size_for)", need);
+            g_last_error = buf;
+        }
+        return TCG_ERR_WORKSPACE;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    // Slow path for operands the TMA cannot address: pack them into 16-byte
+    // pitched rows in the workspace (one launch for both), then run the GEMM
+    // on the copies.
+    if (pack_a + pack_b > 0) {
+        tcg::PackParams pp;
+        memset(&pp, 0, sizeof pp);
+        long long chunks_max = 0;
+        auto add_job = [&](const void*& ptr, int& ld, int rows, int cols, tcg_layout op, size_t offset) {
+            const Rows r = operand_rows(rows, cols, op);
+            const long long ldp = packed_ld(r.inner, eb);
+            tcg::PackJob& j = pp.job[pp.njobs++];
+            j.src = static_cast<const uint8_t*>(ptr);
+            j.src_pitch = static_cast<long long>(ld) * eb;
+            j.dst = reinterpret_cast<uint8_t*>(workspace) + offset;
+            j.dst_pitch = ldp * eb;
+            j.rows = r.outer;
+            j.row_bytes = static_cast<int>(r.inner * eb);
+            j.chunks = (j.row_bytes + 15) / 16;
+            j.total = j.rows * j.chunks;
+            chunks_max = std::max(chunks_max, j.total);
+            ptr = j.dst;
+            ld = static_cast<int>(ldp);
+        };
+        if (pack_a) add_job(A, lda, M, K, opA, base_need);
+        if (pack_b) add_job(B, ldb, K, N, opB, base_need + pack_a);
+        const int grid =
+            static_cast<int>(std::max(1LL, std::min<long long>((chunks_max + 255) / 256, dev.num_sms * 8LL)));
+        tcg::pack_rows_kernel<<<grid, 256, 0, stream>>>(pp);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_launch("pack_rows_kernel", e);
+    }
 
     tcg::KernelParams kp;
     memset(&kp, 0, sizeof kp);
@@ -498,9 +580,12 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
             st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
     }
-    st = encode_2d(&kp.tmD, d_dtype, D, N, M, ldd, tcg::kEpiChunk, 32,
-                   d_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-    if (st != TCG_OK) return st;
+    kp.d_tma = tma_addressable(D, ldd, elem_bytes(d_dtype));
+    if (kp.d_tma) {
+        st = encode_2d(&kp.tmD, d_dtype, D, N, M, ldd, tcg::kEpiChunk, 32,
+                       d_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (st != TCG_OK) return st;
+    }
 
     kp.M = M; kp.N = N; kp.K = K;
     kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
@@ -515,6 +600,9 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
     kp.c_f32 = (c_dtype == TCG_F32);
+    kp.c_vec = has_c && tma_addressable(C, ldc, elem_bytes(c_dtype));
+    kp.bias_vec = epi.bias && aligned16(epi.bias);
+    kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
     kp.bias = epi.bias;
     kp.bias_f32 = (epi.bias_dtype == TCG_F32);
     kp.act = static_cast<int>(epi.act);
@@ -626,7 +714,9 @@ extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const v
         scratch = g_noalloc_ptr[device];
     }
     const Plan pl = make_plan(M, N, K, ab_dtype, dev);
-    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    const int eb = elem_bytes(ab_dtype);
+    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl) +
+                        (K > 0 ? pack_bytes(M, K, opA, A, lda, eb) + pack_bytes(K, N, opB, B, ldb, eb) : 0);
     if (need > kNoAllocScratchBytes) {
         char buf[200];
         snprintf(buf, sizeof buf,

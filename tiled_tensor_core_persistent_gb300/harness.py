@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import torch
 
-from . import gemm, workspace_size, workspace_init
+from . import gemm, workspace_size_for, workspace_init
 from .inputs import GemmCase
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn}
@@ -24,24 +24,32 @@ class DeviceCase:
 
     SENTINEL = 1234.5
 
-    def __init__(self, case: GemmCase, device="cuda", guard_rows: int = 0, stream=None):
+    def __init__(self, case: GemmCase, device="cuda", guard_rows: int = 0, stream=None,
+                 offsets: dict | None = None):
+        """offsets: element offsets {"A", "B", "C", "D", "bias"} of each buffer's
+        start from a 256-byte aligned allocation (to exercise unaligned pointers)."""
         self.case = case
         self.device = torch.device(device)
         self.stream = stream
         dev = self.device
-        self.A = case.A.to(dev)
-        self.B = case.B.to(dev)
-        self.C = case.C.to(dev) if case.C is not None else None
-        self.bias = case.bias.to(dev) if case.bias is not None else None
+        off = offsets or {}
+        self.A = _upload(case.A, dev, off.get("A", 0))
+        self.B = _upload(case.B, dev, off.get("B", 0))
+        self.C = _upload(case.C, dev, off.get("C", 0)) if case.C is not None else None
+        self.bias = _upload(case.bias, dev, off.get("bias", 0)) if case.bias is not None else None
         self.row_scale = case.row_scale.to(dev) if case.row_scale is not None else None
         self.col_scale = case.col_scale.to(dev) if case.col_scale is not None else None
         ddt = _TORCH_DTYPE[case.d_dtype]
         self.guard_rows = guard_rows
         rows = max(case.M, 1) + 2 * guard_rows
-        self.D_full = torch.full((rows, max(case.ldd, 1)), self.SENTINEL, dtype=ddt, device=dev)
+        ld = max(case.ldd, 1)
+        self.d_off = off.get("D", 0)
+        self.D_flat = torch.full((self.d_off + rows * ld,), self.SENTINEL, dtype=ddt, device=dev)
+        self.D_full = self.D_flat[self.d_off:].view(rows, ld)
         self.sentinel_stored = float(torch.tensor(self.SENTINEL, dtype=ddt).float())
         self.D_view = self.D_full[guard_rows:guard_rows + case.M]
-        self.ws_bytes = max(workspace_size(case.M, case.N, case.K, case.ab_dtype), 256)
+        self.ws_bytes = max(workspace_size_for(case.M, case.N, case.K, case.ab_dtype, self.A, case.lda,
+                                               case.opA, self.B, case.ldb, case.opB), 256)
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
 
     def run(self, stream=None) -> None:
@@ -63,4 +71,14 @@ class DeviceCase:
         g, M, N = self.guard_rows, self.case.M, self.case.N
         mask = torch.ones_like(full, dtype=torch.bool)
         mask[g:g + M, :N] = False
-        return bool((full[mask] == self.sentinel_stored).all())
+        head = self.D_flat[:self.d_off].to(torch.float32).cpu()
+        return bool((full[mask] == self.sentinel_stored).all()) and bool((head == self.sentinel_stored).all())
+
+
+def _upload(t: torch.Tensor, dev, offset: int) -> torch.Tensor:
+    """Copy t to the device starting `offset` elements into a fresh allocation."""
+    if offset == 0:
+        return t.to(dev)
+    flat = torch.empty((offset + t.numel(),), dtype=t.dtype, device=dev)
+    flat[offset:] = t.reshape(-1).to(dev)
+    return flat[offset:].view(t.shape)

@@ -185,6 +185,19 @@ def ragged(shape_idx: int, combo_idx: int) -> GemmCase:
                      opA=opA, opB=opB, alpha=1.0, beta=0.5, c_dist="uniform")
 
 
+def ragged_tight(combo_idx: int) -> GemmCase:
+    """The 4095 x 3001 x 1537 ragged shape with tight leading dimensions (each
+    ld equal to the contiguous extent, so none is a multiple of 16 bytes):
+    U[-1,1], C U[-1,1], beta=0.5, ldc = ldd = N."""
+    M, N, K = RAGGED_SHAPES[0]
+    opA, opB = LAYOUT_COMBOS[combo_idx]
+    lda = K if opA == "row" else M
+    ldb = N if opB == "row" else K
+    return make_case(f"ragged_tight_{M}x{N}x{K}_{opA}{opB}", M, N, K, seed=105 + combo_idx,
+                     dist="uniform", opA=opA, opB=opB, alpha=1.0, beta=0.5, c_dist="uniform",
+                     lda=lda, ldb=ldb, ldc=N, ldd=N)
+
+
 def fp8_8192_relu() -> GemmCase:
     """8192^3 e4m3 (N(0,1) quantised with amax/448 per tensor), bias N(0,0.1), ReLU, bf16 D."""
     return make_case("gemm8192_e4m3_bias_relu", 8192, 8192, 8192, seed=17, dist="normal",
