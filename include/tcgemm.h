@@ -189,6 +189,20 @@ tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);
 void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2);
 
 /*
+ * tcg_debug_schedule -- TEST-ONLY, needs no GPU: the work schedule tcg_gemm
+ * would run on a device with num_sms SMs.  sk_mode: -1 = the default, 0 = no
+ * Stream-K, 1 = last partial wave plus one full wave as Stream-K, 2 = last
+ * partial wave only, 3 = all tiles.  Writes up to max_rows rows of 9 ints,
+ * one per unit of work in the order each worker runs them:
+ *   {worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, partial slot}
+ * (k-blocks are pipeline stages; partial slot -1 for an unsplit tile) and
+ * returns the number of units (which may exceed max_rows), or -1 for
+ * invalid sizes.
+ */
+int tcg_debug_schedule(int M, int N, int K, tcg_dtype ab_dtype, int num_sms, int sk_mode,
+                       int* rows, int max_rows);
+
+/*
  * tcg_gemm_noalloc -- the same GEMM as tcg_gemm for callers that cannot
  * allocate device memory, so cannot pass a workspace: e.g. plugins that only
  * receive input/output pointers from an engine that owns all device memory,

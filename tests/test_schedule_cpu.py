@@ -1,0 +1,105 @@
+"""The persistent tile schedule (data-parallel units, split-K, Stream-K) as
+tcg_gemm would run it, checked on the host without a GPU.
+
+"CUTLASS" (stanleyjacob.dev), Part IV Stage 2 (a persistent grid walks the
+output tiles) and Stage 6 (split-K / Stream-K partition the K loop and
+reduce the partial tiles).  Invariants checked for every plan:
+  * every (tile, k-block) iteration of the problem is computed exactly once;
+  * the pieces of a tile are numbered 0..nsplit-1, cover its K range in that
+    order, and agree on nsplit;
+  * unsplit tiles write no partial; the partial slots of split pieces are
+    distinct, so no two pieces overwrite each other;
+  * the work is balanced: with Stream-K no worker has more than one
+    k-block iteration above the average.
+"""
+from collections import defaultdict
+
+import pytest
+
+import tiled_tensor_core_persistent_gb300 as tcg
+from tiled_tensor_core_persistent_gb300 import _build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return tcg.lib()
+
+
+SHAPES = [(8192, 8192, 8192), (4096, 4096, 4096), (4095, 3001, 1537), (16, 8192, 8192),
+          (8192, 128, 8192), (512, 512, 512), (300, 200, 129), (1, 1, 1), (2048, 2560, 256),
+          (1000, 9000, 3000)]
+
+
+def check(M, N, K, ab, sms, mode):
+    rows = tcg.debug_schedule(M, N, K, ab, num_sms=sms, sk_mode=mode)
+    assert rows, "empty schedule"
+    plan_tiles = {}
+    pieces = defaultdict(list)
+    for wid, tile, m, n, kb0, kb1, split, nsplit, slot in rows:
+        assert 0 <= kb0 < kb1, (tile, kb0, kb1)
+        key = (m, n)
+        assert plan_tiles.setdefault(tile, key) == key, "a tile index maps to two output tiles"
+        pieces[tile].append((split, kb0, kb1, nsplit, slot, wid))
+    # the tile index -> (m, n) map is one to one and covers the whole output grid
+    assert len(set(plan_tiles.values())) == len(plan_tiles)
+    num_m = max(m for m, _ in plan_tiles.values()) + 1
+    num_n = max(n for _, n in plan_tiles.values()) + 1
+    assert set(plan_tiles.values()) == {(m, n) for m in range(num_m) for n in range(num_n)}
+    assert sorted(plan_tiles) == list(range(num_m * num_n))
+    slots = []
+    num_kb = None
+    per_worker = defaultdict(int)
+    for tile, ps in pieces.items():
+        ps.sort()
+        nsplit = ps[0][3]
+        assert all(p[3] == nsplit for p in ps)
+        assert [p[0] for p in ps] == list(range(nsplit)), (tile, ps)
+        assert ps[0][1] == 0
+        for a, b in zip(ps, ps[1:]):
+            assert a[2] == b[1], "pieces of a tile must be contiguous in K"
+        if num_kb is None:
+            num_kb = ps[-1][2]
+        assert ps[-1][2] == num_kb, "every tile covers the same K range"
+        if nsplit == 1:
+            assert ps[0][4] == -1
+        else:
+            slots += [p[4] for p in ps]
+        for p in ps:
+            per_worker[p[5]] += p[2] - p[1]
+    assert len(slots) == len(set(slots)), "two pieces share a partial slot"
+    assert all(s >= 0 for s in slots)
+    total = sum(per_worker.values())
+    return rows, per_worker, total
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_schedule_covers_every_iteration_once(shape, mode):
+    M, N, K = shape
+    for sms in (152, 148, 7):
+        check(M, N, K, "bf16", sms, mode)
+
+
+@pytest.mark.parametrize("shape", [(4095, 3001, 1537), (4096, 4096, 4096), (8192, 128, 8192), (16, 8192, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_all_tile_stream_k_is_balanced(shape):
+    M, N, K = shape
+    rows, per_worker, total = check(M, N, K, "bf16", 152, 3)
+    workers = len(per_worker)
+    assert max(per_worker.values()) <= -(-total // workers), (max(per_worker.values()), total / workers)
+    assert min(per_worker.values()) >= total // workers
+
+
+def test_partial_wave_stream_k_evens_out_the_last_wave():
+    # 4096^3 with 256 x 256 pair tiles: 256 tiles on 76 pairs leave a last wave of 28
+    rows0, w0, t0 = check(4096, 4096, 4096, "bf16", 152, 0)
+    rows2, w2, t2 = check(4096, 4096, 4096, "bf16", 152, 2)
+    assert t0 == t2
+    assert max(w2.values()) < max(w0.values())
+    assert max(w2.values()) - min(w2.values()) <= 1 + max(r[5] - r[4] for r in rows2)
+
+
+def test_fp8_schedule():
+    check(8192, 8192, 8192, "e4m3", 152, 1)
+    check(4095, 3001, 1537, "e4m3", 152, 3)

@@ -32,7 +32,8 @@ STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "T
           4: "TCG_ERR_ARCH", 5: "TCG_ERR_WORKSPACE", 6: "TCG_ERR_LAUNCH", 7: "TCG_ERR_TIMEOUT"}
 
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
-            "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc"]
+            "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc",
+            "tcg_debug_schedule"]
 
 
 class TcgError(RuntimeError):
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
         L.tcg_plan.restype = i32
         L.tcg_debug_set.argtypes = [i32, ctypes.c_longlong, i32, i32]
         L.tcg_debug_set.restype = None
+        L.tcg_debug_schedule.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int), i32]
+        L.tcg_debug_schedule.restype = i32
         _lib = L
         return L
 
@@ -188,6 +191,18 @@ def plan(M, N, K, ab_dtype="bf16") -> dict:
         raise TcgError(st, "tcg_plan", last_error())
     keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem"]
     return dict(zip(keys, list(out)))
+
+
+def debug_schedule(M, N, K, ab_dtype="bf16", num_sms=152, sk_mode=-1) -> list:
+    """TEST-ONLY: the units of work tcg_gemm would run (see tcg_debug_schedule):
+    a list of (worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, slot)."""
+    L = lib()
+    n = L.tcg_debug_schedule(M, N, K, _enum(ab_dtype, DTYPES), num_sms, sk_mode, None, 0)
+    if n < 0:
+        raise TcgError(1, "tcg_debug_schedule")
+    buf = (ctypes.c_int * (9 * max(n, 1)))()
+    L.tcg_debug_schedule(M, N, K, _enum(ab_dtype, DTYPES), num_sms, sk_mode, buf, n)
+    return [tuple(buf[9 * i:9 * i + 9]) for i in range(n)]
 
 
 def debug_set(fault_inject=0, wait_timeout_ns=0, force_splits=0, force_cta2=0) -> None:

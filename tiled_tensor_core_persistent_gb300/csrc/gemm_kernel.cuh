@@ -41,21 +41,29 @@ constexpr int kNumThreads = 192;      // 6 warps
 constexpr int kEpiWarp0 = 2;          // epilogue warps 2..5
 constexpr int kEpiThreads = 128;
 constexpr int kEpiChunk = 32;         // columns per tcgen05.ld / TMA store box
-constexpr int kStageBufBytes = 4096;  // one 32 x 128-byte staging tile
-constexpr int kEpiBytes = 4 * 2 * kStageBufBytes;
+constexpr int kEpiWarpBytes = 8192;   // per epilogue warp: 2 or 4 chunk buffers
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;
 constexpr int kStatusTimeout = 7;     // == TCG_ERR_TIMEOUT
 
 struct KernelParams {
     CUtensorMap tmA;
     CUtensorMap tmB;
     CUtensorMap tmD;
+    CUtensorMap tmC;      // C as 32 x 32 boxes (when c_tma)
     int M, N, K;
     int num_m_blk, num_n_blk, num_kb;
-    // Units of work: phase A = units_a units over tiles [0, units_a / splits_a),
-    // each tile split into splits_a K ranges; phase B (the tail that would
-    // leave the last wave half empty) = the remaining tiles, split_b ways.
+    // Work, in two phases.  Data-parallel: units [0, units_a) over tiles
+    // [0, units_a / splits), each tile split into `splits` equal K ranges,
+    // unit u on worker u mod workers.  Stream-K: the next sk_tiles tiles as
+    // one run of sk_iters = sk_tiles * num_kb k-block iterations, worker w
+    // taking iterations [w * sk_iters / workers, (w + 1) * sk_iters / workers)
+    // across tile boundaries; a tile shared by several workers is finished by
+    // the last of them to arrive.  (A worker is a CTA, or a CTA pair.)
     int splits, num_units, group_m;
-    int units_a, splits_b;
+    int units_a;
+    int sk_tiles;
+    long long sk_iters;
+    int sk_slot_base;     // first partial slot of the Stream-K phase (2 per worker)
     int a_mn_major, b_mn_major;
     float alpha, beta;
     const void* C;
@@ -70,10 +78,12 @@ struct KernelParams {
     int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
     int d_tma;            // D has a TMA store map (16-byte aligned base and row pitch)
     int c_vec;            // C rows may be read with 16-byte vector loads
+    int c_tma;            // C is read through tmC into the epilogue buffers
+    int epi_nbuf;         // epilogue buffers per warp (2 or 4, 8 KiB in all)
     int bias_vec;         // bias may be read with 16-byte vector loads
     int cs_vec;           // col_scale may be read with 16-byte vector loads
     int stages;
-    float* partials;      // split-K partials: [slot][BN][kBM] (row fastest), slot = (slot_tile + split) * ranks + rank
+    float* partials;      // split-K partials: [slot * ranks + rank][BN][kBM] (row fastest), slot from partial_slot()
     int* tile_counters;   // split-K arrival counters [tile * ranks + rank]
     int* status;          // [0] status, [1] where, [2] block
     long long timeout_ns;
@@ -104,6 +114,7 @@ struct alignas(8) SmemCtl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
+    uint64_t cbar[4][4];  // per epilogue warp, per buffer: C chunk landed
     uint32_t tmem_base;
     int abort_flag;
     int splitk_last;
@@ -149,37 +160,107 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, ok);
 }
 
-// Unit u -> output tile (m_blk, n_blk), K range [kb0, kb1) of its split out
-// of nsplit, and slot_tile, the first partial slot of the tile's splits.
+// One unit of work: output tile (m_blk, n_blk), its K range [kb0, kb1) in
+// k-blocks, and its place among the nsplit pieces of the tile (split).
+// Data-parallel units: slot_tile = first partial slot of the tile's splits.
+// Stream-K pieces: sk = 1, tl = tile index within the Stream-K run,
+// w_first = first worker holding a piece of the tile.
 struct Unit {
     int m_blk, n_blk, tile, split, nsplit, kb0, kb1, slot_tile;
+    int sk, tl, w_first;
 };
 
-__device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
-    Unit w;
-    if (u < p.units_a) {
-        w.tile = u / p.splits;
-        w.split = u - w.tile * p.splits;
-        w.nsplit = p.splits;
-        w.slot_tile = w.tile * p.splits;
-    } else {
-        const int v = u - p.units_a;
-        const int tiles_a = p.units_a / p.splits;
-        w.tile = tiles_a + v / p.splits_b;
-        w.split = v - (v / p.splits_b) * p.splits_b;
-        w.nsplit = p.splits_b;
-        w.slot_tile = (p.splits > 1 ? p.units_a : 0) + (v / p.splits_b) * p.splits_b;
-    }
+// Tile index -> (m_blk, n_blk) in the grouped raster order: groups of
+// group_m block rows, column-major inside a group ("CUTLASS", Part IV
+// Stage 2: swizzled tile order for L2 reuse).
+__host__ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& m_blk, int& n_blk) {
     const int span = p.group_m * p.num_n_blk;
-    const int gid = w.tile / span;
+    const int gid = tile / span;
     const int first_m = gid * p.group_m;
-    const int gsz = min(p.num_m_blk - first_m, p.group_m);
-    const int local = w.tile - gid * span;
-    w.m_blk = first_m + local % gsz;
-    w.n_blk = local / gsz;
+    const int gsz = p.num_m_blk - first_m < p.group_m ? p.num_m_blk - first_m : p.group_m;
+    const int local = tile - gid * span;
+    m_blk = first_m + local % gsz;
+    n_blk = local / gsz;
+}
+
+__host__ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
+    Unit w;
+    w.tile = u / p.splits;
+    w.split = u - w.tile * p.splits;
+    w.nsplit = p.splits;
+    w.slot_tile = w.tile * p.splits;
+    w.sk = 0;
+    w.tl = 0;
+    w.w_first = 0;
+    tile_coords(p, w.tile, w.m_blk, w.n_blk);
     w.kb0 = static_cast<int>((static_cast<long long>(w.split) * p.num_kb) / w.nsplit);
     w.kb1 = static_cast<int>((static_cast<long long>(w.split + 1) * p.num_kb) / w.nsplit);
     return w;
+}
+
+// Stream-K bookkeeping: first iteration of worker w, and the worker that
+// holds iteration i (the largest w with sk_begin(w) <= i).
+__host__ __device__ __forceinline__ long long sk_begin(const KernelParams& p, int w, int workers) {
+    return static_cast<long long>(w) * p.sk_iters / workers;
+}
+__host__ __device__ __forceinline__ int sk_worker_of(const KernelParams& p, long long i, int workers) {
+    return static_cast<int>(((i + 1) * workers - 1) / p.sk_iters);
+}
+
+// Partial slot of piece q of the unit's tile.  Stream-K: each worker owns two
+// slots, one for the piece in the tile where its range starts and one for the
+// piece in the tile where it ends (the only pieces that can be partial).
+__host__ __device__ __forceinline__ int partial_slot(const KernelParams& p, const Unit& w, int q, int workers) {
+    if (!w.sk) return w.slot_tile + q;
+    const int c = w.w_first + q;
+    const bool starts_here = sk_begin(p, c, workers) >= static_cast<long long>(w.tl) * p.num_kb;
+    return p.sk_slot_base + 2 * c + (starts_here ? 0 : 1);
+}
+
+// The sequence of units of one worker: its data-parallel units, then its
+// Stream-K pieces.  Every role of a CTA walks the same sequence.
+struct WorkIter {
+    int u;             // next data-parallel unit
+    long long it;      // next Stream-K iteration
+    long long it_end;
+    int wid, workers;
+};
+
+__host__ __device__ __forceinline__ WorkIter work_begin(const KernelParams& p, int wid, int workers) {
+    WorkIter s;
+    s.u = wid;
+    s.wid = wid;
+    s.workers = workers;
+    s.it = s.it_end = 0;
+    if (p.sk_tiles > 0) {
+        s.it = sk_begin(p, wid, workers);
+        s.it_end = sk_begin(p, wid + 1, workers);
+    }
+    return s;
+}
+
+__host__ __device__ __forceinline__ bool work_next(const KernelParams& p, WorkIter& s, Unit& w) {
+    if (s.u < p.num_units) {
+        w = decode_unit(p, s.u);
+        s.u += s.workers;
+        return true;
+    }
+    if (s.it >= s.it_end) return false;
+    const int tl = static_cast<int>(s.it / p.num_kb);
+    w.sk = 1;
+    w.tl = tl;
+    w.tile = p.units_a / p.splits + tl;
+    tile_coords(p, w.tile, w.m_blk, w.n_blk);
+    w.kb0 = static_cast<int>(s.it - static_cast<long long>(tl) * p.num_kb);
+    const long long rest = w.kb0 + (s.it_end - s.it);
+    w.kb1 = static_cast<int>(rest < p.num_kb ? rest : static_cast<long long>(p.num_kb));
+    w.w_first = sk_worker_of(p, static_cast<long long>(tl) * p.num_kb, s.workers);
+    const int w_last = sk_worker_of(p, static_cast<long long>(tl + 1) * p.num_kb - 1, s.workers);
+    w.nsplit = w_last - w.w_first + 1;
+    w.split = s.wid - w.w_first;
+    w.slot_tile = 0;
+    s.it += w.kb1 - w.kb0;
+    return true;
 }
 
 
@@ -290,6 +371,18 @@ __device__ __forceinline__ uintptr_t c_chunk_addr(const KernelParams& p, int row
            static_cast<uintptr_t>((static_cast<long long>(row) * p.ldc + col0) * (p.c_f32 ? 4 : 2));
 }
 
+// L2 prefetch of one thread's C row segment of a whole tile, columns
+// [col0, min(col0 + ncols, N)): every 128-byte line that holds a byte of it.
+// Issued a tile ahead, so the epilogue's C loads hit L2 instead of DRAM.
+__device__ __forceinline__ void c_prefetch_l2(const KernelParams& p, int row, int col0, int ncols) {
+    if (row >= p.M || col0 >= p.N) return;
+    const int eb = p.c_f32 ? 4 : 2;
+    const uintptr_t s = c_chunk_addr(p, row, col0);
+    const uintptr_t e = s + static_cast<uintptr_t>(min(ncols, p.N - col0) * eb);
+    for (uintptr_t a = s & ~static_cast<uintptr_t>(127); a < e; a += 128)
+        ptx::prefetch_l2(reinterpret_cast<const void*>(a));
+}
+
 __device__ __forceinline__ void c_prefetch(const KernelParams& p, int row, int col0, uint4 (&q)[9]) {
     if (col0 + 32 > p.N) return;
     const uintptr_t s = c_chunk_addr(p, row, col0);
@@ -373,6 +466,39 @@ __device__ __forceinline__ void c_values(const KernelParams& p, int row, int col
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// One thread's row of a C chunk that the TMA brought into an epilogue buffer
+// (the same swizzled layout stage_row writes for D).
+__device__ __forceinline__ void c_row_from_smem(const uint8_t* buf, int row, int c_f32, float (&c)[32]) {
+    if (c_f32) {
+        const uint8_t* rowp = buf + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 q = *reinterpret_cast<const float4*>(rowp + ((k ^ (row & 7)) << 4));
+            c[4 * k + 0] = q.x; c[4 * k + 1] = q.y; c[4 * k + 2] = q.z; c[4 * k + 3] = q.w;
+        }
+    } else {
+        const uint8_t* rowp = buf + row * 64;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((k ^ ((row >> 1) & 3)) << 4));
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                c[8 * k + 2 * h + 0] = bf16_bits_to_float(wv[h] & 0xFFFFu);
+                c[8 * k + 2 * h + 1] = bf16_bits_to_float(wv[h] >> 16);
+            }
+        }
+    }
+}
+
+// Wait until at most n of this thread's bulk store groups still read shared memory.
+__device__ __forceinline__ void bulk_wait_read_at_most(int n) {
+    if (n <= 0) ptx::bulk_wait_group_read<0>();
+    else if (n == 1) ptx::bulk_wait_group_read<1>();
+    else if (n == 2) ptx::bulk_wait_group_read<2>();
+    else ptx::bulk_wait_group_read<3>();
 }
 
 // Write one thread's 32 results (its row of the 32 x 32 chunk) into the
@@ -485,6 +611,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             ptx::mbar_init(&ctl->tmem_empty[a], kCta2 ? 8 : 4);
         }
         ptx::mbar_init(&ctl->drain, 1);
+        for (int w4 = 0; w4 < 4; ++w4)
+            for (int b = 0; b < 4; ++b) ptx::mbar_init(&ctl->cbar[w4][b], 1);
         ctl->abort_flag = 0;
         ctl->splitk_last = 0;
         ptx::fence_mbar_init();
@@ -519,8 +647,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             long long st_wait = 0;
             bool first = true;
             bool ok = true;
-            for (int u = first_unit; ok && u < p.num_units; u += unit_stride) {
-                const Unit w = decode_unit(p, u);
+            WorkIter wi = work_begin(p, first_unit, unit_stride);
+            Unit w;
+            while (ok && work_next(p, wi, w)) {
                 const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1;
                 const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
                 const int b_row = n_blk * BN + static_cast<int>(rank) * kBRows;
@@ -615,8 +744,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool issued_any = false;
             long long st_full = 0, st_acc = 0;
             const long long st_t0 = p.stats ? clock64() : 0;
-            for (int u = first_unit; ok && u < p.num_units; u += unit_stride, ++t) {
-                const Unit w = decode_unit(p, u);
+            WorkIter wi = work_begin(p, first_unit, unit_stride);
+            Unit w;
+            for (; ok && work_next(p, wi, w); ++t) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
                 const int acc = t & 1;
                 const uint32_t acc_phase = (t >> 1) & 1;
@@ -689,24 +819,75 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         // --------------------------------------------------------- epilogue
         const int g = warp & 3;                 // TMEM lane group this warp may access
         const int row_in_tile = g * 32 + lane;  // this thread's accumulator row
-        uint8_t* const stage_base = epi_smem + (warp - kEpiWarp0) * 2 * kStageBufBytes;
-        int sb = 0;
-        int t = 0;
+        // Per warp, a ring of nbuf chunk buffers (8 KiB in all).  Chunk number
+        // cc (counted over the whole launch) uses buffer cc mod nbuf: C's
+        // 32 x 32 box lands there by TMA (when C is read), the thread reads
+        // its row, then writes its D row into the same buffer for the TMA
+        // store.  C boxes are requested L = nbuf / 2 chunks ahead.
+        uint8_t* const ring = epi_smem + (warp - kEpiWarp0) * kEpiWarpBytes;
+        const int nbuf = p.epi_nbuf;
+        const int buf_bytes = kEpiWarpBytes / nbuf;
+        const int lookahead = nbuf / 2;
+        const uint32_t c_box_bytes = p.c_f32 ? 4096u : 2048u;
+        uint64_t* const cbar = ctl->cbar[warp - kEpiWarp0];
+        int cc = 0;             // chunks processed by this warp
+        uint32_t cph = 0;       // phase bit of each C barrier
+        int c_pending = 0;      // C boxes requested and not yet waited for
+        bool mixed = false;     // a chunk was stored without the TMA: wait for every store before reuse
         const bool has_c = p.beta != 0.0f;
+        const bool c_tma = has_c && p.c_tma;
         long long st_ewait = 0, st_ebusy = 0;
-        for (int u = first_unit; u < p.num_units; u += unit_stride, ++t) {
-            const Unit w = decode_unit(p, u);
+        // Request C chunk x (columns col0, this warp's 32 rows at row0) into
+        // buffer x mod nbuf, once the D store that last used it has read it
+        // (n_wait = stores issued after that one).  Whole warp, converged.
+        auto issue_c = [&](int x, int col0, int row0, int n_wait) {
+            ptx::fence_proxy_async_smem();  // this warp's reads of the buffer come first
+            __syncwarp();
+            if (lane == 0) {
+                bulk_wait_read_at_most(mixed ? 0 : n_wait);
+                uint64_t* bar = &cbar[x & (nbuf - 1)];
+                ptx::mbar_arrive_expect_tx(bar, c_box_bytes);
+                ptx::tma_load_2d(ring + (x & (nbuf - 1)) * buf_bytes, &p.tmC, bar, col0, row0);
+            }
+            ++c_pending;
+        };
+        auto wait_c = [&](int x, bool honor_abort) -> bool {
+            const int b = x & (nbuf - 1);
+            const bool ok = warp_wait(&cbar[b], (cph >> b) & 1u, p, ctl, 5, limit, honor_abort);
+            cph ^= 1u << b;
+            --c_pending;
+            return ok;
+        };
+        int t = 0;
+        WorkIter wi = work_begin(p, first_unit, unit_stride);
+        Unit w;
+        for (; work_next(p, wi, w); ++t) {
             const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1, split = w.split;
             const bool split_mode = w.nsplit > 1;
             constexpr int kRanks = kCta2 ? 2 : 1;
             const int counter = w.tile * kRanks + static_cast<int>(rank);
             const int acc = t & 1;
             const uint32_t acc_phase = (t >> 1) & 1;
+            const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
+            const int n0 = n_blk * BN;
+            const int grow = m0 + row_in_tile;
+            const bool row_ok = grow < p.M;
+            const bool warp_rows_live = (m0 + g * 32) < p.M;
+            const int nchunks = min(BN / kEpiChunk, (p.N - n0 + kEpiChunk - 1) / kEpiChunk);
             uint4 cq[9];
-            {
-                const int pre_row = m_blk * kTileM + static_cast<int>(rank) * kBM + (warp & 3) * 32 + lane;
-                if (has_c && pre_row < p.M && n_blk * BN < p.N) c_prefetch(p, pre_row, n_blk * BN, cq);
+            if (has_c) {
+                // C rows of this tile on the first pass, then always of the next tile, into L2
+                if (t == 0) c_prefetch_l2(p, grow, n0, BN);
+                WorkIter peek = wi;
+                Unit nw;
+                if (work_next(p, peek, nw))
+                    c_prefetch_l2(p, nw.m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile, nw.n_blk * BN, BN);
+                if (!c_tma && row_ok) c_prefetch(p, grow, n0, cq);
             }
+            // First C boxes of a tile that is not split, before the accumulator is ready.
+            if (c_tma && !split_mode && warp_rows_live)
+                for (int l = 0; l < lookahead && l < nchunks; ++l)
+                    issue_c(cc + l, n0 + l * kEpiChunk, m0 + g * 32, nbuf - 1 - l);
             const long long te = p.stats ? clock64() : 0;
             bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
             const long long te1 = p.stats ? clock64() : 0;
@@ -717,11 +898,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             if (!ok) break;
             ptx::tc_fence_after_sync();
 
-            const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
-            const int n0 = n_blk * BN;
-            const int grow = m0 + row_in_tile;
-            const bool row_ok = grow < p.M;
-            const bool warp_rows_live = (m0 + g * 32) < p.M;
             const bool have_acc = kb1 > kb0;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(g * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
@@ -732,11 +908,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 // Column-major within the tile: the 32 rows of a warp form one
                 // contiguous 128-byte line per column (coalesced stores/loads).
                 float* slot = p.partials +
-                              (static_cast<size_t>(w.slot_tile + split) * kRanks + rank) * (kBM * BN) +
+                              (static_cast<size_t>(partial_slot(p, w, split, unit_stride)) * kRanks + rank) * (kBM * BN) +
                               row_in_tile;
                 if (warp_rows_live && have_acc) {
-                    for (int j = 0; j < BN / kEpiChunk; ++j) {
-                        if (n0 + j * kEpiChunk >= p.N) break;
+                    for (int j = 0; j < nchunks; ++j) {
                         uint32_t r[32];
                         ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
                         if (row_ok) {
@@ -758,12 +933,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 ptx::named_barrier_sync(1, kEpiThreads);
                 finish = ctl->splitk_last != 0;
                 __threadfence();
+                if (finish && c_tma && warp_rows_live)
+                    for (int l = 0; l < lookahead && l < nchunks; ++l)
+                        issue_c(cc + l, n0 + l * kEpiChunk, m0 + g * 32, nbuf - 1 - l);
             }
 
             if (finish && warp_rows_live) {
-                for (int j = 0; j < BN / kEpiChunk; ++j) {
+                for (int j = 0; j < nchunks; ++j) {
                     const int col0 = n0 + j * kEpiChunk;
-                    if (col0 >= p.N) break;
                     float v[32];
                     if (have_acc || split_mode) {
                         float s[32];
@@ -785,7 +962,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                     }
                                 } else if (row_ok) {
                                     const float* src =
-                                        p.partials + (static_cast<size_t>(w.slot_tile + q) * kRanks + rank) * (kBM * BN) +
+                                        p.partials + (static_cast<size_t>(partial_slot(p, w, q, unit_stride)) * kRanks + rank) * (kBM * BN) +
                                         static_cast<size_t>(j * kEpiChunk) * kBM + row_in_tile;
                                     float pv[32];
 #pragma unroll
@@ -801,6 +978,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
                     }
+                    if (c_tma && j + lookahead < nchunks)
+                        issue_c(cc + lookahead, col0 + lookahead * kEpiChunk, m0 + g * 32, nbuf - 1 - lookahead);
                     // alpha, beta*C, bias and GELU on packed pairs (f32x2)
                     uint64_t v2[16];
 #pragma unroll
@@ -821,13 +1000,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], ptx::pack2(cs[2 * i], cs[2 * i + 1]));
                         }
                     }
-                    if (has_c && row_ok) {
+                    uint8_t* const buf = ring + (cc & (nbuf - 1)) * buf_bytes;
+                    if (has_c) {
                         float c[32];
-                        c_values(p, grow, col0, cq, c);
-                        if (col0 + kEpiChunk < p.N && j + 1 < BN / kEpiChunk) c_prefetch(p, grow, col0 + kEpiChunk, cq);
-                        const uint64_t be = ptx::pack2(p.beta, p.beta);
+                        if (c_tma) {
+                            wait_c(cc, false);
+                            c_row_from_smem(buf, lane, p.c_f32, c);
+                        } else if (row_ok) {
+                            c_values(p, grow, col0, cq, c);
+                            if (j + 1 < nchunks) c_prefetch(p, grow, col0 + kEpiChunk, cq);
+                        }
+                        if (c_tma || row_ok) {
+                            const uint64_t be = ptx::pack2(p.beta, p.beta);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v2[i] = ptx::fma2(be, ptx::pack2(c[2 * i], c[2 * i + 1]), v2[i]);
+                            for (int i = 0; i < 16; ++i) v2[i] = ptx::fma2(be, ptx::pack2(c[2 * i], c[2 * i + 1]), v2[i]);
+                        }
                     }
                     if (p.bias) {
                         float b[32];
@@ -845,10 +1032,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = apply_act(1, v[i]);
                     }
-                    // The staging buffer is free once its previous TMA store has read it.
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    // The buffer is free: with C, every lane has read its C row
+                    // (and the C request waited for the buffer's last store);
+                    // without, once the store that used it nbuf chunks ago has read it.
+                    if (!c_tma && lane == 0) bulk_wait_read_at_most(mixed ? 0 : nbuf - 1);
                     __syncwarp();
-                    uint8_t* const buf = stage_base + sb * kStageBufBytes;
                     stage_row(buf, lane, p.d_f32, v);
                     if (p.d_tma && (col0 + kEpiChunk <= p.N || p.d_inner_aligned)) {
                         ptx::fence_proxy_async_smem();
@@ -861,8 +1049,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         __syncwarp();
                         store_chunk_direct(p, buf, m0 + g * 32, col0, lane);
                         __syncwarp();
+                        mixed = true;
                     }
-                    sb ^= 1;
+                    ++cc;
                 }
             }
             // Hand the accumulator back to the MMA issuer.
@@ -876,6 +1065,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     ptx::mbar_arrive(&ctl->tmem_empty[acc]);
             }
         }
+        // C boxes still in flight (only after an abort) land before the CTA leaves.
+        while (c_pending > 0) wait_c(cc++, false);
         if (lane == 0) ptx::bulk_wait_group<0>();
         if (p.stats && warp == kEpiWarp0 && lane == 0) {
             atomicAdd(p.stats + kStatEpiWaitFull, static_cast<unsigned long long>(st_ewait));

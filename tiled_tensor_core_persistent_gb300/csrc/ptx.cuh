@@ -92,6 +92,16 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
     return r != 0;
 }
 
+// Bring the 128-byte line holding `p` into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// Bring the line holding `p` into this SM's L1 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -50,9 +50,11 @@ const int g_env_stages = env_int("TCG_STAGES");
 const int g_env_stats = env_int("TCG_STATS");
 // TCG_KATOMS = K atoms per stage for pair tiles (1 or 2; default 2).
 const int g_env_katoms = env_int("TCG_KATOMS");
-// TCG_TAIL=1 splits the tiles of a half-empty last wave over K.  Off by
-// default: measured slower on GB300 (4096^3: 102 -> 112 us).
-const int g_env_tail = env_int("TCG_TAIL");
+// TCG_SK: Stream-K schedule.  0 = off (data-parallel tiles, split-K for
+// shapes with too few tiles); 1 = the last partial wave plus one full wave
+// as one Stream-K run, the rest data-parallel; 2 = only the last partial
+// wave; 3 = every tile (also replaces split-K).  Unset = the default below.
+const int g_env_sk = getenv("TCG_SK") ? env_int("TCG_SK") : -1;
 // TCG_NARROW=0 keeps 128/256-wide tiles for small problems (default: narrow them).
 const int g_env_narrow = getenv("TCG_NARROW") ? env_int("TCG_NARROW") : 1;
 
@@ -218,8 +220,8 @@ struct Plan {
     int cluster = 1;
     int katoms = 1;     // 128-byte K atoms per pipeline stage
     int units_a = 0;    // units of the data-parallel phase (tiles x splits)
-    int tail_tiles = 0; // last tiles, split splits_b ways over K to fill the last wave
-    int splits_b = 1;
+    int sk_tiles = 0;   // tiles of the Stream-K phase (the last ones in raster order)
+    int workers = 0;    // CTAs or CTA pairs
 };
 
 int stage_bytes(int bn, bool cta2, int katoms) {
@@ -232,7 +234,7 @@ int fixed_smem_bytes() {
 
 int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 
-Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
+Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1) {
     Plan pl;
     const int bk = tcg::kRowBytes / elem_bytes(ab);
     pl.bn = (N <= 128) ? 128 : 256;
@@ -267,7 +269,7 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
     if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
     if (g_force_cta2 == 2) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
-    pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : 1;
+    pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
     pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
@@ -289,31 +291,37 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev) {
         slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
         if (slots <= 0) slots = dev.num_sms / 2;
     }
-    // When the tiles leave the last wave at most half full, split those last
-    // tiles over K so their pieces fill it (the rest stays data-parallel).
-    if (splits == 1 && g_env_tail && g_force_splits == 0 && tiles > slots) {
+    // Stream-K: balance the k-block iterations of the last tiles over all
+    // workers instead of leaving the last wave partly empty.
+    const int sk_mode = sk_override >= 0 ? sk_override : (g_env_sk >= 0 ? g_env_sk : 0);
+    if (g_force_splits == 0 && pl.num_kb > 0 && sk_mode > 0) {
         const int rem = tiles % slots;
-        if (rem > 0 && 2 * rem <= slots) {
-            const int sb = std::min(std::min(slots / rem, 4), pl.num_kb / 2);
-            if (sb >= 2) {
-                pl.tail_tiles = rem;
-                pl.splits_b = sb;
-                pl.units_a = tiles - rem;
-                pl.units = pl.units_a + rem * sb;
-            }
+        if (sk_mode == 3) {
+            pl.sk_tiles = tiles;
+        } else if (splits == 1 && rem > 0) {
+            pl.sk_tiles = (sk_mode == 1 && tiles >= 2 * slots) ? rem + slots : rem;
+        }
+        // every worker must own at least one iteration (a piece count per
+        // tile then equals the number of workers that touch it)
+        if (static_cast<long long>(pl.sk_tiles) * pl.num_kb < slots) pl.sk_tiles = 0;
+        if (pl.sk_tiles > 0) {
+            pl.splits = 1;
+            pl.units_a = tiles - pl.sk_tiles;
+            pl.units = pl.units_a;
         }
     }
-    pl.grid = (cta2 ? 2 : 1) * std::max(1, std::min(pl.units, slots));
+    pl.workers = pl.sk_tiles > 0 ? slots : std::max(1, std::min(pl.units, slots));
+    pl.grid = (cta2 ? 2 : 1) * pl.workers;
     return pl;
 }
 
 size_t partial_slots(const Plan& pl) {
     const size_t a = pl.splits > 1 ? static_cast<size_t>(pl.units_a) : 0;
-    const size_t b = pl.splits_b > 1 ? static_cast<size_t>(pl.tail_tiles) * pl.splits_b : 0;
+    const size_t b = pl.sk_tiles > 0 ? 2 * static_cast<size_t>(pl.workers) : 0;
     return (a + b) * static_cast<size_t>(pl.cluster);
 }
 
-bool any_split(const Plan& pl) { return pl.splits > 1 || pl.splits_b > 1; }
+bool any_split(const Plan& pl) { return pl.splits > 1 || pl.sk_tiles > 0; }
 
 size_t partial_bytes(const Plan& pl) {
     return partial_slots(pl) * tcg::kBM * pl.bn * sizeof(float);
@@ -590,7 +598,10 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.M = M; kp.N = N; kp.K = K;
     kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
     kp.splits = pl.splits; kp.num_units = pl.units; kp.group_m = pl.group_m;
-    kp.units_a = pl.units_a; kp.splits_b = pl.splits_b;
+    kp.units_a = pl.units_a;
+    kp.sk_tiles = pl.sk_tiles;
+    kp.sk_iters = static_cast<long long>(pl.sk_tiles) * pl.num_kb;
+    kp.sk_slot_base = pl.splits > 1 ? pl.units_a : 0;
     kp.a_mn_major = (opA == TCG_COL); kp.b_mn_major = (opB == TCG_ROW);
     kp.alpha = alpha * scales.scale_a * scales.scale_b;
     kp.ab_fmt = mma_format(ab_dtype);
@@ -601,6 +612,17 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.ldc = ldc;
     kp.c_f32 = (c_dtype == TCG_F32);
     kp.c_vec = has_c && tma_addressable(C, ldc, elem_bytes(c_dtype));
+    kp.c_tma = kp.c_vec;
+    if (kp.c_tma) {
+        st = encode_2d(&kp.tmC, c_dtype, C, N, M, ldc, tcg::kEpiChunk, 32,
+                       c_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (st != TCG_OK) return st;
+    }
+    {
+        // chunk buffers per epilogue warp: 8 KiB over the larger of the C and D boxes
+        const int box = 32 * 32 * std::max(elem_bytes(d_dtype), kp.c_tma ? elem_bytes(c_dtype) : 0);
+        kp.epi_nbuf = tcg::kEpiWarpBytes / box;
+    }
     kp.bias_vec = epi.bias && aligned16(epi.bias);
     kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
     kp.bias = epi.bias;
@@ -626,6 +648,13 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     if (pl.cluster == 2)
         return fp8 ? launch_kernel<256, true, true, 1>(kp, pl, stream)
                    : launch_kernel<256, false, true, 1>(kp, pl, stream);
+    if (pl.katoms == 2) {
+        if (pl.bn == 256)
+            return fp8 ? launch_kernel<256, true, false, 2>(kp, pl, stream)
+                       : launch_kernel<256, false, false, 2>(kp, pl, stream);
+        return fp8 ? launch_kernel<128, true, false, 2>(kp, pl, stream)
+                   : launch_kernel<128, false, false, 2>(kp, pl, stream);
+    }
     switch (pl.bn) {
         case 256:
             return fp8 ? launch_kernel<256, true, false, 1>(kp, pl, stream)
@@ -637,6 +666,37 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
             return fp8 ? launch_kernel<64, true, false, 1>(kp, pl, stream)
                        : launch_kernel<64, false, false, 1>(kp, pl, stream);
     }
+}
+
+int tcg_debug_schedule(int M, int N, int K, tcg_dtype ab_dtype, int num_sms, int sk_mode, int* rows, int max_rows) {
+    if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0 || !is_ab_type(ab_dtype)) return -1;
+    DeviceInfo dev;
+    dev.num_sms = num_sms;
+    dev.max_smem_optin = 232448;
+    const Plan pl = make_plan(M, N, K, ab_dtype, dev, sk_mode);
+    tcg::KernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
+    kp.splits = pl.splits; kp.num_units = pl.units; kp.group_m = pl.group_m;
+    kp.units_a = pl.units_a;
+    kp.sk_tiles = pl.sk_tiles;
+    kp.sk_iters = static_cast<long long>(pl.sk_tiles) * pl.num_kb;
+    kp.sk_slot_base = pl.splits > 1 ? pl.units_a : 0;
+    int n = 0;
+    for (int wid = 0; wid < pl.workers; ++wid) {
+        tcg::WorkIter it = tcg::work_begin(kp, wid, pl.workers);
+        tcg::Unit w;
+        while (tcg::work_next(kp, it, w)) {
+            if (n < max_rows && rows) {
+                int* r = rows + 9 * n;
+                r[0] = wid; r[1] = w.tile; r[2] = w.m_blk; r[3] = w.n_blk; r[4] = w.kb0; r[5] = w.kb1;
+                r[6] = w.split; r[7] = w.nsplit;
+                r[8] = w.nsplit > 1 ? tcg::partial_slot(kp, w, w.split, pl.workers) : -1;
+            }
+            ++n;
+        }
+    }
+    return n;
 }
 
 tcg_status tcg_device_status(void* workspace, void* stream_) {
