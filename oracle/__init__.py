@@ -13,6 +13,8 @@ marshals numpy arrays through ctypes.  What it computes is
 the one-GEMM identity of the "CUTLASS" page (stanleyjacob.dev), Part I, with
 the epilogue of its Part II (LinearCombination), Part IV Stage 5 (bias, GELU,
 dequantisation scale) and Part VII Lab 4 (activation after alpha*AB + beta*C).
+With block scale factors (Part V, block-scaled narrow formats) a(i,k) and
+b(k,j) are first multiplied by the E8M0 scale of their block of `blk` k's.
 """
 from __future__ import annotations
 
@@ -70,6 +72,9 @@ def _load():
         lib.oracle_set_channel_scales.argtypes = [P, P]
         lib.oracle_set_channel_scales.restype = None
         lib.oracle_act_array.argtypes = [i32, P, P, i64]
+        lib.oracle_decode_e8m0_array.argtypes = [P, P, i64]
+        lib.oracle_set_block_scales.argtypes = [P, i64, P, i64, i32]
+        lib.oracle_set_block_scales.restype = None
         _lib = lib
         return lib
 
@@ -106,7 +111,8 @@ class Problem:
 
     def __init__(self, M, N, K, A, lda, opA, B, ldb, opB, alpha=1.0, beta=0.0,
                  C=None, ldc=0, bias=None, act="none", scale_a=1.0, scale_b=1.0,
-                 ab_dtype=None, c_dtype=None, bias_dtype=None, row_scale=None, col_scale=None):
+                 ab_dtype=None, c_dtype=None, bias_dtype=None, row_scale=None, col_scale=None,
+                 sfa=None, sfb=None, block=32):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.A, ab = _storage(A, ab_dtype)
         self.B, ab2 = _storage(B, ab_dtype)
@@ -121,6 +127,12 @@ class Problem:
         self.row_scale = None if row_scale is None else np.ascontiguousarray(row_scale, dtype=np.float32)
         self.col_scale = None if col_scale is None else np.ascontiguousarray(col_scale, dtype=np.float32)
         self.act = ACT[act] if isinstance(act, str) else int(act)
+        # block scale factors: uint8 E8M0 codes, sfa[M][ceil(K/block)], sfb[N][ceil(K/block)]
+        self.sfa = None if sfa is None else np.ascontiguousarray(sfa, dtype=np.uint8)
+        self.sfb = None if sfb is None else np.ascontiguousarray(sfb, dtype=np.uint8)
+        self.block = int(block)
+        if (self.sfa is None) != (self.sfb is None):
+            raise ValueError("block scales come in pairs (sfa and sfb)")
         self.scale_a, self.scale_b = float(scale_a), float(scale_b)
 
     def _args(self):
@@ -131,7 +143,13 @@ class Problem:
                 self.act, self.scale_a, self.scale_b)
 
     def _scales(self):
-        _load().oracle_set_channel_scales(_ptr(self.row_scale), _ptr(self.col_scale))
+        L = _load()
+        L.oracle_set_channel_scales(_ptr(self.row_scale), _ptr(self.col_scale))
+        if self.sfa is None:
+            L.oracle_set_block_scales(None, 0, None, 0, 32)
+        else:
+            L.oracle_set_block_scales(_ptr(self.sfa), self.sfa.shape[1], _ptr(self.sfb), self.sfb.shape[1],
+                                      self.block)
 
     def full(self, nthreads: int = 0) -> np.ndarray:
         out = np.empty((self.M, self.N), dtype=np.float64)
@@ -187,6 +205,13 @@ def decode_e5m2(bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint8)
     out = np.empty(bits.shape, dtype=np.float64)
     _load().oracle_decode_e5m2_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def decode_e8m0(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode_e8m0_array(_ptr(bits), _ptr(out), bits.size)
     return out
 
 

@@ -24,6 +24,16 @@
  * per-column (j) fp32 scale vectors, multiplying the raw sum the same way
  * (the per-channel dequantisation scale of the same Stage 5 paragraph).
  *
+ * Block-scaled operands (same page, Part V "data types and quantization":
+ * block-scaled narrow formats, where a small group of elements shares a scale
+ * factor, modelled as paired data-and-scale operands): each run of `blk`
+ * consecutive k of row i of A shares the scale sa(i, k / blk), and likewise
+ * for column j of B with sb(j, k / blk).  The operand values are then
+ * sa(i, k/blk) * a(i,k) and sb(j, k/blk) * b(k,j), and the sum runs over those
+ * products.  The scale factors are the 8-bit exponents of the OCP Microscaling
+ * formats (E8M0: value 2^(e - 127), e = 255 is NaN), the reading taken where
+ * the page names no format.
+ *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - bias is indexed by the output column j and added before act;
  *   - GELU is the exact erf form 0.5*x*(1+erf(x/sqrt(2)));
@@ -133,6 +143,13 @@ static double decode_f32(const void* p) {
     return (double)x;
 }
 
+/* E8M0 scale factor of the OCP Microscaling formats: an unsigned 8-bit
+ * exponent with bias 127 and no mantissa; 0xFF is NaN. */
+double oracle_decode_e8m0(uint8_t bits) {
+    if (bits == 0xFF) return NAN;
+    return ldexp(1.0, (int)bits - 127);
+}
+
 static double g_bf16_table[65536];
 static double g_f16_table[65536];
 static double g_e4m3_table[256];
@@ -177,6 +194,11 @@ typedef struct {
     /* optional per-row (length M) and per-column (length N) fp32 scales */
     const float* row_scale;
     const float* col_scale;
+    /* optional block scale factors (E8M0 bytes): sfa[i * ld_sfa + k / blk],
+     * sfb[j * ld_sfb + k / blk] */
+    const uint8_t* sfa; long long ld_sfa;
+    const uint8_t* sfb; long long ld_sfb;
+    int blk;
     /* optional instrumented operation counter (tiny problems only) */
     int count_ops;
 } oracle_problem;
@@ -211,6 +233,10 @@ static double element(const oracle_problem* p, int i, int j, long long* n_mul, l
     for (int k = 0; k < p->K; ++k) {
         double a = load_ab(p->A, p->ab_dtype, a_index(p, i, k));
         double b = load_ab(p->B, p->ab_dtype, b_index(p, k, j));
+        if (p->sfa) {
+            a = oracle_decode_e8m0(p->sfa[(long long)i * p->ld_sfa + k / p->blk]) * a;
+            b = oracle_decode_e8m0(p->sfb[(long long)j * p->ld_sfb + k / p->blk]) * b;
+        }
         s = s + a * b;
         if (p->count_ops) { ++*n_mul; ++*n_add; }
     }
@@ -314,6 +340,30 @@ void oracle_set_channel_scales(const float* row_scale, const float* col_scale) {
     g_col_scale = col_scale;
 }
 
+/* Block scale factors for the next oracle_gemm_* call on this thread (NULL =
+ * none): E8M0 bytes, sfa[i * ld_sfa + kb] for row i of A and k-block kb,
+ * sfb[j * ld_sfb + kb] for column j of B, blocks of blk consecutive k. */
+static _Thread_local const uint8_t* g_sfa = NULL;
+static _Thread_local const uint8_t* g_sfb = NULL;
+static _Thread_local long long g_ld_sfa = 0, g_ld_sfb = 0;
+static _Thread_local int g_blk = 32;
+void oracle_set_block_scales(const uint8_t* sfa, long long ld_sfa, const uint8_t* sfb, long long ld_sfb,
+                             int blk) {
+    g_sfa = sfa; g_ld_sfa = ld_sfa;
+    g_sfb = sfb; g_ld_sfb = ld_sfb;
+    g_blk = blk > 0 ? blk : 32;
+}
+
+static void attach_thread_state(oracle_problem* p) {
+    p->row_scale = g_row_scale;
+    p->col_scale = g_col_scale;
+    if (g_sfa && g_sfb) {
+        p->sfa = g_sfa; p->ld_sfa = g_ld_sfa;
+        p->sfb = g_sfb; p->ld_sfb = g_ld_sfb;
+        p->blk = g_blk;
+    }
+}
+
 /* Selected rows x selected columns of D_ref, written to out (nrows x ncols).
  * Returns the number of elements computed, or -1 on allocation failure. */
 long long oracle_gemm_select(PROBLEM_ARGS, const int* rows, int nrows,
@@ -321,8 +371,7 @@ long long oracle_gemm_select(PROBLEM_ARGS, const int* rows, int nrows,
     oracle_problem p = make_problem(M, N, K, alpha, A, lda, opA, B, ldb, opB, ab_dtype,
                                     beta, C, ldc, c_dtype, bias, bias_dtype, act,
                                     scale_a, scale_b);
-    p.row_scale = g_row_scale;
-    p.col_scale = g_col_scale;
+    attach_thread_state(&p);
     return run_positions(&p, rows, nrows, cols, ncols, out, nthreads, NULL, NULL);
 }
 
@@ -335,8 +384,7 @@ long long oracle_gemm_full(PROBLEM_ARGS, double* out, int nthreads, int count_op
                                     beta, C, ldc, c_dtype, bias, bias_dtype, act,
                                     scale_a, scale_b);
     p.count_ops = count_ops;
-    p.row_scale = g_row_scale;
-    p.col_scale = g_col_scale;
+    attach_thread_state(&p);
     int* rows = (int*)malloc(sizeof(int) * (size_t)(M > 0 ? M : 1));
     int* cols = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
     if (!rows || !cols) { free(rows); free(cols); return -1; }
@@ -359,6 +407,9 @@ void oracle_decode_f16_array(const uint16_t* in, double* out, long long n) {
 }
 void oracle_decode_e5m2_array(const uint8_t* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e5m2(in[i]);
+}
+void oracle_decode_e8m0_array(const uint8_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e8m0(in[i]);
 }
 void oracle_act_array(int act, const double* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_act(act, in[i]);

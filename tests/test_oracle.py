@@ -353,3 +353,104 @@ def test_channel_scales_are_row_and_column_factors():
     np.testing.assert_allclose(scaled, base * r[:, None] * c[None, :], rtol=1e-13)
     only_rows = oracle.Problem(M, N, K, a_bits, K, oracle.ROW, b_bits, K, oracle.COL, row_scale=r).full()
     np.testing.assert_allclose(only_rows, base * r[:, None], rtol=1e-13)
+
+
+# ------------------------------------------------------ block-scaled operands
+
+def test_e8m0_decoder_exhaustive_against_torch():
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ours = oracle.decode_e8m0(bits)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 1 and nan[255]
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[127] == 1.0 and ours[128] == 2.0 and ours[126] == 0.5
+
+
+def _mx_case(M, N, K, seed, lo=124, hi=130, fmt="e4m3"):
+    """Integer-valued fp8 elements in [-4, 4] with random E8M0 scale codes."""
+    rng = np.random.default_rng(seed)
+    tdt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    a = torch.from_numpy(rng.integers(-4, 5, (M, K)).astype(np.float32)).to(tdt)
+    b = torch.from_numpy(rng.integers(-4, 5, (N, K)).astype(np.float32)).to(tdt)
+    kb = (K + 31) // 32
+    sfa = rng.integers(lo, hi + 1, (M, kb)).astype(np.uint8)
+    sfb = rng.integers(lo, hi + 1, (N, kb)).astype(np.uint8)
+    return a, b, sfa, sfb
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 4, 33), (5, 2, 70), (2, 6, 96)])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_block_scaled_tiny_exact_rational(M, N, K, fmt):
+    """Every element against exact rational arithmetic: a(i,k) and b(k,j) are
+    multiplied by 2^(code - 127) of their 32-wide block along k (torch decodes
+    the E8M0 codes and the fp8 elements independently of the oracle)."""
+    a, b, sfa, sfb = _mx_case(M, N, K, M * 31 + N * 7 + K, fmt=fmt)
+    dt = oracle.E4M3 if fmt == "e4m3" else oracle.E5M2
+    got = oracle.Problem(M, N, K, a.view(torch.uint8).numpy(), K, oracle.ROW, b.view(torch.uint8).numpy(), K,
+                         oracle.COL, ab_dtype=dt, sfa=sfa, sfb=sfb, alpha=0.5).full(1)
+    av, bv = a.double().numpy(), b.double().numpy()
+    sa = torch.from_numpy(sfa.copy()).view(torch.float8_e8m0fnu).double().numpy()
+    sb = torch.from_numpy(sfb.copy()).view(torch.float8_e8m0fnu).double().numpy()
+    for i in range(M):
+        for j in range(N):
+            ref = sum((Fraction(sa[i, k // 32]) * Fraction(av[i, k]) * Fraction(sb[j, k // 32]) * Fraction(bv[j, k])
+                       for k in range(K)), Fraction(0))
+            assert got[i, j] == float(Fraction(1, 2) * ref), (i, j)
+
+
+def test_unit_block_scales_reduce_to_plain_fp8():
+    M, N, K = 6, 9, 100
+    a, b, sfa, sfb = _mx_case(M, N, K, 3)
+    sfa[:] = 127
+    sfb[:] = 127
+    args = (M, N, K, a.view(torch.uint8).numpy(), K, oracle.ROW, b.view(torch.uint8).numpy(), K, oracle.COL)
+    plain = oracle.Problem(*args, ab_dtype=oracle.E4M3).full()
+    scaled = oracle.Problem(*args, ab_dtype=oracle.E4M3, sfa=sfa, sfb=sfb).full()
+    assert np.array_equal(plain, scaled)
+
+
+def test_one_block_scale_changes_only_its_block():
+    """Raising the scale of block kb of row i of A by one code (x2) adds exactly
+    that block's contribution to row i of D and leaves the other rows alone;
+    the same for a column block of B (no swapped or shifted block index)."""
+    M, N, K = 4, 5, 96
+    a, b, sfa, sfb = _mx_case(M, N, K, 5)
+    args = (M, N, K, a.view(torch.uint8).numpy(), K, oracle.ROW, b.view(torch.uint8).numpy(), K, oracle.COL)
+    base = oracle.Problem(*args, ab_dtype=oracle.E4M3, sfa=sfa, sfb=sfb).full()
+    av, bv = a.double().numpy(), b.double().numpy()
+    sa = 2.0 ** (sfa.astype(np.float64) - 127)
+    sb = 2.0 ** (sfb.astype(np.float64) - 127)
+    i0, j0, kb = 2, 3, 1
+    ks = np.arange(kb * 32, (kb + 1) * 32)
+    sfa2 = sfa.copy()
+    sfa2[i0, kb] += 1
+    d = oracle.Problem(*args, ab_dtype=oracle.E4M3, sfa=sfa2, sfb=sfb).full() - base
+    contrib = np.array([(sa[i0, kb] * av[i0, ks] * sb[j, kb] * bv[j, ks]).sum() for j in range(N)])
+    np.testing.assert_array_equal(d[i0], contrib)
+    assert not np.delete(d, i0, axis=0).any()
+    sfb2 = sfb.copy()
+    sfb2[j0, kb] += 1
+    d = oracle.Problem(*args, ab_dtype=oracle.E4M3, sfa=sfa, sfb=sfb2).full() - base
+    contrib = np.array([(sa[i, kb] * av[i, ks] * sb[j0, kb] * bv[j0, ks]).sum() for i in range(M)])
+    np.testing.assert_array_equal(d[:, j0], contrib)
+    assert not np.delete(d, j0, axis=1).any()
+
+
+def test_mx_quantiser_and_blocked_layout():
+    """The input generator's OCP MX quantisation keeps every value within the
+    element format's relative step of its source, and the blocked scale layout
+    is a permutation that puts (row r, column c) where the library reads it."""
+    x = torch.randn((7, 70), generator=torch.Generator().manual_seed(0))
+    q, codes = inputs.mx_quantize(x, "e4m3")
+    scale = torch.from_numpy(codes.astype(np.float32) - 127).exp2().repeat_interleave(32, dim=1)[:, :70]
+    deq = q.to(torch.float32) * scale
+    assert torch.all((deq - x).abs() <= 2.0 ** -3 * x.abs() + 2.0 ** -9 * scale)
+    sf = np.arange(300 * 9, dtype=np.int64).reshape(300, 9) % 251
+    blk = inputs.mx_blocked_layout(sf.astype(np.uint8))
+    assert blk.size == 384 * 12
+    for r in (0, 31, 32, 127, 128, 299):
+        for c in (0, 3, 4, 8):
+            off = ((r // 128) * 3 + c // 4) * 512 + (r % 32) * 16 + (r % 128) // 32 * 4 + c % 4
+            assert blk[off] == sf[r, c] % 251

@@ -87,6 +87,8 @@ class GemmCase:
     scale_b: float = 1.0
     row_scale: Optional[torch.Tensor] = None   # fp32 [M] dequantisation scale per row
     col_scale: Optional[torch.Tensor] = None   # fp32 [N] dequantisation scale per column
+    sfa: Optional[np.ndarray] = None           # uint8 E8M0 [M][ceil(K/32)] block scales of A's rows
+    sfb: Optional[np.ndarray] = None           # uint8 E8M0 [N][ceil(K/32)] block scales of B's columns
     ldd: int = 0
     meta: dict = field(default_factory=dict)
 
@@ -107,17 +109,76 @@ def _draw(gen, shape, dist, K):
     raise ValueError(dist)
 
 
+MX_BLOCK = 32
+# largest power-of-two exponent of each element format (e4m3: 448 = 1.75 * 2^8)
+_EMAX = {"e4m3": 8, "e5m2": 15}
+
+
+def mx_quantize(x: torch.Tensor, fmt: str, scale_dist: Optional[tuple] = None, gen=None):
+    """OCP Microscaling quantisation along the last axis in blocks of 32:
+    shared exponent E = floor(log2(amax of the block)) - emax(fmt), scale code
+    E + 127 (E8M0), elements fp8(clamp(x / 2^E)).  All-zero blocks get scale 1.
+    scale_dist = (lo, hi): instead draw each scale code uniformly in [lo, hi]
+    and quantise x / 2^E with it (for integer-valued tests).  Returns the
+    element codes (same shape, fp8 dtype) and the uint8 scale codes
+    [..., ceil(n / 32)]."""
+    n = x.shape[-1]
+    nb = (n + MX_BLOCK - 1) // MX_BLOCK
+    pad = nb * MX_BLOCK - n
+    xp = torch.nn.functional.pad(x, (0, pad)).reshape(*x.shape[:-1], nb, MX_BLOCK)
+    if scale_dist is None:
+        amax = xp.abs().amax(dim=-1)
+        e = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))),
+                        torch.zeros_like(amax)) - _EMAX[fmt]
+        e = torch.where(amax > 0, e, torch.zeros_like(e)).clamp(-127, 127)
+    else:
+        lo, hi = scale_dist
+        e = torch.randint(lo, hi + 1, xp.shape[:-1], generator=gen, dtype=torch.int64).to(torch.float32) - 127
+    q = (xp / torch.exp2(e)[..., None]).clamp(-FP8_MAX[fmt], FP8_MAX[fmt])
+    q = q.reshape(*x.shape[:-1], nb * MX_BLOCK)[..., :n].to(_TORCH[fmt])
+    codes = (e + 127).to(torch.uint8).numpy()
+    return q, codes
+
+
+def mx_blocked_layout(sf: np.ndarray, rows_pad: int = 128, kb_pad: int = 4) -> np.ndarray:
+    """The scale-factor layout the library reads (a permutation, no arithmetic):
+    rows padded to a multiple of 128 and scale columns to a multiple of 4;
+    for each block of 128 rows x 4 scale columns, 512 consecutive bytes, the
+    byte of (row r, column c) at (r % 32) * 16 + (r % 128) // 32 * 4 + c % 4;
+    blocks ordered by row block, then column block.  Padding bytes are 127."""
+    R, C = sf.shape
+    Rp = (R + rows_pad - 1) // rows_pad * rows_pad
+    Cp = (C + kb_pad - 1) // kb_pad * kb_pad
+    full = np.full((Rp, Cp), 127, dtype=np.uint8)
+    full[:R, :C] = sf
+    # [rb][r32_hi(4)][r32_lo(32)][cb][c4] -> [rb][cb][r32_lo][r32_hi][c4]
+    t = full.reshape(Rp // 128, 4, 32, Cp // 4, 4).transpose(0, 3, 2, 1, 4)
+    return np.ascontiguousarray(t).reshape(-1)
+
+
 def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
               ab_dtype="bf16", d_dtype="bf16", alpha=1.0, beta=0.0, c_dist=None,
               c_dtype="bf16", bias_std=None, bias_dtype="bf16", act="none",
-              lda=None, ldb=None, ldc=None, ldd=None, channel_scales=False) -> GemmCase:
+              lda=None, ldb=None, ldc=None, ldd=None, channel_scales=False,
+              block_scaled=False, mx_scale_codes=None) -> GemmCase:
     """Draw one GEMM problem.  Order of draws: A, B, C, bias, channel scales
-    (all from `seed`).  channel_scales: fp32 row and column scales U[0.5, 2]."""
+    (all from `seed`).  channel_scales: fp32 row and column scales U[0.5, 2].
+    block_scaled (fp8 operands, A row-major, B column-major): OCP MX blocks of
+    32 along K with E8M0 scales (mx_quantize); mx_scale_codes = (lo, hi) draws
+    the scale codes instead (after A and B, before C)."""
     gen = torch.Generator().manual_seed(int(seed))
     a = _draw(gen, (M, K), dist, K)
     b = _draw(gen, (K, N), dist, K)
     scale_a = scale_b = 1.0
-    if ab_dtype in FP8_MAX and dist != "int4":
+    sfa = sfb = None
+    if block_scaled:
+        if ab_dtype not in FP8_MAX or opA != "row" or opB != "col":
+            raise ValueError("block-scaled cases are fp8 with A row-major and B column-major")
+        qa, sfa = mx_quantize(a, ab_dtype, mx_scale_codes, gen)
+        qb, sfb = mx_quantize(b.t().contiguous(), ab_dtype, mx_scale_codes, gen)
+        a = qa.to(torch.float32)
+        b = qb.to(torch.float32).t()
+    elif ab_dtype in FP8_MAX and dist != "int4":
         # per-tensor scale amax/fmax, then the quantised codes (the harness does
         # this, not the library): q = fp8(clamp(x / scale, -fmax, fmax)), fmax =
         # 448 (e4m3) or 57344 (e5m2).  Integer draws in [-4, 4] are FP8 codes
@@ -149,7 +210,7 @@ def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
                     d_dtype=d_dtype, A=A, lda=lda, B=B, ldb=ldb, alpha=alpha, beta=beta,
                     C=C, ldc=ldc, c_dtype=c_dtype, bias=bias, bias_dtype=bias_dtype,
                     act=act, scale_a=scale_a, scale_b=scale_b, row_scale=row_scale,
-                    col_scale=col_scale, ldd=ldd, meta={"seed": seed, "dist": dist})
+                    col_scale=col_scale, ldd=ldd, sfa=sfa, sfb=sfb, meta={"seed": seed, "dist": dist})
 
 
 # The workloads, with their sizes and value recipes.  Seeds are fixed per case.
@@ -196,6 +257,13 @@ def ragged_tight(combo_idx: int) -> GemmCase:
     return make_case(f"ragged_tight_{M}x{N}x{K}_{opA}{opB}", M, N, K, seed=105 + combo_idx,
                      dist="uniform", opA=opA, opB=opB, alpha=1.0, beta=0.5, c_dist="uniform",
                      lda=lda, ldb=ldb, ldc=N, ldd=N)
+
+
+def mxfp8_8192_relu(fmt: str = "e4m3") -> GemmCase:
+    """8192^3 MXFP8 (N(0,1) quantised in blocks of 32 along K with E8M0 scales),
+    bias N(0,0.1), ReLU, bf16 D."""
+    return make_case(f"gemm8192_mx{fmt}_bias_relu", 8192, 8192, 8192, seed=18, dist="normal",
+                     ab_dtype=fmt, bias_std=0.1, act="relu", block_scaled=True)
 
 
 def fp8_8192_relu() -> GemmCase:
