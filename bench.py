@@ -69,6 +69,7 @@ WORKLOADS = {
     "skinny_16x8192x8192": (lambda inputs: inputs.ragged(1, 1), True),
     "skinny_8192x128x8192": (lambda inputs: inputs.ragged(2, 1), True),
     "gemm8192_e4m3_bias_relu": (lambda inputs: inputs.fp8_8192_relu(), True),
+    "gemm8192_mxe4m3_bias_relu": (lambda inputs: inputs.mxfp8_8192_relu("e4m3"), True),
 }
 
 def metric_name(workload):
@@ -237,7 +238,8 @@ def oracle_problem(case):
         alpha=case.alpha, beta=case.beta, C=inputs.raw_bits(case.C), ldc=case.ldc,
         bias=inputs.raw_bits(case.bias), act=case.act, scale_a=case.scale_a, scale_b=case.scale_b,
         ab_dtype=ab[case.ab_dtype], c_dtype=vec[case.c_dtype] if case.C is not None else None,
-        bias_dtype=vec[case.bias_dtype] if case.bias is not None else None)
+        bias_dtype=vec[case.bias_dtype] if case.bias is not None else None,
+        sfa=case.sfa, sfb=case.sfb, block=inputs.MX_BLOCK)
 
 
 def cpu_oracle_rows(case, rows, nthreads=0, prob=None):
@@ -403,7 +405,7 @@ def run_ours(args):
                "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{nrows} full rows of D ({nrows}x{case.N}x{case.K}), {t:.1f} s wall"}
 
-    plan = tcg.plan(case.M, case.N, case.K, case.ab_dtype)
+    plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
     if rank == 0:
         line = {"metric": metric_name(args.workload),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -418,16 +420,23 @@ def run_ours(args):
     return 0
 
 
+def inputs_blocked(sf):
+    from tiled_tensor_core_persistent_gb300 import inputs
+    return inputs.mx_blocked_layout(sf)
+
+
 def run_e2e(args, case, dc, stream, device, tcg):
     import torch
     A_h = case.A.pin_memory()
     B_h = case.B.pin_memory()
     bias_h = case.bias.pin_memory() if case.bias is not None else None
     C_h = case.C.pin_memory() if case.C is not None else None
+    sf_h = [(torch.from_numpy(inputs_blocked(x)).pin_memory(), dev) for x, dev in ((case.sfa, dc.sfa), (case.sfb, dc.sfb))
+            if x is not None]
     D_h = torch.empty(dc.D_view.shape, dtype=dc.D_view.dtype).pin_memory()
     h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size() + \
         (bias_h.numel() * bias_h.element_size() if bias_h is not None else 0) + \
-        (C_h.numel() * C_h.element_size() if C_h is not None else 0)
+        (C_h.numel() * C_h.element_size() if C_h is not None else 0) + sum(h.numel() for h, _ in sf_h)
     d2h = D_h.numel() * D_h.element_size()
 
     def step():
@@ -438,6 +447,8 @@ def run_e2e(args, case, dc, stream, device, tcg):
                 dc.bias.copy_(bias_h, non_blocking=True)
             if C_h is not None:
                 dc.C.copy_(C_h, non_blocking=True)
+            for h, dev in sf_h:
+                dev.copy_(h, non_blocking=True)
             dc.run(stream)
             D_h.copy_(dc.D_view, non_blocking=True)
 
@@ -455,7 +466,7 @@ def run_e2e(args, case, dc, stream, device, tcg):
     ms = ev0.elapsed_time(ev1) / n
     return {"value": case.flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
-            "path": "pinned host A, B, C, bias -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
+            "path": "pinned host A, B, C, bias, block scales -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
 
 
 def main():

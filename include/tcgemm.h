@@ -61,9 +61,17 @@ typedef enum {
 
 typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
 
-/* Operands A and B: BF16, F16, E4M3 or E5M2 (both the same).  C, D and bias:
- * BF16 or F32.  E4M3 / E5M2 are the FP8 formats (e4m3 without infinities). */
-typedef enum { TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2, TCG_F16 = 3, TCG_E5M2 = 4 } tcg_dtype;
+/* Operands A and B: BF16, F16, E4M3, E5M2, MXE4M3 or MXE5M2 (both the same).
+ * C, D and bias: BF16 or F32.  E4M3 / E5M2 are the FP8 formats (e4m3 without
+ * infinities).  MXE4M3 / MXE5M2 are block-scaled FP8 (the OCP Microscaling
+ * formats MXFP8): E4M3 / E5M2 elements plus one E8M0 scale (2^(e - 127)) per
+ * 32 consecutive K of each A row and each B column, passed in
+ * tcg_scales.block_sfa / block_sfb ("CUTLASS" page, Part V: block-scaled
+ * narrow formats, where a small group of elements shares a scale factor). */
+typedef enum {
+    TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2, TCG_F16 = 3, TCG_E5M2 = 4,
+    TCG_MXE4M3 = 5, TCG_MXE5M2 = 6
+} tcg_dtype;
 
 typedef enum { TCG_ACT_NONE = 0, TCG_ACT_RELU = 1, TCG_ACT_GELU = 2 } tcg_act;
 
@@ -81,21 +89,36 @@ typedef struct {
  * multiplied by alpha * scale_a * scale_b * row_scale[i] * col_scale[j].
  * scale_a / scale_b: per-tensor (1.0 when unused).  row_scale: NULL or a
  * device vector of M fp32 values; col_scale: NULL or a device vector of N
- * fp32 values (both 4-byte aligned).  Any operand type. */
+ * fp32 values (both 4-byte aligned).  Any operand type.
+ *
+ * block_sfa / block_sfb: the E8M0 block scales of MXE4M3 / MXE5M2 operands
+ * (NULL otherwise; required for them when K > 0), device memory, 16-byte
+ * aligned.  Scale (r, c) belongs to row r of A (column r of B) and to K
+ * elements [32 c, 32 c + 32).  Layout: rows padded to a multiple of 128,
+ * scale columns to a multiple of 4 (padding: any finite code); each block of
+ * 128 rows x 4 columns is 512 consecutive bytes holding (r, c) at byte
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4); block (row block rb, column
+ * block cb) starts at byte (rb * ceil(K / 128) + cb) * 512.  This is the
+ * order in which the tensor cores read them, so the kernel copies each block
+ * unchanged. */
 typedef struct {
     float scale_a;
     float scale_b;
     const float* row_scale;
     const float* col_scale;
+    const void* block_sfa;
+    const void* block_sfb;
 } tcg_scales;
 
 /*
  * tcg_can_implement -- argument validation only (no GPU access, no launch).
  * TCG_OK also for unaligned leading dimensions (the slow path above).
  *   M, N, K        : problem size, >= 0.
- *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3 or TCG_E5M2 (A and B share
- *                    it).  The 8-bit types require opA = TCG_ROW and
- *                    opB = TCG_COL (both K-contiguous).
+ *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3, TCG_E5M2, TCG_MXE4M3 or
+ *                    TCG_MXE5M2 (A and B share it).  The 8-bit types
+ *                    require opA = TCG_ROW and opB = TCG_COL (both
+ *                    K-contiguous); the MX types also a 16-byte aligned A and
+ *                    B with lda, ldb multiples of 16 (else TCG_ERR_UNSUPPORTED).
  *   A, lda, opA    : operand A; lda >= K (ROW) or >= M (COL).
  *   B, ldb, opB    : operand B; ldb >= N (ROW) or >= K (COL).
  *   has_c, C, ldc, c_dtype : has_c != 0 when beta != 0; then C row-major,

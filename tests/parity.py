@@ -24,7 +24,8 @@ def oracle_for(case: inputs.GemmCase) -> oracle.Problem:
         ab_dtype=_AB[case.ab_dtype], c_dtype=_VEC[case.c_dtype] if case.C is not None else None,
         bias_dtype=_VEC[case.bias_dtype] if case.bias is not None else None,
         row_scale=None if case.row_scale is None else case.row_scale.numpy(),
-        col_scale=None if case.col_scale is None else case.col_scale.numpy())
+        col_scale=None if case.col_scale is None else case.col_scale.numpy(),
+        sfa=case.sfa, sfb=case.sfb, block=inputs.MX_BLOCK)
 
 
 def assert_within(got: np.ndarray, ref: np.ndarray, tol: float, what: str = "") -> float:

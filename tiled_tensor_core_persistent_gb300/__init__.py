@@ -21,10 +21,11 @@ import threading
 from . import _build
 
 ROW, COL = 0, 1
-BF16, E4M3, F32, F16, E5M2 = 0, 1, 2, 3, 4
+BF16, E4M3, F32, F16, E5M2, MXE4M3, MXE5M2 = 0, 1, 2, 3, 4, 5, 6
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 
-DTYPES = {"bf16": BF16, "e4m3": E4M3, "f32": F32, "f16": F16, "e5m2": E5M2}
+DTYPES = {"bf16": BF16, "e4m3": E4M3, "f32": F32, "f16": F16, "e5m2": E5M2, "mxe4m3": MXE4M3,
+          "mxe5m2": MXE5M2}
 LAYOUTS = {"row": ROW, "col": COL}
 ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
 
@@ -48,7 +49,8 @@ class Epilogue(ctypes.Structure):
 
 class Scales(ctypes.Structure):
     _fields_ = [("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float),
-                ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p)]
+                ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p),
+                ("block_sfa", ctypes.c_void_p), ("block_sfb", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -154,13 +156,15 @@ def workspace_init(workspace, nbytes, stream=None) -> None:
 
 def gemm(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd, d_dtype, *,
          bias=None, bias_dtype="bf16", act="none", ab_dtype="bf16", scale_a=1.0, scale_b=1.0,
-         row_scale=None, col_scale=None, workspace=None, workspace_bytes=0, stream=None) -> None:
+         row_scale=None, col_scale=None, block_sfa=None, block_sfb=None, workspace=None, workspace_bytes=0,
+         stream=None) -> None:
     """Queue D = act(alpha*scale_a*scale_b*(A@B) + beta*C + bias) on `stream` (see tcgemm.h)."""
     epi = Epilogue(_addr(bias), _enum(bias_dtype, DTYPES), _enum(act, ACTS))
     st = lib().tcg_gemm(M, N, K, alpha, _addr(A), lda, _enum(opA, LAYOUTS), _addr(B), ldb,
                         _enum(opB, LAYOUTS), beta, _addr(C), ldc, _enum(c_dtype, DTYPES), _addr(D), ldd,
                         _enum(d_dtype, DTYPES), epi, _enum(ab_dtype, DTYPES),
-                        Scales(scale_a, scale_b, _addr(row_scale), _addr(col_scale)),
+                        Scales(scale_a, scale_b, _addr(row_scale), _addr(col_scale), _addr(block_sfa),
+                               _addr(block_sfb)),
                         _addr(workspace), int(workspace_bytes), _stream(stream))
     if st != 0:
         raise TcgError(st, "tcg_gemm", last_error())
@@ -168,13 +172,14 @@ def gemm(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd
 
 def gemm_noalloc(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd, d_dtype, *,
                  bias=None, bias_dtype="bf16", act="none", ab_dtype="bf16", scale_a=1.0, scale_b=1.0,
-                 row_scale=None, col_scale=None, stream=None) -> None:
+                 row_scale=None, col_scale=None, block_sfa=None, block_sfb=None, stream=None) -> None:
     """tcg_gemm_noalloc: the same GEMM with the library's built-in device scratch (see tcgemm.h)."""
     epi = Epilogue(_addr(bias), _enum(bias_dtype, DTYPES), _enum(act, ACTS))
     st = lib().tcg_gemm_noalloc(M, N, K, alpha, _addr(A), lda, _enum(opA, LAYOUTS), _addr(B), ldb,
                                 _enum(opB, LAYOUTS), beta, _addr(C), ldc, _enum(c_dtype, DTYPES), _addr(D),
                                 ldd, _enum(d_dtype, DTYPES), epi, _enum(ab_dtype, DTYPES),
-                                Scales(scale_a, scale_b, _addr(row_scale), _addr(col_scale)), _stream(stream))
+                                Scales(scale_a, scale_b, _addr(row_scale), _addr(col_scale), _addr(block_sfa),
+                               _addr(block_sfb)), _stream(stream))
     if st != 0:
         raise TcgError(st, "tcg_gemm_noalloc", last_error())
 

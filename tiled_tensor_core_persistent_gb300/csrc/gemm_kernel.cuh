@@ -92,6 +92,12 @@ struct KernelParams {
     uint32_t ab_fmt;            // operand format field of the instruction descriptor
     const float* row_scale;     // optional dequantisation scale per output row (M)
     const float* col_scale;     // optional dequantisation scale per output column (N)
+    // Block scale factors (OCP MX, E8M0 per 32 consecutive K), in 512-byte
+    // blocks of 128 rows x 4 scales: block (row block rb, K atom ka) at
+    // (rb * num_katoms + ka) * 512.  Used by the kMx kernel only.
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    int num_katoms;             // 128-element K atoms per row (ceil(K / 128))
 };
 
 
@@ -570,7 +576,12 @@ __device__ __forceinline__ void store_chunk_direct(const KernelParams& p, const 
 // kKAtoms = 128-byte K atoms per pipeline stage (1 or 2).  Two atoms put
 // twice the MMAs behind each stage handshake (wait, commit), which is what
 // keeps the tensor pipe busy with pair tiles.
-template <int BN, bool kFp8, bool kCta2, int kKAtoms>
+// kMx: block-scaled fp8 operands (1-CTA tiles, BN = 128).  Each stage also
+// carries the tile's scale blocks (512 bytes per 128 rows per K atom, for A
+// and for B), which the MMA thread copies to TMEM with tcgen05.cp before the
+// stage's block-scaled MMAs; TMEM columns [2 BN, ...) hold one 8-column slot
+// (4 for A, 4 for B) per stage and atom.
+template <int BN, bool kFp8, bool kCta2, int kKAtoms, bool kMx = false>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
     constexpr int kBK = kRowBytes / kElemBytes;       // K elements per 128-byte atom
@@ -584,9 +595,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
-    constexpr int kStageBytes = kABytes + kBBytes;
+    static_assert(!kMx || (kFp8 && !kCta2 && BN == 128), "block-scaled tiles are 1-CTA fp8 128 x 128");
+    constexpr int kSfBlock = 512;                          // 128 rows x 4 E8M0 scales
+    constexpr int kSfBytes = kMx ? kKAtoms * 2 * kSfBlock : 0;
+    constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+    static_assert(kStageBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
-    constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr uint32_t kTmemCols = kMx ? 512 : 2 * BN;
+    constexpr int kSfCol0 = 2 * BN;                        // first scale-factor column in TMEM
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -690,6 +706,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int h = 0; h < kBRows / kAtom; ++h)
                                 load(sB + h * kRowBytes * kStageK, &p.tmB, b_row + h * kAtom, k0);
                         }
+                        if constexpr (kMx) {
+                            // scale blocks of this stage's atoms: A's row block, B's column block
+                            uint8_t* sSf = sB + kBBytes;
+#pragma unroll
+                            for (int at = 0; at < kKAtoms; ++at) {
+                                // atoms past K (a last stage of two atoms) reuse the last
+                                // scale block: their elements are zero-filled by the TMA
+                                const int ka = min(kb * kKAtoms + at, p.num_katoms - 1);
+                                ptx::bulk_load(sSf + (2 * at) * kSfBlock,
+                                               p.sfa + (static_cast<size_t>(m_blk) * p.num_katoms + ka) * kSfBlock,
+                                               kSfBlock, fb);
+                                ptx::bulk_load(sSf + (2 * at + 1) * kSfBlock,
+                                               p.sfb + (static_cast<size_t>(n_blk) * p.num_katoms + ka) * kSfBlock,
+                                               kSfBlock, fb);
+                            }
+                        }
                     }
                     if (!skip) {
                         armed |= 1u << stage;
@@ -715,7 +747,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         // ------------------------------------------------------- MMA issuer
         if (leader) {
             const bool issuer = lane == 0;
-            const uint32_t idesc = (1u << 4) | (p.ab_fmt << 7) | (p.ab_fmt << 10) |
+            // Instruction descriptor.  kind::f16 / kind::f8f6f4: D format F32 in
+            // bits 4-5.  Block-scaled kind::mxf8f6f4: bits 4-5 select B's scale
+            // byte, bits 29-30 A's (set per MMA below), bit 23 = E8M0 scales.
+            const uint32_t idesc = (kMx ? (1u << 23) : (1u << 4)) | (p.ab_fmt << 7) | (p.ab_fmt << 10) |
                                    (static_cast<uint32_t>(p.a_mn_major) << 15) |
                                    (static_cast<uint32_t>(p.b_mn_major) << 16) |
                                    (static_cast<uint32_t>(BN >> 3) << 17) |
@@ -765,12 +800,33 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     const uint32_t sB = sA + kABytes;
                     const uint64_t a_desc = ptx::smem_desc_sw128(sA, a_lbo, 1024);
                     const uint64_t b_desc = ptx::smem_desc_sw128(sB, b_lbo, 1024);
+                    uint32_t sf_a = 0, sf_b = 0;
+                    if constexpr (kMx) {
+                        // this stage's scale blocks -> TMEM (slot per stage and atom)
+                        const uint32_t sSf = sB + static_cast<uint32_t>(kBBytes);
+#pragma unroll
+                        for (int at = 0; at < kKAtoms; ++at) {
+                            const uint32_t col = static_cast<uint32_t>(kSfCol0 + (stage * kKAtoms + at) * 8);
+                            ptx::tmem_cp_32x128b_warpx4(tmem_base + col,
+                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + (2 * at) * kSfBlock));
+                            ptx::tmem_cp_32x128b_warpx4(tmem_base + col + 4,
+                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + (2 * at + 1) * kSfBlock));
+                        }
+                        sf_a = tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kKAtoms * 8);
+                        sf_b = sf_a + 4;
+                    }
 #pragma unroll
                     for (int k = 0; k < kKAtoms * kKSteps; ++k) {
                         const uint64_t ad = a_desc + static_cast<uint64_t>(a_off(k));
                         const uint64_t bd = b_desc + static_cast<uint64_t>(b_off(k));
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if constexpr (kCta2) {
+                        if constexpr (kMx) {
+                            // MMA k of atom k / kKSteps uses scale byte k % kKSteps of its slot
+                            const uint32_t sfid = static_cast<uint32_t>(k % kKSteps);
+                            const uint32_t slot = static_cast<uint32_t>((k / kKSteps) * 8);
+                            ptx::mma_mxf8(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), sf_a + slot, sf_b + slot,
+                                          accum);
+                        } else if constexpr (kCta2) {
                             if constexpr (kFp8) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);
                             else ptx::mma_f16_pair(d_tmem, ad, bd, idesc, accum);
                         } else {

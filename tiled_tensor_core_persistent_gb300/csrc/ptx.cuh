@@ -194,6 +194,38 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// Block-scaled MMA (OCP MX operands): D[tmem] (+)= (sA . A) * (sB . B) with
+// one E8M0 scale per 32 consecutive K of each A row and each B column, read
+// from TMEM at sfa_tmem / sfb_tmem (byte chosen by the scale-factor IDs of
+// the instruction descriptor).  kind::mxf8f6f4, one scale per MMA K step.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 32 rows x 128 bits from shared memory (descriptor s_desc) to TMEM at
+// taddr, replicated into the four 32-lane quadrants (lane l of every quadrant
+// receives row l as 4 consecutive 32-bit columns).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// 1-D bulk copy global -> shared (this CTA), `bytes` a multiple of 16 and
+// both addresses 16-byte aligned; completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -354,6 +386,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
            (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
            (2ull << 61);
+}
+
+// Shared-memory descriptor without swizzle for a K-major stack of 8-row x
+// 16-byte core matrices (used for the 32-row scale-factor blocks): both byte
+// offsets are 128, the distance between consecutive core matrices.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle_16b_rows(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128u >> 4) << 16) |
+           (static_cast<uint64_t>(128u >> 4) << 32) | (1ull << 46);
 }
 
 }  // namespace ptx

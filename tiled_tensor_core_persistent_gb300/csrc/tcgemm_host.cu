@@ -71,17 +71,20 @@ int elem_bytes(tcg_dtype t) {
         case TCG_F16: return 2;
         case TCG_E4M3: return 1;
         case TCG_E5M2: return 1;
+        case TCG_MXE4M3: return 1;
+        case TCG_MXE5M2: return 1;
         case TCG_F32: return 4;
     }
     return 0;
 }
 
-bool is_fp8(tcg_dtype t) { return t == TCG_E4M3 || t == TCG_E5M2; }
+bool is_mx(tcg_dtype t) { return t == TCG_MXE4M3 || t == TCG_MXE5M2; }
+bool is_fp8(tcg_dtype t) { return t == TCG_E4M3 || t == TCG_E5M2 || is_mx(t); }
 bool is_ab_type(tcg_dtype t) { return t == TCG_BF16 || t == TCG_F16 || is_fp8(t); }
 
 // Operand format field of the tcgen05 instruction descriptor: kind::f16
 // (F16 = 0, BF16 = 1) and kind::f8f6f4 (E4M3 = 0, E5M2 = 1).
-uint32_t mma_format(tcg_dtype t) { return (t == TCG_BF16 || t == TCG_E5M2) ? 1u : 0u; }
+uint32_t mma_format(tcg_dtype t) { return (t == TCG_BF16 || t == TCG_E5M2 || t == TCG_MXE5M2) ? 1u : 0u; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void* p, int bytes) { return (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(bytes)) == 0; }
@@ -176,6 +179,8 @@ CUtensorMapDataType tma_dtype(tcg_dtype t) {
         case TCG_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         case TCG_E4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         case TCG_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        case TCG_MXE4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        case TCG_MXE5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -224,8 +229,9 @@ struct Plan {
     int workers = 0;    // CTAs or CTA pairs
 };
 
-int stage_bytes(int bn, bool cta2, int katoms) {
-    return katoms * (tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes;
+int stage_bytes(int bn, bool cta2, int katoms, bool mx = false) {
+    // block-scaled stages also hold one 512-byte scale block for A and one for B per atom
+    return katoms * ((tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes + (mx ? 2 * 512 : 0));
 }
 
 int fixed_smem_bytes() {
@@ -237,7 +243,8 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1) {
     Plan pl;
     const int bk = tcg::kRowBytes / elem_bytes(ab);
-    pl.bn = (N <= 128) ? 128 : 256;
+    const bool mx = is_mx(ab);   // block-scaled: 1-CTA 128 x 128 tiles only
+    pl.bn = (N <= 128 || mx) ? 128 : 256;
     // K atoms per stage are decided with the tile shape below; the split-K
     // heuristic works on single-atom k-blocks.
     pl.num_kb = (K + bk - 1) / bk;
@@ -247,7 +254,7 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_
     // tiles would fill less than half of the SMs.  Measured on GB300: 512^3
     // 12.4 -> 10.3 us; for long K, split-K beats narrowing (16x8192x8192:
     // 49 vs 60 us).
-    if (g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && pl.num_kb < 16) {
+    if (!mx && g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && pl.num_kb < 16) {
         while (pl.bn > 64 && num_m1 * ((N + pl.bn - 1) / pl.bn) * 2 < dev.num_sms) pl.bn /= 2;
     }
     const int num_n = (N + pl.bn - 1) / pl.bn;
@@ -267,7 +274,7 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_
     const int num_m2 = (M + 2 * tcg::kBM - 1) / (2 * tcg::kBM);
     bool cta2 = splits == 1 && pl.bn == 256 && M > tcg::kBM && num_m2 * num_n * 2 >= dev.num_sms;
     if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
-    if (g_force_cta2 == 2) cta2 = false;
+    if (g_force_cta2 == 2 || mx) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
     pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
     pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
@@ -281,11 +288,11 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
-    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms);
+    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms, mx);
     stages = std::max(2, std::min(stages, 8));
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
-    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms);
+    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms, mx);
     int slots = dev.num_sms;  // units that run at once
     if (cta2) {
         slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
@@ -332,15 +339,15 @@ size_t counter_bytes(const Plan& pl) {
     return (static_cast<size_t>(pl.num_m) * pl.num_n * pl.cluster * sizeof(int) + 255) / 256 * 256;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA>
+template <int BN, bool kFp8, bool kCta2, int KA, bool kMx = false>
 cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>,
+        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (err == cudaSuccess && kCta2)
-            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>,
+            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     });
     return err;
@@ -386,9 +393,9 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     return n;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA>
+template <int BN, bool kFp8, bool kCta2, int KA, bool kMx = false>
 tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA>();
+    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA, kMx>();
     if (e != cudaSuccess) return fail_launch("cudaFuncSetAttribute", e);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -405,7 +412,7 @@ tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA>, kp);
+    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>, kp);
     if (e != cudaSuccess) return fail_launch("cudaLaunchKernelEx", e);
     return TCG_OK;
 }
@@ -447,6 +454,9 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
     if (ldd < N) return TCG_ERR_INVALID_ARG;
     if (has_c && ldc < N) return TCG_ERR_INVALID_ARG;
     if (is_fp8(ab_dtype) && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
+    if (is_mx(ab_dtype) && K > 0 && (!aligned16(A) || !aligned16(B) || (static_cast<long long>(lda) % 16) ||
+                                     (static_cast<long long>(ldb) % 16)))
+        return TCG_ERR_UNSUPPORTED;  // block-scaled operands take the fast path only
     // Every pointer aligned to its element size.  Operands and outputs whose
     // base or row pitch is not a multiple of 16 bytes are still implemented:
     // A and B through a packed copy in the workspace, C, D and bias through
@@ -521,6 +531,10 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     }
     if (scales.col_scale && !aligned_to(scales.col_scale, 4)) return TCG_ERR_MISALIGNED;
     if (scales.row_scale && !aligned_to(scales.row_scale, 4)) return TCG_ERR_MISALIGNED;
+    if (is_mx(ab_dtype) && K > 0) {
+        if (!scales.block_sfa || !scales.block_sfb) return TCG_ERR_INVALID_ARG;
+        if (!aligned16(scales.block_sfa) || !aligned16(scales.block_sfb)) return TCG_ERR_MISALIGNED;
+    }
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
     const int eb = elem_bytes(ab_dtype);
     const size_t base_need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
@@ -607,6 +621,9 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.ab_fmt = mma_format(ab_dtype);
     kp.row_scale = scales.row_scale;
     kp.col_scale = scales.col_scale;
+    kp.sfa = static_cast<const uint8_t*>(scales.block_sfa);
+    kp.sfb = static_cast<const uint8_t*>(scales.block_sfb);
+    kp.num_katoms = (K + 127) / 128;
     kp.beta = beta;
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
@@ -642,6 +659,10 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = is_fp8(ab_dtype);
+    if (is_mx(ab_dtype)) {
+        return pl.katoms == 2 ? launch_kernel<128, true, false, 2, true>(kp, pl, stream)
+                              : launch_kernel<128, true, false, 1, true>(kp, pl, stream);
+    }
     if (pl.cluster == 2 && pl.katoms == 2)
         return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)
                    : launch_kernel<256, false, true, 2>(kp, pl, stream);

@@ -37,6 +37,13 @@ class DeviceCase:
         self.B = _upload(case.B, dev, off.get("B", 0))
         self.C = _upload(case.C, dev, off.get("C", 0)) if case.C is not None else None
         self.bias = _upload(case.bias, dev, off.get("bias", 0)) if case.bias is not None else None
+        # block-scaled operands: the library reads the E8M0 scales in its blocked layout
+        self.ab_dtype = case.ab_dtype if case.sfa is None else "mx" + case.ab_dtype
+        self.sfa = self.sfb = None
+        if case.sfa is not None:
+            from .inputs import mx_blocked_layout
+            self.sfa = torch.from_numpy(mx_blocked_layout(case.sfa)).to(dev)
+            self.sfb = torch.from_numpy(mx_blocked_layout(case.sfb)).to(dev)
         self.row_scale = case.row_scale.to(dev) if case.row_scale is not None else None
         self.col_scale = case.col_scale.to(dev) if case.col_scale is not None else None
         ddt = _TORCH_DTYPE[case.d_dtype]
@@ -48,7 +55,7 @@ class DeviceCase:
         self.D_full = self.D_flat[self.d_off:].view(rows, ld)
         self.sentinel_stored = float(torch.tensor(self.SENTINEL, dtype=ddt).float())
         self.D_view = self.D_full[guard_rows:guard_rows + case.M]
-        self.ws_bytes = max(workspace_size_for(case.M, case.N, case.K, case.ab_dtype, self.A, case.lda,
+        self.ws_bytes = max(workspace_size_for(case.M, case.N, case.K, self.ab_dtype, self.A, case.lda,
                                                case.opA, self.B, case.ldb, case.opB), 256)
         self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
 
@@ -56,8 +63,9 @@ class DeviceCase:
         c = self.case
         gemm(c.M, c.N, c.K, c.alpha, self.A, c.lda, c.opA, self.B, c.ldb, c.opB, c.beta, self.C,
              c.ldc, c.c_dtype, self.D_view, c.ldd, c.d_dtype, bias=self.bias,
-             bias_dtype=c.bias_dtype, act=c.act, ab_dtype=c.ab_dtype, scale_a=c.scale_a,
+             bias_dtype=c.bias_dtype, act=c.act, ab_dtype=self.ab_dtype, scale_a=c.scale_a,
              scale_b=c.scale_b, row_scale=self.row_scale, col_scale=self.col_scale,
+             block_sfa=self.sfa, block_sfb=self.sfb,
              workspace=self.workspace, workspace_bytes=self.ws_bytes,
              stream=stream if stream is not None else self.stream)
 
