@@ -138,3 +138,32 @@ def test_config_ragged_tight(combo_idx):
     assert_within(got_rows, prob.select(rows, np.arange(N, dtype=np.int32)), TOL["bf16"], case.name + " rows")
     got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
     assert_within(got_cols, prob.select(np.arange(M, dtype=np.int32), cols), TOL["bf16"], case.name + " cols")
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_split_k_with_unaligned_c_and_d(splits):
+    """Split K with C and D rows off the 16-byte grid: the pieces' sums are
+    finished by all four epilogue warps, C read element-wise, D stored without
+    the TMA."""
+    tcg.debug_set(force_splits=splits)
+    try:
+        case = inputs.make_case(f"split_odd{splits}", 200, 301, 1024, seed=140 + splits, dist="uniform",
+                                beta=0.5, c_dist="uniform", ldc=301, ldd=303, bias_std=0.1, act="relu")
+        dc = run(case, offsets={"C": 1})
+        assert_within(dc.result().numpy(), oracle_for(case).full(), TOL["bf16"], case.name)
+        assert dc.untouched_outside()
+    finally:
+        tcg.debug_set()
+
+
+def test_split_k_few_rows_with_c():
+    """16 rows: one live row group, its split sums spread over the four warps."""
+    tcg.debug_set(force_splits=3)
+    try:
+        case = inputs.make_case("split_m16", 16, 520, 1536, seed=151, dist="int4", beta=1.0, c_dist="int4",
+                                c_dtype="f32", d_dtype="f32")
+        dc = run(case)
+        assert np.array_equal(dc.result().numpy(), oracle_for(case).full())
+        assert dc.untouched_outside()
+    finally:
+        tcg.debug_set()

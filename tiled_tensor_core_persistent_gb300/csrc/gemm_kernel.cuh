@@ -938,7 +938,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 Unit nw;
                 if (work_next(p, peek, nw))
                     c_prefetch_l2(p, nw.m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile, nw.n_blk * BN, BN);
-                if (!c_tma && row_ok) c_prefetch(p, grow, n0, cq);
+                if (!c_tma && row_ok && !split_mode) c_prefetch(p, grow, n0, cq);
             }
             // First C boxes of a tile that is not split, before the accumulator is ready.
             if (c_tma && !split_mode && warp_rows_live)
@@ -989,53 +989,81 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 ptx::named_barrier_sync(1, kEpiThreads);
                 finish = ctl->splitk_last != 0;
                 __threadfence();
-                if (finish && c_tma && warp_rows_live)
-                    for (int l = 0; l < lookahead && l < nchunks; ++l)
-                        issue_c(cc + l, n0 + l * kEpiChunk, m0 + g * 32, nbuf - 1 - l);
             }
 
-            if (finish && warp_rows_live) {
-                for (int j = 0; j < nchunks; ++j) {
+            // The chunks this warp finishes, as (row group rg, column chunk j).
+            // Unsplit tile: its own TMEM quadrant (rg = g), every chunk.  Split
+            // tile: every piece's partial (its own included) is in global
+            // memory, so the (row group, chunk) items of the tile's live rows
+            // are dealt round-robin to the four epilogue warps, which then
+            // sum and store in parallel.
+            const int wq = warp - kEpiWarp0;
+            const int live_groups = max(0, min(4, (p.M - m0 + 31) / 32));
+            auto item_of = [&](int k, int& rg, int& jj) -> bool {
+                if (!finish) return false;
+                if (!split_mode) {
+                    if (!warp_rows_live || k >= nchunks) return false;
+                    rg = g;
+                    jj = k;
+                    return true;
+                }
+                const int i = wq + 4 * k;
+                if (i >= live_groups * nchunks) return false;
+                rg = i / nchunks;
+                jj = i - rg * nchunks;
+                return true;
+            };
+            if (has_c && !c_tma && split_mode) {
+                int rg, jj;
+                if (item_of(0, rg, jj) && m0 + rg * 32 + lane < p.M) c_prefetch(p, m0 + rg * 32 + lane, n0 + jj * kEpiChunk, cq);
+            }
+            if (c_tma && split_mode)
+                for (int l = 0; l < lookahead; ++l) {
+                    int rg, jj;
+                    if (!item_of(l, rg, jj)) break;
+                    issue_c(cc + l, n0 + jj * kEpiChunk, m0 + rg * 32, nbuf - 1 - l);
+                }
+            {
+                for (int k = 0;; ++k) {
+                    int rg, j;
+                    if (!item_of(k, rg, j)) break;
                     const int col0 = n0 + j * kEpiChunk;
+                    const int grow = m0 + rg * 32 + lane;
+                    const bool row_ok = grow < p.M;
                     float v[32];
-                    if (have_acc || split_mode) {
-                        float s[32];
+                    if (!split_mode) {
                         uint32_t r[32];
-                        if (have_acc) ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
-                        if (!split_mode) {
+                        if (have_acc) {
+                            ptx::tmem_load_32cols(t_row + static_cast<uint32_t>(j * kEpiChunk), r);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                         } else {
-                            // Fixed order over the splits: the sum does not
-                            // depend on which split arrived last.
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) s[i] = 0.0f;
-                            for (int q = 0; q < w.nsplit; ++q) {
-                                if (q == split) {
-                                    if (have_acc) {
-#pragma unroll
-                                        for (int i = 0; i < 32; ++i) s[i] += __uint_as_float(r[i]);
-                                    }
-                                } else if (row_ok) {
-                                    const float* src =
-                                        p.partials + (static_cast<size_t>(partial_slot(p, w, q, unit_stride)) * kRanks + rank) * (kBM * BN) +
-                                        static_cast<size_t>(j * kEpiChunk) * kBM + row_in_tile;
-                                    float pv[32];
-#pragma unroll
-                                    for (int i = 0; i < 32; ++i) pv[i] = __ldcg(src + i * kBM);
-#pragma unroll
-                                    for (int i = 0; i < 32; ++i) s[i] += pv[i];
-                                }
-                            }
+                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
                         }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = s[i];
                     } else {
+                        // Fixed order over the pieces: the sum does not depend
+                        // on which piece arrived last.
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        if (row_ok) {
+                            for (int q = 0; q < w.nsplit; ++q) {
+                                const float* src =
+                                    p.partials + (static_cast<size_t>(partial_slot(p, w, q, unit_stride)) * kRanks + rank) * (kBM * BN) +
+                                    static_cast<size_t>(j * kEpiChunk) * kBM + rg * 32 + lane;
+                                float pv[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) pv[i] = __ldcg(src + i * kBM);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] += pv[i];
+                            }
+                        }
                     }
-                    if (c_tma && j + lookahead < nchunks)
-                        issue_c(cc + lookahead, col0 + lookahead * kEpiChunk, m0 + g * 32, nbuf - 1 - lookahead);
+                    if (c_tma) {
+                        int rg2, j2;
+                        if (item_of(k + lookahead, rg2, j2))
+                            issue_c(cc + lookahead, n0 + j2 * kEpiChunk, m0 + rg2 * 32, nbuf - 1 - lookahead);
+                    }
                     // alpha, beta*C, bias and GELU on packed pairs (f32x2)
                     uint64_t v2[16];
 #pragma unroll
@@ -1064,7 +1092,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             c_row_from_smem(buf, lane, p.c_f32, c);
                         } else if (row_ok) {
                             c_values(p, grow, col0, cq, c);
-                            if (j + 1 < nchunks) c_prefetch(p, grow, col0 + kEpiChunk, cq);
+                            int rg2, j2;
+                            if (item_of(k + 1, rg2, j2) && m0 + rg2 * 32 + lane < p.M)
+                                c_prefetch(p, m0 + rg2 * 32 + lane, n0 + j2 * kEpiChunk, cq);
                         }
                         if (c_tma || row_ok) {
                             const uint64_t be = ptx::pack2(p.beta, p.beta);
@@ -1098,12 +1128,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmD, buf, col0, m0 + g * 32);
+                            ptx::tma_store_2d(&p.tmD, buf, col0, m0 + rg * 32);
                             ptx::bulk_commit_group();
                         }
                     } else {
                         __syncwarp();
-                        store_chunk_direct(p, buf, m0 + g * 32, col0, lane);
+                        store_chunk_direct(p, buf, m0 + rg * 32, col0, lane);
                         __syncwarp();
                         mixed = true;
                     }
