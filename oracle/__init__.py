@@ -31,7 +31,8 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_OUT_DIR, "libgemm_oracle.so")
 
 ROW, COL = 0, 1
-BF16, E4M3, F32, F16, E5M2 = 0, 1, 2, 3, 4
+BF16, E4M3, F32, F16, E5M2, E2M1 = 0, 1, 2, 3, 4, 5
+SF_E8M0, SF_UE4M3 = 0, 1
 ACT = {"none": 0, "relu": 1, "gelu": 2}
 
 _lock = threading.Lock()
@@ -73,7 +74,9 @@ def _load():
         lib.oracle_set_channel_scales.restype = None
         lib.oracle_act_array.argtypes = [i32, P, P, i64]
         lib.oracle_decode_e8m0_array.argtypes = [P, P, i64]
-        lib.oracle_set_block_scales.argtypes = [P, i64, P, i64, i32]
+        lib.oracle_set_block_scales.argtypes = [P, i64, P, i64, i32, i32]
+        lib.oracle_decode_ue4m3_array.argtypes = [P, P, i64]
+        lib.oracle_decode_e2m1_array.argtypes = [P, P, i64]
         lib.oracle_set_block_scales.restype = None
         _lib = lib
         return lib
@@ -106,13 +109,17 @@ class Problem:
     A is the logical M x K matrix, stored row-major (opA=ROW, element (i,k) at
     i*lda+k) or column-major (opA=COL, element (i,k) at k*lda+i); B is the
     logical K x N matrix with the same convention; C is row-major M x N.
-    Storage arrays hold raw bits: uint16 = bf16, uint8 = e4m3, float32 = f32.
+    Storage arrays hold raw bits: uint16 = bf16, uint8 = e4m3, float32 = f32;
+    ab_dtype=E2M1 reads packed FP4 (element e of the storage at byte e // 2,
+    low nibble for even e; lda / ldb count elements).  Block scales: sfa[M][.],
+    sfb[N][.], one per `block` consecutive k, E8M0 (sf_format=SF_E8M0) or
+    unsigned E4M3 (SF_UE4M3) codes.
     """
 
     def __init__(self, M, N, K, A, lda, opA, B, ldb, opB, alpha=1.0, beta=0.0,
                  C=None, ldc=0, bias=None, act="none", scale_a=1.0, scale_b=1.0,
                  ab_dtype=None, c_dtype=None, bias_dtype=None, row_scale=None, col_scale=None,
-                 sfa=None, sfb=None, block=32):
+                 sfa=None, sfb=None, block=32, sf_format=SF_E8M0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.A, ab = _storage(A, ab_dtype)
         self.B, ab2 = _storage(B, ab_dtype)
@@ -131,6 +138,7 @@ class Problem:
         self.sfa = None if sfa is None else np.ascontiguousarray(sfa, dtype=np.uint8)
         self.sfb = None if sfb is None else np.ascontiguousarray(sfb, dtype=np.uint8)
         self.block = int(block)
+        self.sf_format = int(sf_format)
         if (self.sfa is None) != (self.sfb is None):
             raise ValueError("block scales come in pairs (sfa and sfb)")
         self.scale_a, self.scale_b = float(scale_a), float(scale_b)
@@ -146,10 +154,10 @@ class Problem:
         L = _load()
         L.oracle_set_channel_scales(_ptr(self.row_scale), _ptr(self.col_scale))
         if self.sfa is None:
-            L.oracle_set_block_scales(None, 0, None, 0, 32)
+            L.oracle_set_block_scales(None, 0, None, 0, 32, 0)
         else:
             L.oracle_set_block_scales(_ptr(self.sfa), self.sfa.shape[1], _ptr(self.sfb), self.sfb.shape[1],
-                                      self.block)
+                                      self.block, self.sf_format)
 
     def full(self, nthreads: int = 0) -> np.ndarray:
         out = np.empty((self.M, self.N), dtype=np.float64)
@@ -212,6 +220,20 @@ def decode_e8m0(bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint8)
     out = np.empty(bits.shape, dtype=np.float64)
     _load().oracle_decode_e8m0_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def decode_ue4m3(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode_ue4m3_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def decode_e2m1(nibbles: np.ndarray) -> np.ndarray:
+    nibbles = np.ascontiguousarray(nibbles, dtype=np.uint8)
+    out = np.empty(nibbles.shape, dtype=np.float64)
+    _load().oracle_decode_e2m1_array(_ptr(nibbles), _ptr(out), nibbles.size)
     return out
 
 

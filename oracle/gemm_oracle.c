@@ -31,8 +31,10 @@
  * for column j of B with sb(j, k / blk).  The operand values are then
  * sa(i, k/blk) * a(i,k) and sb(j, k/blk) * b(k,j), and the sum runs over those
  * products.  The scale factors are the 8-bit exponents of the OCP Microscaling
- * formats (E8M0: value 2^(e - 127), e = 255 is NaN), the reading taken where
- * the page names no format.
+ * formats (E8M0: value 2^(e - 127), e = 255 is NaN) with blk = 32, or the
+ * unsigned E4M3 scales of NVFP4 with blk = 16, the readings taken where the
+ * page names no format.  The four-bit elements are FP4 E2M1 (OCP MX), two per
+ * byte, the even element of each pair in the low nibble.
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - bias is indexed by the output column j and added before act;
@@ -56,7 +58,8 @@
 #include <unistd.h>
 
 enum { OR_ROW = 0, OR_COL = 1 };
-enum { OR_BF16 = 0, OR_E4M3 = 1, OR_F32 = 2, OR_F16 = 3, OR_E5M2 = 4 };
+enum { OR_BF16 = 0, OR_E4M3 = 1, OR_F32 = 2, OR_F16 = 3, OR_E5M2 = 4, OR_E2M1 = 5 };
+enum { OR_SF_E8M0 = 0, OR_SF_UE4M3 = 1 };
 enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_GELU = 2 };
 
 /* ------------------------------------------------------------------------ */
@@ -143,11 +146,32 @@ static double decode_f32(const void* p) {
     return (double)x;
 }
 
+/* FP4 E2M1 (OCP Microscaling formats): 1 sign, 2 exponent bits (bias 1),
+ * 1 fraction bit; normal (e > 0): (-1)^s 2^(e-1) (1 + f/2); subnormal
+ * (e = 0): (-1)^s (f/2).  No infinities or NaN; largest value 6. */
+double oracle_decode_e2m1(uint8_t nibble) {
+    int s = (nibble >> 3) & 1;
+    int e = (nibble >> 1) & 3;
+    int f = nibble & 1;
+    double v = (e == 0) ? 0.5 * (double)f : ldexp(1.0 + 0.5 * (double)f, e - 1);
+    return s ? -v : v;
+}
+
+/* Unsigned E4M3 scale of NVFP4: the E4M3 encoding without its sign bit
+ * (4 exponent bits, bias 7, 3 fraction bits); 0x7F is NaN, bit 7 ignored. */
+double oracle_decode_ue4m3(uint8_t bits) {
+    return oracle_decode_e4m3((uint8_t)(bits & 0x7F));
+}
+
 /* E8M0 scale factor of the OCP Microscaling formats: an unsigned 8-bit
  * exponent with bias 127 and no mantissa; 0xFF is NaN. */
 double oracle_decode_e8m0(uint8_t bits) {
     if (bits == 0xFF) return NAN;
     return ldexp(1.0, (int)bits - 127);
+}
+
+static double decode_scale(int fmt, uint8_t bits) {
+    return fmt == OR_SF_UE4M3 ? oracle_decode_ue4m3(bits) : oracle_decode_e8m0(bits);
 }
 
 static double g_bf16_table[65536];
@@ -199,6 +223,7 @@ typedef struct {
     const uint8_t* sfa; long long ld_sfa;
     const uint8_t* sfb; long long ld_sfb;
     int blk;
+    int sf_fmt;
     /* optional instrumented operation counter (tiny problems only) */
     int count_ops;
 } oracle_problem;
@@ -207,6 +232,10 @@ static double load_ab(const void* base, int dtype, long long idx) {
     switch (dtype) {
     case OR_E4M3: return g_e4m3_table[((const uint8_t*)base)[idx]];
     case OR_E5M2: return g_e5m2_table[((const uint8_t*)base)[idx]];
+    case OR_E2M1: {
+        uint8_t byte = ((const uint8_t*)base)[idx >> 1];
+        return oracle_decode_e2m1((uint8_t)((idx & 1) ? (byte >> 4) : (byte & 0xF)));
+    }
     case OR_F16: return g_f16_table[((const uint16_t*)base)[idx]];
     case OR_F32: return decode_f32((const float*)base + idx);
     default: return g_bf16_table[((const uint16_t*)base)[idx]];
@@ -234,8 +263,8 @@ static double element(const oracle_problem* p, int i, int j, long long* n_mul, l
         double a = load_ab(p->A, p->ab_dtype, a_index(p, i, k));
         double b = load_ab(p->B, p->ab_dtype, b_index(p, k, j));
         if (p->sfa) {
-            a = oracle_decode_e8m0(p->sfa[(long long)i * p->ld_sfa + k / p->blk]) * a;
-            b = oracle_decode_e8m0(p->sfb[(long long)j * p->ld_sfb + k / p->blk]) * b;
+            a = decode_scale(p->sf_fmt, p->sfa[(long long)i * p->ld_sfa + k / p->blk]) * a;
+            b = decode_scale(p->sf_fmt, p->sfb[(long long)j * p->ld_sfb + k / p->blk]) * b;
         }
         s = s + a * b;
         if (p->count_ops) { ++*n_mul; ++*n_add; }
@@ -347,11 +376,13 @@ static _Thread_local const uint8_t* g_sfa = NULL;
 static _Thread_local const uint8_t* g_sfb = NULL;
 static _Thread_local long long g_ld_sfa = 0, g_ld_sfb = 0;
 static _Thread_local int g_blk = 32;
+static _Thread_local int g_sf_fmt = OR_SF_E8M0;
 void oracle_set_block_scales(const uint8_t* sfa, long long ld_sfa, const uint8_t* sfb, long long ld_sfb,
-                             int blk) {
+                             int blk, int sf_fmt) {
     g_sfa = sfa; g_ld_sfa = ld_sfa;
     g_sfb = sfb; g_ld_sfb = ld_sfb;
     g_blk = blk > 0 ? blk : 32;
+    g_sf_fmt = sf_fmt;
 }
 
 static void attach_thread_state(oracle_problem* p) {
@@ -361,6 +392,7 @@ static void attach_thread_state(oracle_problem* p) {
         p->sfa = g_sfa; p->ld_sfa = g_ld_sfa;
         p->sfb = g_sfb; p->ld_sfb = g_ld_sfb;
         p->blk = g_blk;
+        p->sf_fmt = g_sf_fmt;
     }
 }
 
@@ -410,6 +442,12 @@ void oracle_decode_e5m2_array(const uint8_t* in, double* out, long long n) {
 }
 void oracle_decode_e8m0_array(const uint8_t* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e8m0(in[i]);
+}
+void oracle_decode_ue4m3_array(const uint8_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_ue4m3(in[i]);
+}
+void oracle_decode_e2m1_array(const uint8_t* in, double* out, long long n) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_decode_e2m1(in[i]);
 }
 void oracle_act_array(int act, const double* in, double* out, long long n) {
     for (long long i = 0; i < n; ++i) out[i] = oracle_act(act, in[i]);

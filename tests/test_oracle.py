@@ -454,3 +454,79 @@ def test_mx_quantiser_and_blocked_layout():
         for c in (0, 3, 4, 8):
             off = ((r // 128) * 3 + c // 4) * 512 + (r % 32) * 16 + (r % 128) // 32 * 4 + c % 4
             assert blk[off] == sf[r, c] % 251
+
+
+# ------------------------------------------------------------ FP4 operands
+
+def test_e2m1_decoder_against_e4m3_reencoding():
+    """Each E2M1 code re-encoded bit by bit as the E4M3 code of the same value
+    (exponent rebased from bias 1 to bias 7, fraction shifted into place) and
+    decoded by torch must equal the oracle's decode."""
+    codes = np.arange(16, dtype=np.uint8)
+    ours = oracle.decode_e2m1(codes)
+    for c in codes:
+        s, e, f = (c >> 3) & 1, (c >> 1) & 3, c & 1
+        if e == 0 and f == 0:
+            bits = s << 7
+        elif e == 0:   # subnormal 0.5 = 2^-1: E4M3 exponent field -1 + 7 = 6, fraction 0
+            bits = (s << 7) | (6 << 3)
+        else:
+            bits = (s << 7) | ((e - 1 + 7) << 3) | (f << 2)
+        ref = torch.tensor([bits], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item()
+        assert ours[c] == ref, (c, ours[c], ref)
+    assert sorted(set(np.abs(ours))) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_ue4m3_decoder_against_torch():
+    bits = np.arange(128, dtype=np.uint8)
+    ours = oracle.decode_ue4m3(bits)
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 1
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(oracle.decode_ue4m3(bits | 0x80)[~nan], ours[~nan])  # the sign bit is ignored
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 2), (3, 4, 34), (5, 2, 96), (2, 3, 130)])
+def test_fp4_block_scaled_tiny_exact_rational(fmt, M, N, K):
+    """Packed FP4 elements (even element in the low nibble) with per-block
+    scales against exact rational arithmetic, elements and scales decoded
+    independently of the oracle (nibble unpacking here, torch for the scales)."""
+    case = inputs.make_fp4_case("t", M, N, K, seed=M * 13 + N * 5 + K, fmt=fmt, dist="codes",
+                                code_range=list(range(16)),
+                                scale_codes=[0x30, 0x38, 0x40, 0x44] if fmt == "nvfp4" else [125, 127, 129])
+    got = oracle.Problem(M, N, K, case.A.numpy(), case.lda, oracle.ROW, case.B.numpy(), case.ldb, oracle.COL,
+                         ab_dtype=oracle.E2M1, sfa=case.sfa, sfb=case.sfb, block=case.sf_block,
+                         sf_format=oracle.SF_UE4M3 if fmt == "nvfp4" else oracle.SF_E8M0).full(1)
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+    def unpack(storage):
+        b = storage.numpy()
+        nib = np.stack([b & 0xF, b >> 4], axis=-1).reshape(b.shape[0], -1)[:, :K]
+        return [[Fraction(grid[n & 7]) * (-1 if n & 8 else 1) for n in row] for row in nib]
+
+    def scale(code):
+        if fmt == "nvfp4":
+            return Fraction(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn).double().item())
+        return Fraction(2) ** (int(code) - 127)
+
+    a, b = unpack(case.A), unpack(case.B)
+    blk = case.sf_block
+    for i in range(M):
+        for j in range(N):
+            ref = sum((scale(case.sfa[i, k // blk]) * a[i][k] * scale(case.sfb[j, k // blk]) * b[j][k]
+                       for k in range(K)), Fraction(0))
+            assert got[i, j] == float(ref), (i, j)
+
+
+def test_fp4_quantiser_keeps_values_within_one_step():
+    case = inputs.make_fp4_case("q", 4, 3, 64, seed=2, fmt="nvfp4")
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((4, 64))  # the same first draw the generator quantised for A
+    b = case.A.numpy()
+    nib = np.stack([b & 0xF, b >> 4], axis=-1).reshape(4, -1)[:, :64]
+    vals = oracle.decode_e2m1(nib) * np.repeat(oracle.decode_ue4m3(case.sfa), 16, axis=1)
+    scale = np.repeat(oracle.decode_ue4m3(case.sfa), 16, axis=1)
+    # the largest E2M1 step is 2 (between 4 and 6): half a step of the scaled grid, plus the scale's rounding
+    assert np.all(np.abs(vals - x) <= 1.0 * scale + 0.07 * np.abs(x))

@@ -58,6 +58,8 @@ def raw_bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
         return t.contiguous().view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.contiguous().numpy()
+    if t.dtype == torch.uint8:  # packed FP4 storage
+        return t.contiguous().numpy()
     raise TypeError(t.dtype)
 
 
@@ -89,6 +91,8 @@ class GemmCase:
     col_scale: Optional[torch.Tensor] = None   # fp32 [N] dequantisation scale per column
     sfa: Optional[np.ndarray] = None           # uint8 E8M0 [M][ceil(K/32)] block scales of A's rows
     sfb: Optional[np.ndarray] = None           # uint8 E8M0 [N][ceil(K/32)] block scales of B's columns
+    sf_block: int = 32                          # elements per block scale (32 MX, 16 NVFP4)
+    sf_format: str = "e8m0"                     # "e8m0" or "ue4m3" scale codes
     ldd: int = 0
     meta: dict = field(default_factory=dict)
 
@@ -140,7 +144,7 @@ def mx_quantize(x: torch.Tensor, fmt: str, scale_dist: Optional[tuple] = None, g
     return q, codes
 
 
-def mx_blocked_layout(sf: np.ndarray, rows_pad: int = 128, kb_pad: int = 4) -> np.ndarray:
+def mx_blocked_layout(sf: np.ndarray, rows_pad: int = 128, kb_pad: int = 4, pad_code: int = 127) -> np.ndarray:
     """The scale-factor layout the library reads (a permutation, no arithmetic):
     rows padded to a multiple of 128 and scale columns to a multiple of 4;
     for each block of 128 rows x 4 scale columns, 512 consecutive bytes, the
@@ -149,11 +153,101 @@ def mx_blocked_layout(sf: np.ndarray, rows_pad: int = 128, kb_pad: int = 4) -> n
     R, C = sf.shape
     Rp = (R + rows_pad - 1) // rows_pad * rows_pad
     Cp = (C + kb_pad - 1) // kb_pad * kb_pad
-    full = np.full((Rp, Cp), 127, dtype=np.uint8)
+    full = np.full((Rp, Cp), pad_code, dtype=np.uint8)
     full[:R, :C] = sf
     # [rb][r32_hi(4)][r32_lo(32)][cb][c4] -> [rb][cb][r32_lo][r32_hi][c4]
     t = full.reshape(Rp // 128, 4, 32, Cp // 4, 4).transpose(0, 3, 2, 1, 4)
     return np.ascontiguousarray(t).reshape(-1)
+
+
+# FP4 E2M1 (OCP Microscaling formats): the eight magnitudes of codes 0..7
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+UE4M3_ONE = 0x38  # 1.0 as an unsigned E4M3 scale
+
+
+def e2m1_codes(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 value (ties to the even code), saturating at 6."""
+    mag = np.minimum(np.abs(v), 6.0)
+    mids = (E2M1_GRID[1:] + E2M1_GRID[:-1]) / 2
+    code = np.searchsorted(mids, mag, side="left")          # mag <= mid -> lower code
+    tie = np.isin(mag, mids)
+    code = np.where(tie & (code % 2 == 1), code + 1, code)  # exact tie -> even code
+    code = np.where(tie & (code % 2 == 1), code - 1, code)
+    return (code | np.where(v < 0, 8, 0)).astype(np.uint8)
+
+
+def pack_fp4(codes: np.ndarray, ld: int) -> np.ndarray:
+    """Rows of 4-bit codes -> bytes, two per byte (even element in the low
+    nibble), rows ld elements long (ld even; padding nibbles 7 = 6.0)."""
+    rows, k = codes.shape
+    full = np.full((rows, ld), 7, dtype=np.uint8)
+    full[:, :k] = codes
+    return (full[:, 0::2] | (full[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _fp4_scales(blocks: np.ndarray, fmt: str, gen_codes):
+    """Per-block scale codes and values for FP4 quantisation of `blocks`
+    [..., nb, blk]: NVFP4 amax / 6 rounded to unsigned E4M3, MXFP4
+    2^(floor(log2 amax) - 2) as E8M0."""
+    amax = np.abs(blocks).max(axis=-1)
+    if gen_codes is not None:
+        return gen_codes(amax.shape)
+    if fmt == "nvfp4":
+        s = np.where(amax > 0, np.minimum(amax / 6.0, 448.0), 1.0).astype(np.float32)
+        codes = torch.from_numpy(s).to(torch.float8_e4m3fn).view(torch.uint8).numpy() & 0x7F
+        codes = np.where(codes == 0, UE4M3_ONE, codes).astype(np.uint8)
+        return codes
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2, 0).clip(-127, 127)
+    return (e + 127).astype(np.uint8)
+
+
+def make_fp4_case(name, M, N, K, *, seed, fmt="nvfp4", dist="normal", lda=None, ldb=None, d_dtype="bf16",
+                  alpha=1.0, beta=0.0, c_dist="uniform", bias_std=None, act="none", code_range=None,
+                  scale_codes=None) -> GemmCase:
+    """A block-scaled FP4 problem: A row-major, B column-major (both K-major),
+    E2M1 elements packed two per byte.  fmt "nvfp4": unsigned E4M3 scales per
+    16 elements; "mxfp4": E8M0 scales per 32.  dist "normal": N(0,1) quantised
+    per block; dist "codes": element codes uniform over code_range (a list of
+    E2M1 codes) and scale codes uniform over scale_codes (a list), for exact
+    tests.  Order of draws: A, B (elements then scales), C, bias."""
+    rng = np.random.default_rng(int(seed))
+    blk = 16 if fmt == "nvfp4" else 32
+    nb = (K + blk - 1) // blk
+    ld_a = lda if lda is not None else (K + 31) // 32 * 32
+    ld_b = ldb if ldb is not None else (K + 31) // 32 * 32
+
+    def operand(rows):
+        if dist == "codes":
+            codes = rng.choice(np.asarray(code_range, dtype=np.uint8), size=(rows, K))
+            sc = rng.choice(np.asarray(scale_codes, dtype=np.uint8), size=(rows, nb))
+            return codes, sc
+        x = rng.standard_normal((rows, nb * blk))
+        xb = x.reshape(rows, nb, blk)
+        sc = _fp4_scales(xb, fmt, None)
+        if fmt == "nvfp4":
+            sval = torch.from_numpy(sc.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        else:
+            sval = np.exp2(sc.astype(np.float64) - 127)
+        codes = e2m1_codes(xb / sval[..., None]).reshape(rows, nb * blk)[:, :K]
+        return codes, sc
+
+    ca, sfa = operand(M)
+    cb, sfb = operand(N)
+    A = torch.from_numpy(pack_fp4(ca, ld_a))
+    B = torch.from_numpy(pack_fp4(cb, ld_b))
+    gen = torch.Generator().manual_seed(int(seed) + 1)
+    C = None
+    ldc = 0
+    if beta != 0.0:
+        c = _draw(gen, (M, N), c_dist, K)
+        C, ldc = _store(c, "row", "bf16")
+    bias = None
+    if bias_std is not None:
+        bias = (torch.randn((N,), generator=gen, dtype=torch.float32) * bias_std).to(torch.bfloat16)
+    return GemmCase(name=name, M=M, N=N, K=K, opA="row", opB="col", ab_dtype=fmt, d_dtype=d_dtype, A=A, lda=ld_a,
+                    B=B, ldb=ld_b, alpha=alpha, beta=beta, C=C, ldc=ldc, bias=bias, act=act,
+                    ldd=padded_ld(N, d_dtype), sfa=sfa, sfb=sfb, sf_block=blk,
+                    sf_format="ue4m3" if fmt == "nvfp4" else "e8m0", meta={"seed": seed, "dist": dist})
 
 
 def make_case(name, M, N, K, *, seed, dist="uniform", opA="row", opB="col",
@@ -264,6 +358,13 @@ def mxfp8_8192_relu(fmt: str = "e4m3") -> GemmCase:
     bias N(0,0.1), ReLU, bf16 D."""
     return make_case(f"gemm8192_mx{fmt}_bias_relu", 8192, 8192, 8192, seed=18, dist="normal",
                      ab_dtype=fmt, bias_std=0.1, act="relu", block_scaled=True)
+
+
+def nvfp4_8192_relu() -> GemmCase:
+    """8192^3 NVFP4 (N(0,1) quantised to E2M1 in blocks of 16 with unsigned
+    E4M3 scales), bias N(0,0.1), ReLU, bf16 D."""
+    return make_fp4_case("gemm8192_nvfp4_bias_relu", 8192, 8192, 8192, seed=19, fmt="nvfp4", bias_std=0.1,
+                         act="relu")
 
 
 def fp8_8192_relu() -> GemmCase:
