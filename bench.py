@@ -70,13 +70,14 @@ WORKLOADS = {
     "skinny_8192x128x8192": (lambda inputs: inputs.ragged(2, 1), True),
     "gemm8192_e4m3_bias_relu": (lambda inputs: inputs.fp8_8192_relu(), True),
     "gemm8192_mxe4m3_bias_relu": (lambda inputs: inputs.mxfp8_8192_relu("e4m3"), True),
+    "gemm8192_nvfp4_bias_relu": (lambda inputs: inputs.nvfp4_8192_relu(), True),
 }
 
 def metric_name(workload):
     return METRIC if workload == DEFAULT_WORKLOAD else f"GEMM TFLOP/s ({workload}), 1 GPU"
 
 
-_EB = {"bf16": 2, "f16": 2, "e4m3": 1, "e5m2": 1, "f32": 4}
+_EB = {"bf16": 2, "f16": 2, "e4m3": 1, "e5m2": 1, "f32": 4, "nvfp4": 0.5, "mxfp4": 0.5}
 
 
 def case_bytes(case):
@@ -229,7 +230,8 @@ def max_over_ranks(pg, value, device):
 def oracle_problem(case):
     import oracle
     from tiled_tensor_core_persistent_gb300 import inputs
-    ab = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+    ab = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2,
+          "nvfp4": oracle.E2M1, "mxfp4": oracle.E2M1}
     vec = {"bf16": oracle.BF16, "f32": oracle.F32}
     return oracle.Problem(
         case.M, case.N, case.K, inputs.raw_bits(case.A), case.lda,
@@ -239,7 +241,8 @@ def oracle_problem(case):
         bias=inputs.raw_bits(case.bias), act=case.act, scale_a=case.scale_a, scale_b=case.scale_b,
         ab_dtype=ab[case.ab_dtype], c_dtype=vec[case.c_dtype] if case.C is not None else None,
         bias_dtype=vec[case.bias_dtype] if case.bias is not None else None,
-        sfa=case.sfa, sfb=case.sfb, block=inputs.MX_BLOCK)
+        sfa=case.sfa, sfb=case.sfb, block=case.sf_block,
+        sf_format=oracle.SF_UE4M3 if case.sf_format == "ue4m3" else oracle.SF_E8M0)
 
 
 def cpu_oracle_rows(case, rows, nthreads=0, prob=None):
@@ -370,8 +373,11 @@ def run_ours(args):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     in_bytes = _EB[case.ab_dtype]
     # dense tensor peak of the operand type: fp8 = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
-    tensor_peak = bf16_peak * (2.0 if in_bytes == 1 else 1.0)
-    nominal = 2250.0 * (2.0 if in_bytes == 1 else 1.0)
+    # dense tensor peak of the operand type from the measured bf16 peak and the
+    # nominal dense ratios of GB300: fp8 4.5 / 2.25 = 2, fp4 13.5 / 2.25 = 6
+    ratio = 6.0 if in_bytes == 0.5 else (2.0 if in_bytes == 1 else 1.0)
+    tensor_peak = bf16_peak * ratio
+    nominal = 2250.0 * ratio
     alg_bytes = case_bytes(case)
     intensity = analysis.boundary_intensity(case.M, case.N, case.K, in_bytes)
     hbm_bound = intensity * hbm * 1e-3 < tensor_peak
@@ -383,9 +389,9 @@ def run_ours(args):
             "frac": (gbs / hbm) if hbm_bound else (per_launch_tflops / tensor_peak),
             "traffic": recorded_traffic(args.workload),
             "peak_kind": (f"{peak_kind} copy bandwidth" if hbm_bound else
-                          f"{peak_kind} bf16 burst (cuBLAS 8192^3)" + (" x 2 for fp8" if in_bytes == 1 else "")),
+                          f"{peak_kind} bf16 burst (cuBLAS 8192^3)" + (f" x {ratio:g} for the operand type" if ratio != 1 else "")),
             "peak_sustained": None if hbm_bound else
-            peaks.get("bf16_tflops_sustained", 0) * (2.0 if in_bytes == 1 else 1.0) or None,
+            peaks.get("bf16_tflops_sustained", 0) * ratio or None,
             "tflops": per_launch_tflops, "gbs": gbs,
             "frac_of_nominal_tensor": per_launch_tflops / nominal,
             "algorithmic": "2*M*N*K flop per launch; bytes = A + B + D (+ C, bias) once",

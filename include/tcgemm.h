@@ -70,8 +70,13 @@ typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
  * narrow formats, where a small group of elements shares a scale factor). */
 typedef enum {
     TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2, TCG_F16 = 3, TCG_E5M2 = 4,
-    TCG_MXE4M3 = 5, TCG_MXE5M2 = 6
+    TCG_MXE4M3 = 5, TCG_MXE5M2 = 6, TCG_NVFP4 = 7, TCG_MXFP4 = 8
 } tcg_dtype;
+/* TCG_NVFP4 / TCG_MXFP4: the block-scaled four-bit formats (same page, Part
+ * V): FP4 E2M1 elements packed two per byte (the even element of each pair in
+ * the low nibble; lda / ldb count elements), with one unsigned E4M3 scale per
+ * 16 consecutive K (NVFP4) or one E8M0 scale per 32 (MXFP4), passed like the
+ * MX scales in tcg_scales.block_sfa / block_sfb. */
 
 typedef enum { TCG_ACT_NONE = 0, TCG_ACT_RELU = 1, TCG_ACT_GELU = 2 } tcg_act;
 
@@ -91,16 +96,16 @@ typedef struct {
  * device vector of M fp32 values; col_scale: NULL or a device vector of N
  * fp32 values (both 4-byte aligned).  Any operand type.
  *
- * block_sfa / block_sfb: the E8M0 block scales of MXE4M3 / MXE5M2 operands
+ * block_sfa / block_sfb: the block scales of the block-scaled operand types
  * (NULL otherwise; required for them when K > 0), device memory, 16-byte
  * aligned.  Scale (r, c) belongs to row r of A (column r of B) and to K
- * elements [32 c, 32 c + 32).  Layout: rows padded to a multiple of 128,
- * scale columns to a multiple of 4 (padding: any finite code); each block of
- * 128 rows x 4 columns is 512 consecutive bytes holding (r, c) at byte
- * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4); block (row block rb, column
- * block cb) starts at byte (rb * ceil(K / 128) + cb) * 512.  This is the
- * order in which the tensor cores read them, so the kernel copies each block
- * unchanged. */
+ * elements [g c, g c + g), g = 32 (MX types) or 16 (NVFP4).  Layout: rows
+ * padded to a multiple of 128, scale columns to a multiple of 4 (padding:
+ * any finite code); each block of 128 rows x 4 columns is 512 consecutive
+ * bytes holding (r, c) at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4);
+ * block (row block rb, column block cb) starts at byte
+ * (rb * ceil(ceil(K / g) / 4) + cb) * 512.  This is the order in which the
+ * tensor cores read them, so the kernel copies each block unchanged. */
 typedef struct {
     float scale_a;
     float scale_b;
@@ -117,8 +122,9 @@ typedef struct {
  *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3, TCG_E5M2, TCG_MXE4M3 or
  *                    TCG_MXE5M2 (A and B share it).  The 8-bit types
  *                    require opA = TCG_ROW and opB = TCG_COL (both
- *                    K-contiguous); the MX types also a 16-byte aligned A and
- *                    B with lda, ldb multiples of 16 (else TCG_ERR_UNSUPPORTED).
+ *                    K-contiguous); the block-scaled types also a 16-byte
+ *                    aligned A and B whose row pitch in bytes is a multiple of
+ *                    16 (else TCG_ERR_UNSUPPORTED), and for FP4 an even K.
  *   A, lda, opA    : operand A; lda >= K (ROW) or >= M (COL).
  *   B, ldb, opB    : operand B; ldb >= N (ROW) or >= K (COL).
  *   has_c, C, ldc, c_dtype : has_c != 0 when beta != 0; then C row-major,

@@ -8,9 +8,10 @@ from tiled_tensor_core_persistent_gb300 import inputs
 
 # Tolerances of the comparison |D - D_ref| <= tol * max(1, |D_ref|):
 # 1e-2 for bf16 operands, 5e-2 for e4m3 operands with per-tensor scales.
-TOL = {"bf16": 1e-2, "f16": 1e-2, "e4m3": 5e-2, "e5m2": 5e-2}
+TOL = {"bf16": 1e-2, "f16": 1e-2, "e4m3": 5e-2, "e5m2": 5e-2, "nvfp4": 5e-2, "mxfp4": 5e-2}
 
-_AB = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2}
+_AB = {"bf16": oracle.BF16, "f16": oracle.F16, "e4m3": oracle.E4M3, "e5m2": oracle.E5M2,
+       "nvfp4": oracle.E2M1, "mxfp4": oracle.E2M1}
 _VEC = {"bf16": oracle.BF16, "f32": oracle.F32}
 
 
@@ -25,7 +26,8 @@ def oracle_for(case: inputs.GemmCase) -> oracle.Problem:
         bias_dtype=_VEC[case.bias_dtype] if case.bias is not None else None,
         row_scale=None if case.row_scale is None else case.row_scale.numpy(),
         col_scale=None if case.col_scale is None else case.col_scale.numpy(),
-        sfa=case.sfa, sfb=case.sfb, block=inputs.MX_BLOCK)
+        sfa=case.sfa, sfb=case.sfb, block=case.sf_block,
+        sf_format=oracle.SF_UE4M3 if case.sf_format == "ue4m3" else oracle.SF_E8M0)
 
 
 def assert_within(got: np.ndarray, ref: np.ndarray, tol: float, what: str = "") -> float:

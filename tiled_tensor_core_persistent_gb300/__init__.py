@@ -21,11 +21,11 @@ import threading
 from . import _build
 
 ROW, COL = 0, 1
-BF16, E4M3, F32, F16, E5M2, MXE4M3, MXE5M2 = 0, 1, 2, 3, 4, 5, 6
+BF16, E4M3, F32, F16, E5M2, MXE4M3, MXE5M2, NVFP4, MXFP4 = 0, 1, 2, 3, 4, 5, 6, 7, 8
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 
 DTYPES = {"bf16": BF16, "e4m3": E4M3, "f32": F32, "f16": F16, "e5m2": E5M2, "mxe4m3": MXE4M3,
-          "mxe5m2": MXE5M2}
+          "mxe5m2": MXE5M2, "nvfp4": NVFP4, "mxfp4": MXFP4}
 LAYOUTS = {"row": ROW, "col": COL}
 ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
 

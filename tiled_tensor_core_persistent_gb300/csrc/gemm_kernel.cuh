@@ -92,12 +92,12 @@ struct KernelParams {
     uint32_t ab_fmt;            // operand format field of the instruction descriptor
     const float* row_scale;     // optional dequantisation scale per output row (M)
     const float* col_scale;     // optional dequantisation scale per output column (N)
-    // Block scale factors (OCP MX, E8M0 per 32 consecutive K), in 512-byte
-    // blocks of 128 rows x 4 scales: block (row block rb, K atom ka) at
-    // (rb * num_katoms + ka) * 512.  Used by the kMx kernel only.
+    // Block scale factors, in 512-byte blocks of 128 rows x 4 scales: block
+    // (row block rb, column block cb) at (rb * num_sfcb + cb) * 512.  Used by
+    // the block-scaled kernels only.
     const uint8_t* sfa;
     const uint8_t* sfb;
-    int num_katoms;             // 128-element K atoms per row (ceil(K / 128))
+    int num_sfcb;               // 4-scale column blocks per row (ceil(ceil(K / block) / 4))
 };
 
 
@@ -576,12 +576,15 @@ __device__ __forceinline__ void store_chunk_direct(const KernelParams& p, const 
 // kKAtoms = 128-byte K atoms per pipeline stage (1 or 2).  Two atoms put
 // twice the MMAs behind each stage handshake (wait, commit), which is what
 // keeps the tensor pipe busy with pair tiles.
-// kMx: block-scaled fp8 operands (1-CTA tiles, BN = 128).  Each stage also
-// carries the tile's scale blocks (512 bytes per 128 rows per K atom, for A
-// and for B), which the MMA thread copies to TMEM with tcgen05.cp before the
-// stage's block-scaled MMAs; TMEM columns [2 BN, ...) hold one 8-column slot
-// (4 for A, 4 for B) per stage and atom.
-template <int BN, bool kFp8, bool kCta2, int kKAtoms, bool kMx = false>
+// kBlk: block-scaled operands (1-CTA tiles, BN = 128): 1 = MXFP8 (E4M3/E5M2,
+// E8M0 per 32, kind::mxf8f6f4 1X), 2 = NVFP4 (E2M1, unsigned E4M3 per 16,
+// kind::mxf4nvf4 4X), 3 = MXFP4 (E2M1, E8M0 per 32, kind::mxf4nvf4 2X).
+// FP4 operands are handled as bytes (two elements each, K counted in bytes).
+// Each stage also carries the tile's scale blocks for its 128-byte K atoms
+// (512 bytes per 128 rows and 4 scales: 1, 4 or 2 blocks per atom per
+// operand), which the MMA thread copies to TMEM with tcgen05.cp before the
+// stage's MMAs; TMEM columns [2 BN, ...) hold 4 columns per block.
+template <int BN, bool kFp8, bool kCta2, int kKAtoms, int kBlk = 0>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
     constexpr int kBK = kRowBytes / kElemBytes;       // K elements per 128-byte atom
@@ -595,9 +598,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
-    static_assert(!kMx || (kFp8 && !kCta2 && BN == 128), "block-scaled tiles are 1-CTA fp8 128 x 128");
-    constexpr int kSfBlock = 512;                          // 128 rows x 4 E8M0 scales
-    constexpr int kSfBytes = kMx ? kKAtoms * 2 * kSfBlock : 0;
+    constexpr bool kMx = kBlk != 0;
+    static_assert(!kMx || (kFp8 && !kCta2 && BN == 128), "block-scaled tiles are 1-CTA 8-bit 128 x 128");
+    constexpr int kSfBlock = 512;                          // 128 rows x 4 scales
+    constexpr int kSfPerAtom = kBlk == 2 ? 4 : (kBlk == 3 ? 2 : 1);   // scale blocks per operand per atom
+    constexpr int kSfBytes = kMx ? kKAtoms * 2 * kSfPerAtom * kSfBlock : 0;
     constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static_assert(kStageBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
@@ -707,19 +712,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                 load(sB + h * kRowBytes * kStageK, &p.tmB, b_row + h * kAtom, k0);
                         }
                         if constexpr (kMx) {
-                            // scale blocks of this stage's atoms: A's row block, B's column block
+                            // scale blocks of this stage's atoms: per atom kSfPerAtom blocks
+                            // of A's row block, then kSfPerAtom of B's column block
                             uint8_t* sSf = sB + kBBytes;
 #pragma unroll
                             for (int at = 0; at < kKAtoms; ++at) {
-                                // atoms past K (a last stage of two atoms) reuse the last
-                                // scale block: their elements are zero-filled by the TMA
-                                const int ka = min(kb * kKAtoms + at, p.num_katoms - 1);
-                                ptx::bulk_load(sSf + (2 * at) * kSfBlock,
-                                               p.sfa + (static_cast<size_t>(m_blk) * p.num_katoms + ka) * kSfBlock,
-                                               kSfBlock, fb);
-                                ptx::bulk_load(sSf + (2 * at + 1) * kSfBlock,
-                                               p.sfb + (static_cast<size_t>(n_blk) * p.num_katoms + ka) * kSfBlock,
-                                               kSfBlock, fb);
+#pragma unroll
+                                for (int sb = 0; sb < kSfPerAtom; ++sb) {
+                                    // blocks past K (a last, partial atom) reuse the last one:
+                                    // their elements are zero-filled by the TMA
+                                    const int cb = min((kb * kKAtoms + at) * kSfPerAtom + sb, p.num_sfcb - 1);
+                                    ptx::bulk_load(sSf + ((2 * at) * kSfPerAtom + sb) * kSfBlock,
+                                                   p.sfa + (static_cast<size_t>(m_blk) * p.num_sfcb + cb) * kSfBlock,
+                                                   kSfBlock, fb);
+                                    ptx::bulk_load(sSf + ((2 * at + 1) * kSfPerAtom + sb) * kSfBlock,
+                                                   p.sfb + (static_cast<size_t>(n_blk) * p.num_sfcb + cb) * kSfBlock,
+                                                   kSfBlock, fb);
+                                }
                             }
                         }
                     }
@@ -748,9 +757,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         if (leader) {
             const bool issuer = lane == 0;
             // Instruction descriptor.  kind::f16 / kind::f8f6f4: D format F32 in
-            // bits 4-5.  Block-scaled kind::mxf8f6f4: bits 4-5 select B's scale
-            // byte, bits 29-30 A's (set per MMA below), bit 23 = E8M0 scales.
-            const uint32_t idesc = (kMx ? (1u << 23) : (1u << 4)) | (p.ab_fmt << 7) | (p.ab_fmt << 10) |
+            // bits 4-5.  Block-scaled kinds: bits 4-5 select B's scale byte, bits
+            // 29-30 A's (set per MMA below), bit 23 = E8M0 (1) or UE4M3 (0)
+            // scales; the operand format of kind::mxf4nvf4 is E2M1 = 1.
+            constexpr uint32_t kScaleType = (kBlk == 1 || kBlk == 3) ? (1u << 23) : 0u;
+            const uint32_t ab_fmt = (kBlk == 2 || kBlk == 3) ? 1u : p.ab_fmt;
+            const uint32_t idesc = (kMx ? kScaleType : (1u << 4)) | (ab_fmt << 7) | (ab_fmt << 10) |
                                    (static_cast<uint32_t>(p.a_mn_major) << 15) |
                                    (static_cast<uint32_t>(p.b_mn_major) << 16) |
                                    (static_cast<uint32_t>(BN >> 3) << 17) |
@@ -800,20 +812,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     const uint32_t sB = sA + kABytes;
                     const uint64_t a_desc = ptx::smem_desc_sw128(sA, a_lbo, 1024);
                     const uint64_t b_desc = ptx::smem_desc_sw128(sB, b_lbo, 1024);
-                    uint32_t sf_a = 0, sf_b = 0;
+                    uint32_t sf_base = 0;
                     if constexpr (kMx) {
-                        // this stage's scale blocks -> TMEM (slot per stage and atom)
+                        // this stage's scale blocks -> TMEM, 4 columns per block, in
+                        // the order they sit in shared memory (per atom: A's, then B's)
                         const uint32_t sSf = sB + static_cast<uint32_t>(kBBytes);
+                        sf_base = tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kKAtoms * 8 * kSfPerAtom);
 #pragma unroll
-                        for (int at = 0; at < kKAtoms; ++at) {
-                            const uint32_t col = static_cast<uint32_t>(kSfCol0 + (stage * kKAtoms + at) * 8);
-                            ptx::tmem_cp_32x128b_warpx4(tmem_base + col,
-                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + (2 * at) * kSfBlock));
-                            ptx::tmem_cp_32x128b_warpx4(tmem_base + col + 4,
-                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + (2 * at + 1) * kSfBlock));
-                        }
-                        sf_a = tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kKAtoms * 8);
-                        sf_b = sf_a + 4;
+                        for (int blk = 0; blk < 2 * kSfPerAtom * kKAtoms; ++blk)
+                            ptx::tmem_cp_32x128b_warpx4(sf_base + static_cast<uint32_t>(blk * 4),
+                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + blk * kSfBlock));
                     }
 #pragma unroll
                     for (int k = 0; k < kKAtoms * kKSteps; ++k) {
@@ -821,11 +829,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         const uint64_t bd = b_desc + static_cast<uint64_t>(b_off(k));
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
                         if constexpr (kMx) {
-                            // MMA k of atom k / kKSteps uses scale byte k % kKSteps of its slot
-                            const uint32_t sfid = static_cast<uint32_t>(k % kKSteps);
-                            const uint32_t slot = static_cast<uint32_t>((k / kKSteps) * 8);
-                            ptx::mma_mxf8(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), sf_a + slot, sf_b + slot,
-                                          accum);
+                            // MMA kk of atom `at`: its scale blocks and the byte the first
+                            // of its scales sits at inside each 32-bit TMEM word
+                            const int at = k / kKSteps, kk = k % kKSteps;
+                            const uint32_t a_blocks = sf_base + static_cast<uint32_t>(at * 8 * kSfPerAtom);
+                            const uint32_t b_blocks = a_blocks + static_cast<uint32_t>(4 * kSfPerAtom);
+                            if constexpr (kBlk == 1) {          // one scale per MMA: byte kk of block 0
+                                const uint32_t sfid = static_cast<uint32_t>(kk);
+                                ptx::mma_mxf8(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), a_blocks, b_blocks,
+                                              accum);
+                            } else if constexpr (kBlk == 2) {   // four scales per MMA: all of block kk
+                                const uint32_t off = static_cast<uint32_t>(kk * 4);
+                                ptx::mma_mxf4_4x(d_tmem, ad, bd, idesc, a_blocks + off, b_blocks + off, accum);
+                            } else {                            // two scales per MMA: half of block kk / 2
+                                const uint32_t off = static_cast<uint32_t>((kk / 2) * 4);
+                                const uint32_t sfid = static_cast<uint32_t>((kk & 1) * 2);
+                                ptx::mma_mxf4_2x(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), a_blocks + off,
+                                                 b_blocks + off, accum);
+                            }
                         } else if constexpr (kCta2) {
                             if constexpr (kFp8) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);
                             else ptx::mma_f16_pair(d_tmem, ad, bd, idesc, accum);

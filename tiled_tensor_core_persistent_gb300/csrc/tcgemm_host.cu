@@ -73,12 +73,20 @@ int elem_bytes(tcg_dtype t) {
         case TCG_E5M2: return 1;
         case TCG_MXE4M3: return 1;
         case TCG_MXE5M2: return 1;
+        case TCG_NVFP4: return 1;  // bytes of two packed elements: FP4 sizes are converted to bytes first
+        case TCG_MXFP4: return 1;
         case TCG_F32: return 4;
     }
     return 0;
 }
 
-bool is_mx(tcg_dtype t) { return t == TCG_MXE4M3 || t == TCG_MXE5M2; }
+bool is_fp4(tcg_dtype t) { return t == TCG_NVFP4 || t == TCG_MXFP4; }
+bool is_mx(tcg_dtype t) { return t == TCG_MXE4M3 || t == TCG_MXE5M2 || is_fp4(t); }  // block-scaled
+// K in the kernel's units: bytes for packed FP4, elements otherwise
+int k_units(tcg_dtype t, int K) { return is_fp4(t) ? (K + 1) / 2 : K; }
+// elements per block scale, and scale blocks (4 scales) per 128-byte K atom
+int sf_group(tcg_dtype t) { return t == TCG_NVFP4 ? 16 : 32; }
+int sf_blocks_per_atom(tcg_dtype t) { return t == TCG_NVFP4 ? 4 : (t == TCG_MXFP4 ? 2 : 1); }
 bool is_fp8(tcg_dtype t) { return t == TCG_E4M3 || t == TCG_E5M2 || is_mx(t); }
 bool is_ab_type(tcg_dtype t) { return t == TCG_BF16 || t == TCG_F16 || is_fp8(t); }
 
@@ -181,6 +189,8 @@ CUtensorMapDataType tma_dtype(tcg_dtype t) {
         case TCG_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         case TCG_MXE4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         case TCG_MXE5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        case TCG_NVFP4: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        case TCG_MXFP4: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
         default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -229,9 +239,9 @@ struct Plan {
     int workers = 0;    // CTAs or CTA pairs
 };
 
-int stage_bytes(int bn, bool cta2, int katoms, bool mx = false) {
-    // block-scaled stages also hold one 512-byte scale block for A and one for B per atom
-    return katoms * ((tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes + (mx ? 2 * 512 : 0));
+int stage_bytes(int bn, bool cta2, int katoms, int sf_blocks = 0) {
+    // block-scaled stages also hold sf_blocks 512-byte scale blocks for A and for B per atom
+    return katoms * ((tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes + 2 * sf_blocks * 512);
 }
 
 int fixed_smem_bytes() {
@@ -240,10 +250,12 @@ int fixed_smem_bytes() {
 
 int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 
-Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1) {
+Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1) {
     Plan pl;
+    const int K = k_units(ab, K_elems);
     const int bk = tcg::kRowBytes / elem_bytes(ab);
     const bool mx = is_mx(ab);   // block-scaled: 1-CTA 128 x 128 tiles only
+    const int sfb = mx ? sf_blocks_per_atom(ab) : 0;
     pl.bn = (N <= 128 || mx) ? 128 : 256;
     // K atoms per stage are decided with the tile shape below; the split-K
     // heuristic works on single-atom k-blocks.
@@ -277,6 +289,7 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_
     if (g_force_cta2 == 2 || mx) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
     pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
+    if (is_fp4(ab)) pl.katoms = 1;  // the FP4 kernels are built with one K atom per stage
     pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
@@ -288,11 +301,11 @@ Plan make_plan(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, int sk_
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
-    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms, mx);
+    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms, sfb);
     stages = std::max(2, std::min(stages, 8));
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
-    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms, mx);
+    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms, sfb);
     int slots = dev.num_sms;  // units that run at once
     if (cta2) {
         slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
@@ -339,7 +352,7 @@ size_t counter_bytes(const Plan& pl) {
     return (static_cast<size_t>(pl.num_m) * pl.num_n * pl.cluster * sizeof(int) + 255) / 256 * 256;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA, bool kMx = false>
+template <int BN, bool kFp8, bool kCta2, int KA, int kMx = 0>
 cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
@@ -393,7 +406,7 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     return n;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA, bool kMx = false>
+template <int BN, bool kFp8, bool kCta2, int KA, int kMx = 0>
 tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
     cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA, kMx>();
     if (e != cudaSuccess) return fail_launch("cudaFuncSetAttribute", e);
@@ -454,9 +467,14 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
     if (ldd < N) return TCG_ERR_INVALID_ARG;
     if (has_c && ldc < N) return TCG_ERR_INVALID_ARG;
     if (is_fp8(ab_dtype) && (opA != TCG_ROW || opB != TCG_COL)) return TCG_ERR_UNSUPPORTED;
-    if (is_mx(ab_dtype) && K > 0 && (!aligned16(A) || !aligned16(B) || (static_cast<long long>(lda) % 16) ||
-                                     (static_cast<long long>(ldb) % 16)))
-        return TCG_ERR_UNSUPPORTED;  // block-scaled operands take the fast path only
+    if (is_mx(ab_dtype) && K > 0) {
+        // block-scaled operands take the fast path only; FP4 rows are whole bytes
+        const int per_byte = is_fp4(ab_dtype) ? 2 : 1;
+        if (is_fp4(ab_dtype) && ((K % 2) || (lda % 2) || (ldb % 2))) return TCG_ERR_UNSUPPORTED;
+        if (!aligned16(A) || !aligned16(B) || ((static_cast<long long>(lda) / per_byte) % 16) ||
+            ((static_cast<long long>(ldb) / per_byte) % 16))
+            return TCG_ERR_UNSUPPORTED;
+    }
     // Every pointer aligned to its element size.  Operands and outputs whose
     // base or row pitch is not a multiple of 16 bytes are still implemented:
     // A and B through a packed copy in the workspace, C, D and bias through
@@ -489,6 +507,7 @@ size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const voi
     const size_t base = tcg_workspace_size(M, N, K, ab_dtype);
     if (base == 0 || M == 0 || N == 0 || K == 0) return base;
     if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return 0;
+    if (is_mx(ab_dtype)) return base;  // block-scaled operands are never packed
     const int eb = elem_bytes(ab_dtype);
     return base + pack_bytes(M, K, opA, A, lda, eb) + pack_bytes(K, N, opB, B, ldb, eb);
 }
@@ -538,8 +557,8 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     Plan pl = make_plan(M, N, K, ab_dtype, dev);
     const int eb = elem_bytes(ab_dtype);
     const size_t base_need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
-    const size_t pack_a = K > 0 ? pack_bytes(M, K, opA, A, lda, eb) : 0;
-    const size_t pack_b = K > 0 ? pack_bytes(K, N, opB, B, ldb, eb) : 0;
+    const size_t pack_a = (K > 0 && !is_mx(ab_dtype)) ? pack_bytes(M, K, opA, A, lda, eb) : 0;
+    const size_t pack_b = (K > 0 && !is_mx(ab_dtype)) ? pack_bytes(K, N, opB, B, ldb, eb) : 0;
     const size_t need = base_need + pack_a + pack_b;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) {
         if (pack_a + pack_b > 0) {
@@ -584,6 +603,13 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         if (e != cudaSuccess) return fail_launch("pack_rows_kernel", e);
     }
 
+    // Packed FP4 operands are streamed as bytes: K and the leading dimensions in bytes.
+    const int K_elems = K;
+    if (is_fp4(ab_dtype)) {
+        K /= 2;
+        lda /= 2;
+        ldb /= 2;
+    }
     tcg::KernelParams kp;
     memset(&kp, 0, sizeof kp);
     const int bk = tcg::kRowBytes / elem_bytes(ab_dtype);
@@ -623,7 +649,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.col_scale = scales.col_scale;
     kp.sfa = static_cast<const uint8_t*>(scales.block_sfa);
     kp.sfb = static_cast<const uint8_t*>(scales.block_sfb);
-    kp.num_katoms = (K + 127) / 128;
+    kp.num_sfcb = ((K_elems + sf_group(ab_dtype) - 1) / sf_group(ab_dtype) + 3) / 4;
     kp.beta = beta;
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
@@ -659,9 +685,11 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = is_fp8(ab_dtype);
+    if (ab_dtype == TCG_NVFP4) return launch_kernel<128, true, false, 1, 2>(kp, pl, stream);
+    if (ab_dtype == TCG_MXFP4) return launch_kernel<128, true, false, 1, 3>(kp, pl, stream);
     if (is_mx(ab_dtype)) {
-        return pl.katoms == 2 ? launch_kernel<128, true, false, 2, true>(kp, pl, stream)
-                              : launch_kernel<128, true, false, 1, true>(kp, pl, stream);
+        return pl.katoms == 2 ? launch_kernel<128, true, false, 2, 1>(kp, pl, stream)
+                              : launch_kernel<128, true, false, 1, 1>(kp, pl, stream);
     }
     if (pl.cluster == 2 && pl.katoms == 2)
         return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)

@@ -38,12 +38,14 @@ class DeviceCase:
         self.C = _upload(case.C, dev, off.get("C", 0)) if case.C is not None else None
         self.bias = _upload(case.bias, dev, off.get("bias", 0)) if case.bias is not None else None
         # block-scaled operands: the library reads the E8M0 scales in its blocked layout
-        self.ab_dtype = case.ab_dtype if case.sfa is None else "mx" + case.ab_dtype
+        fp4 = case.ab_dtype in ("nvfp4", "mxfp4")
+        self.ab_dtype = case.ab_dtype if (case.sfa is None or fp4) else "mx" + case.ab_dtype
         self.sfa = self.sfb = None
         if case.sfa is not None:
-            from .inputs import mx_blocked_layout
-            self.sfa = torch.from_numpy(mx_blocked_layout(case.sfa)).to(dev)
-            self.sfb = torch.from_numpy(mx_blocked_layout(case.sfb)).to(dev)
+            from .inputs import UE4M3_ONE, mx_blocked_layout
+            pad = UE4M3_ONE if case.sf_format == "ue4m3" else 127
+            self.sfa = torch.from_numpy(mx_blocked_layout(case.sfa, pad_code=pad)).to(dev)
+            self.sfb = torch.from_numpy(mx_blocked_layout(case.sfb, pad_code=pad)).to(dev)
         self.row_scale = case.row_scale.to(dev) if case.row_scale is not None else None
         self.col_scale = case.col_scale.to(dev) if case.col_scale is not None else None
         ddt = _TORCH_DTYPE[case.d_dtype]
