@@ -100,3 +100,20 @@ def test_config_nvfp4_8192_bias_relu():
     assert_within(got_rows, prob.select(rows, np.arange(case.N, dtype=np.int32)), TOL["nvfp4"], "rows")
     got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
     assert_within(got_cols, prob.select(np.arange(case.M, dtype=np.int32), cols), TOL["nvfp4"], "cols")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+@pytest.mark.parametrize("shape", [(512, 512, 1024), (520, 700, 334), (256, 256, 64)], ids=lambda s: "x".join(map(str, s)))
+def test_fp4_pair_tiles_exact(shape, fmt):
+    """256 x 256 tiles on CTA pairs with one accumulator; scale blocks by TMA."""
+    M, N, K = shape
+    tcg.debug_set(force_cta2=1)
+    try:
+        case = exact_case(M, N, K, fmt, seed=M + 3 * N + K)
+        plan = tcg.plan(M, N, K, fmt)
+        assert plan["cluster"] == 2 and plan["BN"] == 256
+        dc = run(case)
+        assert np.array_equal(dc.result().numpy(), oracle_for(case).full())
+        assert dc.untouched_outside()
+    finally:
+        tcg.debug_set()

@@ -126,3 +126,21 @@ def test_config_mxfp8_8192_bias_relu():
     assert_within(got_rows, prob.select(rows, np.arange(case.N, dtype=np.int32)), TOL["e4m3"], "rows")
     got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
     assert_within(got_cols, prob.select(np.arange(case.M, dtype=np.int32), cols), TOL["e4m3"], "cols")
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("shape", [(512, 512, 1024), (520, 700, 333), (256, 256, 32)], ids=lambda s: "x".join(map(str, s)))
+def test_mx_pair_tiles_exact(shape, fmt):
+    """256 x 256 tiles on CTA pairs (cta_group::2): each CTA copies its A rows'
+    scales and all 256 columns' B scales into its own TMEM."""
+    M, N, K = shape
+    tcg.debug_set(force_cta2=1)
+    try:
+        case = exact_case(M, N, K, fmt, seed=M + N + K)
+        plan = tcg.plan(M, N, K, "mx" + fmt)
+        assert plan["cluster"] == 2 and plan["BN"] == 256
+        dc = run(case)
+        assert np.array_equal(dc.result().numpy(), oracle_for(case).full())
+        assert dc.untouched_outside()
+    finally:
+        tcg.debug_set()

@@ -43,6 +43,10 @@ constexpr int kEpiThreads = 128;
 constexpr int kEpiChunk = 32;         // columns per tcgen05.ld / TMA store box
 constexpr int kEpiWarpBytes = 8192;   // per epilogue warp: 2 or 4 chunk buffers
 constexpr int kEpiBytes = 4 * kEpiWarpBytes;
+// Block-scaled pair tiles keep half of that (one or two buffers per warp), so
+// that three stages of two K atoms fit next to it.
+constexpr int kEpiWarpBytesSmall = 4096;
+__host__ __device__ constexpr int epi_warp_bytes(bool small) { return small ? kEpiWarpBytesSmall : kEpiWarpBytes; }
 constexpr int kStatusTimeout = 7;     // == TCG_ERR_TIMEOUT
 
 struct KernelParams {
@@ -50,6 +54,8 @@ struct KernelParams {
     CUtensorMap tmB;
     CUtensorMap tmD;
     CUtensorMap tmC;      // C as 32 x 32 boxes (when c_tma)
+    CUtensorMap tmSFA;    // block scales as rows of 128 x 32-bit words (one 512-byte block each), pair tiles
+    CUtensorMap tmSFB;
     int M, N, K;
     int num_m_blk, num_n_blk, num_kb;
     // Work, in two phases.  Data-parallel: units [0, units_a) over tiles
@@ -599,21 +605,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
     constexpr bool kMx = kBlk != 0;
-    static_assert(!kMx || (kFp8 && !kCta2 && BN == 128), "block-scaled tiles are 1-CTA 8-bit 128 x 128");
+    static_assert(!kMx || (kFp8 && (kCta2 ? BN == 256 : BN == 128)),
+                  "block-scaled tiles are 8-bit 128 x 128 (one CTA) or 256 x 256 (a pair)");
     constexpr int kSfBlock = 512;                          // 128 rows x 4 scales
     constexpr int kSfPerAtom = kBlk == 2 ? 4 : (kBlk == 3 ? 2 : 1);   // scale blocks per operand per atom
-    constexpr int kSfBytes = kMx ? kKAtoms * 2 * kSfPerAtom * kSfBlock : 0;
+    // scale blocks per atom: A's (this CTA's 128 rows) and B's (all BN columns: a pair's
+    // tensor cores each need the scales of every column)
+    constexpr int kSfA = kSfPerAtom, kSfB = kSfPerAtom * (BN / 128);
+    constexpr int kSfBytes = kMx ? (kKAtoms * (kSfA + kSfB) * kSfBlock + 1023) / 1024 * 1024 : 0;  // 1 KiB padded
+    // A pair tile's 256 accumulator columns leave no room for scales next to a
+    // second accumulator: block-scaled pair tiles use one accumulator.
+    constexpr int kAccBufs = (kMx && kCta2) ? 1 : 2;
     constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static_assert(kStageBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
-    constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * kStageBytes;
+    // bytes the stage's copies deliver (the scale area's padding is not loaded)
+    constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * (kABytes + kBBytes + (kMx ? kKAtoms * (kSfA + kSfB) * kSfBlock : 0));
     constexpr uint32_t kTmemCols = kMx ? 512 : 2 * BN;
-    constexpr int kSfCol0 = 2 * BN;                        // first scale-factor column in TMEM
+    constexpr int kSfCol0 = kAccBufs * BN;                 // first scale-factor column in TMEM
+    static_assert(!kMx || kSfCol0 + 8 * (kSfA + kSfB) * kKAtoms <= 512, "scale columns fit in TMEM for 2 stages");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
     uint8_t* epi_smem = smem + S * kStageBytes;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_smem + kEpiBytes);
+    constexpr int kRingWarp = epi_warp_bytes(kMx && kCta2);   // epilogue buffers per warp
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_smem + 4 * kRingWarp);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -711,7 +727,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int h = 0; h < kBRows / kAtom; ++h)
                                 load(sB + h * kRowBytes * kStageK, &p.tmB, b_row + h * kAtom, k0);
                         }
-                        if constexpr (kMx) {
+                        if constexpr (kMx && kCta2) {
+                            // scale blocks of this stage's atoms, per atom: kSfA blocks of
+                            // this CTA's 128-row block of A, then kSfPerAtom blocks of each
+                            // of B's two 128-column blocks (both CTAs load all of B's)
+                            uint8_t* sSf = sB + kBBytes;
+                            const int rb_a = m_blk * 2 + static_cast<int>(rank);
+#pragma unroll
+                            for (int at = 0; at < kKAtoms; ++at) {
+                                const int cb = (kb * kKAtoms + at) * kSfPerAtom;
+                                uint8_t* dst = sSf + at * (kSfA + kSfB) * kSfBlock;
+                                load(dst, &p.tmSFA, 0, rb_a * p.num_sfcb + cb);
+#pragma unroll
+                                for (int h = 0; h < BN / 128; ++h)
+                                    load(dst + (kSfA + h * kSfPerAtom) * kSfBlock, &p.tmSFB, 0,
+                                         (n_blk * (BN / 128) + h) * p.num_sfcb + cb);
+                            }
+                        } else if constexpr (kMx) {
                             // scale blocks of this stage's atoms: per atom kSfPerAtom blocks
                             // of A's row block, then kSfPerAtom of B's column block
                             uint8_t* sSf = sB + kBBytes;
@@ -795,8 +827,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             Unit w;
             for (; ok && work_next(p, wi, w); ++t) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
-                const int acc = t & 1;
-                const uint32_t acc_phase = (t >> 1) & 1;
+                const int acc = kAccBufs == 2 ? (t & 1) : 0;
+                const uint32_t acc_phase = kAccBufs == 2 ? ((t >> 1) & 1) : (t & 1);
                 const long long ta = p.stats ? clock64() : 0;
                 if (!warp_wait(&ctl->tmem_empty[acc], acc_phase ^ 1u, p, ctl, 2, limit)) { ok = false; break; }
                 if (p.stats) st_acc += clock64() - ta;
@@ -817,11 +849,25 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         // this stage's scale blocks -> TMEM, 4 columns per block, in
                         // the order they sit in shared memory (per atom: A's, then B's)
                         const uint32_t sSf = sB + static_cast<uint32_t>(kBBytes);
-                        sf_base = tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kKAtoms * 8 * kSfPerAtom);
+                        sf_base = tmem_base + static_cast<uint32_t>(kSfCol0 + stage * kKAtoms * 4 * (kSfA + kSfB));
+                        // TMEM order per atom: A's blocks, then B's with the column blocks of
+                        // one scale index side by side (the MMA reads column n at n / 32)
+                        auto cp = [&](int smem_block, int col) {
+                            const uint64_t sd = ptx::smem_desc_noswizzle_16b_rows(sSf + smem_block * kSfBlock);
+                            if constexpr (kCta2) ptx::tmem_cp_32x128b_warpx4_pair(sf_base + static_cast<uint32_t>(col), sd);
+                            else ptx::tmem_cp_32x128b_warpx4(sf_base + static_cast<uint32_t>(col), sd);
+                        };
 #pragma unroll
-                        for (int blk = 0; blk < 2 * kSfPerAtom * kKAtoms; ++blk)
-                            ptx::tmem_cp_32x128b_warpx4(sf_base + static_cast<uint32_t>(blk * 4),
-                                                        ptx::smem_desc_noswizzle_16b_rows(sSf + blk * kSfBlock));
+                        for (int at = 0; at < kKAtoms; ++at) {
+                            const int blk0 = at * (kSfA + kSfB), col0 = 4 * blk0;
+#pragma unroll
+                            for (int sb = 0; sb < kSfA; ++sb) cp(blk0 + sb, col0 + 4 * sb);
+#pragma unroll
+                            for (int h = 0; h < BN / 128; ++h)
+#pragma unroll
+                                for (int sb = 0; sb < kSfPerAtom; ++sb)
+                                    cp(blk0 + kSfA + h * kSfPerAtom + sb, col0 + 4 * kSfA + 4 * (sb * (BN / 128) + h));
+                        }
                     }
 #pragma unroll
                     for (int k = 0; k < kKAtoms * kKSteps; ++k) {
@@ -831,21 +877,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         if constexpr (kMx) {
                             // MMA kk of atom `at`: its scale blocks and the byte the first
                             // of its scales sits at inside each 32-bit TMEM word
+                            // (B's scales: for BN = 256 two 128-column blocks, 4 columns apart
+                            // per scale-block index, as the MMA reads column n at n / 32)
                             const int at = k / kKSteps, kk = k % kKSteps;
-                            const uint32_t a_blocks = sf_base + static_cast<uint32_t>(at * 8 * kSfPerAtom);
-                            const uint32_t b_blocks = a_blocks + static_cast<uint32_t>(4 * kSfPerAtom);
+                            const uint32_t a_blocks = sf_base + static_cast<uint32_t>(at * 4 * (kSfA + kSfB));
+                            const uint32_t b_blocks = a_blocks + static_cast<uint32_t>(4 * kSfA);
+                            uint32_t sfid = 0, a_sf = a_blocks, b_sf = b_blocks;
                             if constexpr (kBlk == 1) {          // one scale per MMA: byte kk of block 0
-                                const uint32_t sfid = static_cast<uint32_t>(kk);
-                                ptx::mma_mxf8(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), a_blocks, b_blocks,
-                                              accum);
+                                sfid = static_cast<uint32_t>(kk);
                             } else if constexpr (kBlk == 2) {   // four scales per MMA: all of block kk
-                                const uint32_t off = static_cast<uint32_t>(kk * 4);
-                                ptx::mma_mxf4_4x(d_tmem, ad, bd, idesc, a_blocks + off, b_blocks + off, accum);
+                                a_sf += static_cast<uint32_t>(kk * 4);
+                                b_sf += static_cast<uint32_t>(kk * 4 * (BN / 128));
                             } else {                            // two scales per MMA: half of block kk / 2
-                                const uint32_t off = static_cast<uint32_t>((kk / 2) * 4);
-                                const uint32_t sfid = static_cast<uint32_t>((kk & 1) * 2);
-                                ptx::mma_mxf4_2x(d_tmem, ad, bd, idesc | (sfid << 4) | (sfid << 29), a_blocks + off,
-                                                 b_blocks + off, accum);
+                                a_sf += static_cast<uint32_t>((kk / 2) * 4);
+                                b_sf += static_cast<uint32_t>((kk / 2) * 4 * (BN / 128));
+                                sfid = static_cast<uint32_t>((kk & 1) * 2);
+                            }
+                            const uint32_t id = idesc | (sfid << 4) | (sfid << 29);
+                            if constexpr (kCta2) {
+                                if constexpr (kBlk == 1) ptx::mma_mxf8_pair(d_tmem, ad, bd, id, a_sf, b_sf, accum);
+                                else if constexpr (kBlk == 2) ptx::mma_mxf4_4x_pair(d_tmem, ad, bd, id, a_sf, b_sf, accum);
+                                else ptx::mma_mxf4_2x_pair(d_tmem, ad, bd, id, a_sf, b_sf, accum);
+                            } else {
+                                if constexpr (kBlk == 1) ptx::mma_mxf8(d_tmem, ad, bd, id, a_sf, b_sf, accum);
+                                else if constexpr (kBlk == 2) ptx::mma_mxf4_4x(d_tmem, ad, bd, id, a_sf, b_sf, accum);
+                                else ptx::mma_mxf4_2x(d_tmem, ad, bd, id, a_sf, b_sf, accum);
                             }
                         } else if constexpr (kCta2) {
                             if constexpr (kFp8) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);
@@ -901,9 +957,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         // 32 x 32 box lands there by TMA (when C is read), the thread reads
         // its row, then writes its D row into the same buffer for the TMA
         // store.  C boxes are requested L = nbuf / 2 chunks ahead.
-        uint8_t* const ring = epi_smem + (warp - kEpiWarp0) * kEpiWarpBytes;
+        uint8_t* const ring = epi_smem + (warp - kEpiWarp0) * kRingWarp;
         const int nbuf = p.epi_nbuf;
-        const int buf_bytes = kEpiWarpBytes / nbuf;
+        const int buf_bytes = kRingWarp / nbuf;
         const int lookahead = nbuf / 2;
         const uint32_t c_box_bytes = p.c_f32 ? 4096u : 2048u;
         uint64_t* const cbar = ctl->cbar[warp - kEpiWarp0];
@@ -943,8 +999,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const bool split_mode = w.nsplit > 1;
             constexpr int kRanks = kCta2 ? 2 : 1;
             const int counter = w.tile * kRanks + static_cast<int>(rank);
-            const int acc = t & 1;
-            const uint32_t acc_phase = (t >> 1) & 1;
+            const int acc = kAccBufs == 2 ? (t & 1) : 0;
+            const uint32_t acc_phase = kAccBufs == 2 ? ((t >> 1) & 1) : (t & 1);
             const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
             const int n0 = n_blk * BN;
             const int grow = m0 + row_in_tile;

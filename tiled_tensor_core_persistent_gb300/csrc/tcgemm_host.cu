@@ -240,12 +240,12 @@ struct Plan {
 };
 
 int stage_bytes(int bn, bool cta2, int katoms, int sf_blocks = 0) {
-    // block-scaled stages also hold sf_blocks 512-byte scale blocks for A and for B per atom
-    return katoms * ((tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes + 2 * sf_blocks * 512);
+    // block-scaled stages also hold sf_blocks 512-byte scale blocks (A's and B's) per atom
+    return katoms * (tcg::kBM + (cta2 ? bn / 2 : bn)) * tcg::kRowBytes + (katoms * sf_blocks * 512 + 1023) / 1024 * 1024;
 }
 
-int fixed_smem_bytes() {
-    return 1024 /*alignment slack*/ + tcg::kEpiBytes + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
+int fixed_smem_bytes(bool small_ring = false) {
+    return 1024 /*alignment slack*/ + 4 * tcg::epi_warp_bytes(small_ring) + static_cast<int>(sizeof(tcg::SmemCtl)) + 64;
 }
 
 int max_active_pairs(int bn, bool fp8, int katoms, int smem);
@@ -254,9 +254,16 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     Plan pl;
     const int K = k_units(ab, K_elems);
     const int bk = tcg::kRowBytes / elem_bytes(ab);
-    const bool mx = is_mx(ab);   // block-scaled: 1-CTA 128 x 128 tiles only
-    const int sfb = mx ? sf_blocks_per_atom(ab) : 0;
-    pl.bn = (N <= 128 || mx) ? 128 : 256;
+    const bool mx = is_mx(ab);   // block-scaled: 128 x 128 (one CTA) or 256 x 256 (a pair) tiles
+    pl.bn = (N <= 128) ? 128 : 256;
+    if (mx) {
+        // pairs when there is a full wave of 256 x 256 tiles, else one CTA per 128 x 128
+        const int pairs = ((M + 255) / 256) * ((N + 255) / 256);
+        bool pair = M > tcg::kBM && N > 128 && pairs * 2 >= dev.num_sms && g_force_splits == 0;
+        if (g_force_cta2 == 1) pair = N > 128;
+        if (g_force_cta2 == 2) pair = false;
+        pl.bn = pair ? 256 : 128;
+    }
     // K atoms per stage are decided with the tile shape below; the split-K
     // heuristic works on single-atom k-blocks.
     pl.num_kb = (K + bk - 1) / bk;
@@ -286,10 +293,16 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     const int num_m2 = (M + 2 * tcg::kBM - 1) / (2 * tcg::kBM);
     bool cta2 = splits == 1 && pl.bn == 256 && M > tcg::kBM && num_m2 * num_n * 2 >= dev.num_sms;
     if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
-    if (g_force_cta2 == 2 || mx) cta2 = false;
+    if (g_force_cta2 == 2 || (mx && pl.bn != 256)) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
     pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
-    if (is_fp4(ab)) pl.katoms = 1;  // the FP4 kernels are built with one K atom per stage
+    // block-scaled: two K atoms per stage on pair tiles, else one.  Measured on
+    // 8192^3: MXFP8 pairs 1841 -> 2199 TFLOP/s (6 x 1 atom -> 3 x 2), NVFP4
+    // pairs 2217 -> 2515 (5 x 1 -> 2 x 2)
+    if (mx) pl.katoms = g_env_katoms > 0 ? std::min(g_env_katoms, 2) : (cta2 ? 2 : 1);
+    if (mx && is_fp4(ab) && !cta2) pl.katoms = 1;
+    // scale blocks per stage atom: A's rows, then B's columns (a pair holds all 256)
+    const int sfb = mx ? sf_blocks_per_atom(ab) * (1 + pl.bn / 128) : 0;
     pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
@@ -301,11 +314,18 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
-    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms, sfb);
+    const bool small_ring = mx && cta2;   // block-scaled pair tiles: half-size epilogue ring
+    int stages = (dev.max_smem_optin - fixed_smem_bytes(small_ring)) / stage_bytes(pl.bn, cta2, pl.katoms, sfb);
     stages = std::max(2, std::min(stages, 8));
+    if (mx) {
+        // TMEM: accumulators (2 x 128 columns, or one 256-column pair accumulator) plus
+        // 4 columns per scale block per stage atom
+        const int sf_cols = 512 - 256;
+        stages = std::max(2, std::min(stages, sf_cols / (4 * sfb * pl.katoms)));
+    }
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
     pl.stages = stages;
-    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms, sfb);
+    pl.smem = fixed_smem_bytes(small_ring) + stages * stage_bytes(pl.bn, cta2, pl.katoms, sfb);
     int slots = dev.num_sms;  // units that run at once
     if (cta2) {
         slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
@@ -650,6 +670,19 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.sfa = static_cast<const uint8_t*>(scales.block_sfa);
     kp.sfb = static_cast<const uint8_t*>(scales.block_sfb);
     kp.num_sfcb = ((K_elems + sf_group(ab_dtype) - 1) / sf_group(ab_dtype) + 3) / 4;
+    if (is_mx(ab_dtype) && pl.cluster == 2 && K > 0) {
+        // pair tiles load their scale blocks with the TMA: rows of 128 x 32-bit words
+        // (one 512-byte block per row), boxes of the blocks of one K atom
+        const uint32_t per_atom = static_cast<uint32_t>(sf_blocks_per_atom(ab_dtype));
+        st = encode_2d(&kp.tmSFA, TCG_F32, scales.block_sfa, 128,
+                       static_cast<uint64_t>((M + 127) / 128) * kp.num_sfcb, 128, 128, per_atom,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != TCG_OK) return st;
+        st = encode_2d(&kp.tmSFB, TCG_F32, scales.block_sfb, 128,
+                       static_cast<uint64_t>((N + 127) / 128) * kp.num_sfcb, 128, 128, per_atom,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != TCG_OK) return st;
+    }
     kp.beta = beta;
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
@@ -664,7 +697,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     {
         // chunk buffers per epilogue warp: 8 KiB over the larger of the C and D boxes
         const int box = 32 * 32 * std::max(elem_bytes(d_dtype), kp.c_tma ? elem_bytes(c_dtype) : 0);
-        kp.epi_nbuf = tcg::kEpiWarpBytes / box;
+        kp.epi_nbuf = tcg::epi_warp_bytes(is_mx(ab_dtype) && pl.cluster == 2) / box;
     }
     kp.bias_vec = epi.bias && aligned16(epi.bias);
     kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
@@ -685,6 +718,16 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = is_fp8(ab_dtype);
+    if (is_mx(ab_dtype) && pl.cluster == 2) {
+        if (ab_dtype == TCG_NVFP4)
+            return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 2>(kp, pl, stream)
+                                  : launch_kernel<256, true, true, 1, 2>(kp, pl, stream);
+        if (ab_dtype == TCG_MXFP4)
+            return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 3>(kp, pl, stream)
+                                  : launch_kernel<256, true, true, 1, 3>(kp, pl, stream);
+        return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 1>(kp, pl, stream)
+                              : launch_kernel<256, true, true, 1, 1>(kp, pl, stream);
+    }
     if (ab_dtype == TCG_NVFP4) return launch_kernel<128, true, false, 1, 2>(kp, pl, stream);
     if (ab_dtype == TCG_MXFP4) return launch_kernel<128, true, false, 1, 3>(kp, pl, stream);
     if (is_mx(ab_dtype)) {
