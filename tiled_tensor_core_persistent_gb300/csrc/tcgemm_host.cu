@@ -197,8 +197,35 @@ CUtensorMapDataType tma_dtype(tcg_dtype t) {
 
 // A 2-D row-major view: `inner` contiguous elements per row, `outer` rows
 // ld_elems apart; boxes of box_inner x box_outer elements.
+// The descriptor is a pure function of its arguments, so encoded maps are
+// kept in a small process-wide cache (a call with the same pointers and
+// shapes as an earlier one skips the encode).  Bounded: cleared when full.
+struct MapKey {
+    int dtype;
+    const void* base;
+    uint64_t inner, outer, ld_elems;
+    uint32_t box_inner, box_outer;
+    int sw;
+    bool operator<(const MapKey& o) const {
+        return std::tie(dtype, base, inner, outer, ld_elems, box_inner, box_outer, sw) <
+               std::tie(o.dtype, o.base, o.inner, o.outer, o.ld_elems, o.box_inner, o.box_outer, o.sw);
+    }
+};
+std::mutex g_map_mu;
+std::map<MapKey, CUtensorMap> g_map_cache;
+constexpr size_t kMapCacheMax = 1024;
+
 tcg_status encode_2d(CUtensorMap* map, tcg_dtype t, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    const MapKey key{static_cast<int>(t), base, inner, outer, ld_elems, box_inner, box_outer, static_cast<int>(sw)};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_map_cache.find(key);
+        if (it != g_map_cache.end()) {
+            *map = it->second;
+            return TCG_OK;
+        }
+    }
     EncodeTiledFn fn;
     tcg_status st = get_encoder(fn);
     if (st != TCG_OK) return st;
@@ -218,6 +245,9 @@ tcg_status encode_2d(CUtensorMap* map, tcg_dtype t, const void* base, uint64_t i
         g_last_error = buf;
         return TCG_ERR_LAUNCH;
     }
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+    g_map_cache.emplace(key, *map);
     return TCG_OK;
 }
 
