@@ -129,16 +129,20 @@ def test_config_mxfp8_8192_bias_relu():
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("shape", [(512, 512, 1024), (520, 700, 333), (256, 256, 32)], ids=lambda s: "x".join(map(str, s)))
-def test_mx_pair_tiles_exact(shape, fmt):
-    """256 x 256 tiles on CTA pairs (cta_group::2): each CTA copies its A rows'
-    scales and all 256 columns' B scales into its own TMEM."""
+@pytest.mark.parametrize("width", [192, 256])
+@pytest.mark.parametrize("shape", [(512, 512, 1024), (520, 700, 333), (256, 256, 32), (300, 1000, 96)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_mx_pair_tiles_exact(shape, width, fmt):
+    """256 x 192 and 256 x 256 tiles on CTA pairs (cta_group::2): each CTA copies
+    its A rows' scales and the B scale blocks its tile's columns overlap into its
+    own TMEM.  A 192-wide tile that starts half-way into a 128-column scale
+    block (odd tile columns) reads its B scales from the block's third column."""
     M, N, K = shape
-    tcg.debug_set(force_cta2=1)
+    tcg.debug_set(force_cta2=4 if width == 192 else 3)
     try:
         case = exact_case(M, N, K, fmt, seed=M + N + K)
         plan = tcg.plan(M, N, K, "mx" + fmt)
-        assert plan["cluster"] == 2 and plan["BN"] == 256
+        assert plan["cluster"] == 2 and plan["BN"] == width
         dc = run(case)
         assert np.array_equal(dc.result().numpy(), oracle_for(case).full())
         assert dc.untouched_outside()

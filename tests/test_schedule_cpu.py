@@ -103,3 +103,13 @@ def test_partial_wave_stream_k_evens_out_the_last_wave():
 def test_fp8_schedule():
     check(8192, 8192, 8192, "e4m3", 152, 1)
     check(4095, 3001, 1537, "e4m3", 152, 3)
+
+
+@pytest.mark.parametrize("ab, width", [("mxe4m3", 256), ("mxfp4", 192), ("nvfp4", 256)])
+def test_block_scaled_pair_tile_grid(ab, width):
+    # block-scaled pairs: 256 x 192 tiles (MXFP4) or 256 x 256 (MXFP8, NVFP4)
+    M = N = K = 8192
+    rows, per_worker, total = check(M, N, K, ab, 152, 0)
+    assert max(r[2] for r in rows) + 1 == M // 256
+    assert max(r[3] for r in rows) + 1 == -(-N // width)
+    assert tcg.debug_schedule(M, N, K, ab, num_sms=152, sk_mode=0)[0][7] == 1   # K is not split

@@ -582,14 +582,15 @@ __device__ __forceinline__ void store_chunk_direct(const KernelParams& p, const 
 // kKAtoms = 128-byte K atoms per pipeline stage (1 or 2).  Two atoms put
 // twice the MMAs behind each stage handshake (wait, commit), which is what
 // keeps the tensor pipe busy with pair tiles.
-// kBlk: block-scaled operands (1-CTA tiles, BN = 128): 1 = MXFP8 (E4M3/E5M2,
-// E8M0 per 32, kind::mxf8f6f4 1X), 2 = NVFP4 (E2M1, unsigned E4M3 per 16,
-// kind::mxf4nvf4 4X), 3 = MXFP4 (E2M1, E8M0 per 32, kind::mxf4nvf4 2X).
+// kBlk: block-scaled operands (1-CTA tiles with BN = 128, pairs with BN = 192
+// or 256): 1 = MXFP8 (E4M3/E5M2, E8M0 per 32, kind::mxf8f6f4 1X), 2 = NVFP4
+// (E2M1, unsigned E4M3 per 16, kind::mxf4nvf4 4X), 3 = MXFP4 (E2M1, E8M0 per
+// 32, kind::mxf4nvf4 2X).
 // FP4 operands are handled as bytes (two elements each, K counted in bytes).
 // Each stage also carries the tile's scale blocks for its 128-byte K atoms
 // (512 bytes per 128 rows and 4 scales: 1, 4 or 2 blocks per atom per
 // operand), which the MMA thread copies to TMEM with tcgen05.cp before the
-// stage's MMAs; TMEM columns [2 BN, ...) hold 4 columns per block.
+// stage's MMAs; the TMEM columns after the accumulators hold 4 columns per block.
 template <int BN, bool kFp8, bool kCta2, int kKAtoms, int kBlk = 0>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
@@ -605,17 +606,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
     constexpr bool kMx = kBlk != 0;
-    static_assert(!kMx || (kFp8 && (kCta2 ? BN == 256 : BN == 128)),
-                  "block-scaled tiles are 8-bit 128 x 128 (one CTA) or 256 x 256 (a pair)");
+    static_assert(!kMx || (kFp8 && (kCta2 ? (BN == 256 || BN == 192) : BN == 128)),
+                  "block-scaled tiles are 8-bit 128 x 128 (one CTA) or 256 x 256 / 256 x 192 (a pair)");
     constexpr int kSfBlock = 512;                          // 128 rows x 4 scales
     constexpr int kSfPerAtom = kBlk == 2 ? 4 : (kBlk == 3 ? 2 : 1);   // scale blocks per operand per atom
     // scale blocks per atom: A's (this CTA's 128 rows) and B's (all BN columns: a pair's
-    // tensor cores each need the scales of every column)
-    constexpr int kSfA = kSfPerAtom, kSfB = kSfPerAtom * (BN / 128);
+    // tensor cores each need the scales of every column).  B's tile columns
+    // [n0, n0 + BN) start on a multiple of 64, so two 128-row scale blocks
+    // cover them for BN = 192 and 256 (kBH column blocks per scale index).
+    constexpr int kBH = BN > 128 ? 2 : 1;
+    constexpr int kSfA = kSfPerAtom, kSfB = kSfPerAtom * kBH;
     constexpr int kSfBytes = kMx ? (kKAtoms * (kSfA + kSfB) * kSfBlock + 1023) / 1024 * 1024 : 0;  // 1 KiB padded
     // A pair tile's 256 accumulator columns leave no room for scales next to a
-    // second accumulator: block-scaled pair tiles use one accumulator.
-    constexpr int kAccBufs = (kMx && kCta2) ? 1 : 2;
+    // second accumulator: block-scaled 256-wide pair tiles use one
+    // accumulator; 192-wide ones keep two (2 x 192 columns + scales).
+    constexpr int kAccBufs = (kMx && kCta2 && BN == 256) ? 1 : 2;
     constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static_assert(kStageBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     // bytes the stage's copies deliver (the scale area's padding is not loaded)
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
     uint8_t* epi_smem = smem + S * kStageBytes;
-    constexpr int kRingWarp = epi_warp_bytes(kMx && kCta2);   // epilogue buffers per warp
+    constexpr int kRingWarp = epi_warp_bytes(kMx && kCta2 && BN == 256);   // epilogue buffers per warp
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_smem + 4 * kRingWarp);
 
     const int warp = threadIdx.x >> 5;
@@ -739,9 +744,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                                 uint8_t* dst = sSf + at * (kSfA + kSfB) * kSfBlock;
                                 load(dst, &p.tmSFA, 0, rb_a * p.num_sfcb + cb);
 #pragma unroll
-                                for (int h = 0; h < BN / 128; ++h)
+                                for (int h = 0; h < kBH; ++h)
                                     load(dst + (kSfA + h * kSfPerAtom) * kSfBlock, &p.tmSFB, 0,
-                                         (n_blk * (BN / 128) + h) * p.num_sfcb + cb);
+                                         ((n_blk * BN) / 128 + h) * p.num_sfcb + cb);
                             }
                         } else if constexpr (kMx) {
                             // scale blocks of this stage's atoms: per atom kSfPerAtom blocks
@@ -863,10 +868,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
 #pragma unroll
                             for (int sb = 0; sb < kSfA; ++sb) cp(blk0 + sb, col0 + 4 * sb);
 #pragma unroll
-                            for (int h = 0; h < BN / 128; ++h)
+                            for (int h = 0; h < kBH; ++h)
 #pragma unroll
                                 for (int sb = 0; sb < kSfPerAtom; ++sb)
-                                    cp(blk0 + kSfA + h * kSfPerAtom + sb, col0 + 4 * kSfA + 4 * (sb * (BN / 128) + h));
+                                    cp(blk0 + kSfA + h * kSfPerAtom + sb, col0 + 4 * kSfA + 4 * (sb * kBH + h));
                         }
                     }
 #pragma unroll
@@ -881,16 +886,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             // per scale-block index, as the MMA reads column n at n / 32)
                             const int at = k / kKSteps, kk = k % kKSteps;
                             const uint32_t a_blocks = sf_base + static_cast<uint32_t>(at * 4 * (kSfA + kSfB));
-                            const uint32_t b_blocks = a_blocks + static_cast<uint32_t>(4 * kSfA);
+                            // B's tile starts (n0 % 128) / 32 columns into its first block
+                            const uint32_t b_blocks = a_blocks + static_cast<uint32_t>(4 * kSfA) +
+                                                      static_cast<uint32_t>(((w.n_blk * BN) & 127) >> 5);
                             uint32_t sfid = 0, a_sf = a_blocks, b_sf = b_blocks;
                             if constexpr (kBlk == 1) {          // one scale per MMA: byte kk of block 0
                                 sfid = static_cast<uint32_t>(kk);
                             } else if constexpr (kBlk == 2) {   // four scales per MMA: all of block kk
                                 a_sf += static_cast<uint32_t>(kk * 4);
-                                b_sf += static_cast<uint32_t>(kk * 4 * (BN / 128));
+                                b_sf += static_cast<uint32_t>(kk * 4 * kBH);
                             } else {                            // two scales per MMA: half of block kk / 2
                                 a_sf += static_cast<uint32_t>((kk / 2) * 4);
-                                b_sf += static_cast<uint32_t>((kk / 2) * 4 * (BN / 128));
+                                b_sf += static_cast<uint32_t>((kk / 2) * 4 * kBH);
                                 sfid = static_cast<uint32_t>((kk & 1) * 2);
                             }
                             const uint32_t id = idesc | (sfid << 4) | (sfid << 29);

@@ -50,6 +50,8 @@ const int g_env_stages = env_int("TCG_STAGES");
 const int g_env_stats = env_int("TCG_STATS");
 // TCG_KATOMS = K atoms per stage for pair tiles (1 or 2; default 2).
 const int g_env_katoms = env_int("TCG_KATOMS");
+// width of block-scaled pair tiles (192 or 256; 0 = the format's default)
+const int g_env_mx_bn = env_int("TCG_MX_BN");
 // TCG_SK: Stream-K schedule.  0 = off (data-parallel tiles, split-K for
 // shapes with too few tiles); 1 = the last partial wave plus one full wave
 // as one Stream-K run, the rest data-parallel; 2 = only the last partial
@@ -284,15 +286,26 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     Plan pl;
     const int K = k_units(ab, K_elems);
     const int bk = tcg::kRowBytes / elem_bytes(ab);
-    const bool mx = is_mx(ab);   // block-scaled: 128 x 128 (one CTA) or 256 x 256 (a pair) tiles
+    const bool mx = is_mx(ab);   // block-scaled: 128 x 128 (one CTA) or 256 x BN (a pair) tiles
     pl.bn = (N <= 128) ? 128 : 256;
     if (mx) {
-        // pairs when there is a full wave of 256 x 256 tiles, else one CTA per 128 x 128
-        const int pairs = ((M + 255) / 256) * ((N + 255) / 256);
+        // Pair tiles: 256 x 256 with one accumulator (the scales take the TMEM
+        // columns of a second one), or 256 x 192 with two accumulators, so
+        // that one tile's epilogue overlaps the next tile's MMAs (not for
+        // NVFP4, whose four scale blocks per atom leave no room).  Measured
+        // on 8192^3 (TFLOP/s, 256 wide vs 192 wide): MXFP8 2241 vs 2141,
+        // MXFP4 3019 vs 3300.
+        int pbn = ab == TCG_MXFP4 ? 192 : 256;
+        if (g_env_mx_bn == 192 || g_env_mx_bn == 256) pbn = g_env_mx_bn;
+        if (g_force_cta2 == 3) pbn = 256;
+        if (g_force_cta2 == 4) pbn = 192;
+        if (ab == TCG_NVFP4) pbn = 256;
+        // pairs when there is a full wave of pair tiles, else one CTA per 128 x 128
+        const int pairs = ((M + 255) / 256) * ((N + pbn - 1) / pbn);
         bool pair = M > tcg::kBM && N > 128 && pairs * 2 >= dev.num_sms && g_force_splits == 0;
-        if (g_force_cta2 == 1) pair = N > 128;
+        if (g_force_cta2 == 1 || g_force_cta2 >= 3) pair = N > 128 && g_force_splits <= 1;
         if (g_force_cta2 == 2) pair = false;
-        pl.bn = pair ? 256 : 128;
+        pl.bn = pair ? pbn : 128;
     }
     // K atoms per stage are decided with the tile shape below; the split-K
     // heuristic works on single-atom k-blocks.
@@ -303,7 +316,7 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // tiles would fill less than half of the SMs.  Measured on GB300: 512^3
     // 12.4 -> 10.3 us; for long K, split-K beats narrowing (16x8192x8192:
     // 49 vs 60 us).
-    if (!mx && g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && pl.num_kb < 16) {
+    if (!mx && g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && g_force_cta2 < 3 && pl.num_kb < 16) {
         while (pl.bn > 64 && num_m1 * ((N + pl.bn - 1) / pl.bn) * 2 < dev.num_sms) pl.bn /= 2;
     }
     const int num_n = (N + pl.bn - 1) / pl.bn;
@@ -318,12 +331,14 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
         splits = std::max(1, std::min(splits, 16));
     }
     splits = std::max(1, std::min(splits, std::max(pl.num_kb, 1)));
+    if (mx && pl.bn > 128) splits = 1;   // block-scaled pair tiles do not split K
     // 2-CTA pair tiles (256 x BN) when K is not split and there is at least
     // one full wave of pairs; they halve the operand bytes each SM streams.
     const int num_m2 = (M + 2 * tcg::kBM - 1) / (2 * tcg::kBM);
     bool cta2 = splits == 1 && pl.bn == 256 && M > tcg::kBM && num_m2 * num_n * 2 >= dev.num_sms;
-    if (g_force_cta2 == 1) cta2 = splits == 1 && pl.bn == 256;
-    if (g_force_cta2 == 2 || (mx && pl.bn != 256)) cta2 = false;
+    if (g_force_cta2 == 1 || g_force_cta2 >= 3) cta2 = splits == 1 && pl.bn == 256;
+    if (mx) cta2 = pl.bn > 128;
+    if (g_force_cta2 == 2) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
     pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
     // block-scaled: two K atoms per stage on pair tiles, else one.  Measured on
@@ -331,8 +346,10 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // pairs 2217 -> 2515 (5 x 1 -> 2 x 2)
     if (mx) pl.katoms = g_env_katoms > 0 ? std::min(g_env_katoms, 2) : (cta2 ? 2 : 1);
     if (mx && is_fp4(ab) && !cta2) pl.katoms = 1;
-    // scale blocks per stage atom: A's rows, then B's columns (a pair holds all 256)
-    const int sfb = mx ? sf_blocks_per_atom(ab) * (1 + pl.bn / 128) : 0;
+    if (mx && pl.bn == 192) pl.katoms = 2;
+    // scale blocks per stage atom: A's rows, then B's columns (a pair holds the
+    // two 128-column blocks its 192 or 256 columns overlap)
+    const int sfb = mx ? sf_blocks_per_atom(ab) * (1 + (pl.bn > 128 ? 2 : 1)) : 0;
     pl.num_kb = (K + pl.katoms * bk - 1) / (pl.katoms * bk);
     pl.num_m = cta2 ? num_m2 : num_m1;
     pl.num_n = num_n;
@@ -344,13 +361,13 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // plus B rows small: about 19 x 8 blocks of 128 x 256 tiles, 8 x 9 pairs.
     pl.group_m = cta2 ? 8 : 16;
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
-    const bool small_ring = mx && cta2;   // block-scaled pair tiles: half-size epilogue ring
+    const bool small_ring = mx && cta2 && pl.bn == 256;   // 256-wide block-scaled pairs: half-size epilogue ring
     int stages = (dev.max_smem_optin - fixed_smem_bytes(small_ring)) / stage_bytes(pl.bn, cta2, pl.katoms, sfb);
     stages = std::max(2, std::min(stages, 8));
     if (mx) {
-        // TMEM: accumulators (2 x 128 columns, or one 256-column pair accumulator) plus
-        // 4 columns per scale block per stage atom
-        const int sf_cols = 512 - 256;
+        // TMEM: accumulators (2 x 128 or 2 x 192 columns, or one 256-column pair
+        // accumulator) plus 4 columns per scale block per stage atom
+        const int sf_cols = 512 - (pl.bn == 192 ? 2 * 192 : 256);
         stages = std::max(2, std::min(stages, sf_cols / (4 * sfb * pl.katoms)));
     }
     if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
@@ -452,6 +469,9 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     int n = 0;
     if (bn == 256 && katoms == 2) n = fp8 ? active_pairs_for<256, true, 2>(smem) : active_pairs_for<256, false, 2>(smem);
     if (bn == 256 && katoms == 1) n = fp8 ? active_pairs_for<256, true, 1>(smem) : active_pairs_for<256, false, 1>(smem);
+    // 192-wide (block-scaled) pairs: residency is set by the shared memory, the
+    // block size and the cluster shape, which the 256-wide kernel shares
+    if (bn == 192) n = active_pairs_for<256, true, 2>(smem);
     cache[key] = n;
     return n;
 }
@@ -727,7 +747,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     {
         // chunk buffers per epilogue warp: 8 KiB over the larger of the C and D boxes
         const int box = 32 * 32 * std::max(elem_bytes(d_dtype), kp.c_tma ? elem_bytes(c_dtype) : 0);
-        kp.epi_nbuf = tcg::epi_warp_bytes(is_mx(ab_dtype) && pl.cluster == 2) / box;
+        kp.epi_nbuf = tcg::epi_warp_bytes(is_mx(ab_dtype) && pl.cluster == 2 && pl.bn == 256) / box;
     }
     kp.bias_vec = epi.bias && aligned16(epi.bias);
     kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
@@ -752,9 +772,11 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         if (ab_dtype == TCG_NVFP4)
             return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 2>(kp, pl, stream)
                                   : launch_kernel<256, true, true, 1, 2>(kp, pl, stream);
+        if (ab_dtype == TCG_MXFP4 && pl.bn == 192) return launch_kernel<192, true, true, 2, 3>(kp, pl, stream);
         if (ab_dtype == TCG_MXFP4)
             return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 3>(kp, pl, stream)
                                   : launch_kernel<256, true, true, 1, 3>(kp, pl, stream);
+        if (pl.bn == 192) return launch_kernel<192, true, true, 2, 1>(kp, pl, stream);
         return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 1>(kp, pl, stream)
                               : launch_kernel<256, true, true, 1, 1>(kp, pl, stream);
     }
