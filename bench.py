@@ -71,7 +71,23 @@ WORKLOADS = {
     "gemm8192_e4m3_bias_relu": (lambda inputs: inputs.fp8_8192_relu(), True),
     "gemm8192_mxe4m3_bias_relu": (lambda inputs: inputs.mxfp8_8192_relu("e4m3"), True),
     "gemm8192_nvfp4_bias_relu": (lambda inputs: inputs.nvfp4_8192_relu(), True),
+    # grouped GEMM: 16 MoE experts, 32768 routed rows, 4096 x 4096 weights (768 MiB of operands)
+    "grouped_moe16_32768x4096x4096_bias_gelu": (lambda inputs: inputs.grouped_moe(), False),
 }
+
+
+def is_grouped(case):
+    return hasattr(case, "problems")
+
+
+def head(case):
+    """The problem whose shared attributes (types, layouts, epilogue) describe the case."""
+    return case.problems[0] if is_grouped(case) else case
+
+
+def largest(case):
+    """The problem the oracle samples rows from (the only one for a single GEMM)."""
+    return max(case.problems, key=lambda p: p.M) if is_grouped(case) else case
 
 def metric_name(workload):
     return METRIC if workload == DEFAULT_WORKLOAD else f"GEMM TFLOP/s ({workload}), 1 GPU"
@@ -81,14 +97,30 @@ _EB = {"bf16": 2, "f16": 2, "e4m3": 1, "e5m2": 1, "f32": 4, "nvfp4": 0.5, "mxfp4
 
 
 def case_bytes(case):
-    """Algorithmic bytes of one launch: A and B once, C once if beta != 0, D once, bias once."""
+    """Algorithmic bytes of one launch: A and B once, C once if beta != 0, D once, bias once
+    (summed over the problems of a grouped GEMM)."""
     from tiled_tensor_core_persistent_gb300 import analysis
+    if is_grouped(case):
+        return sum(case_bytes(p) for p in case.problems)
     return analysis.gemm_bytes(case.M, case.N, case.K, _EB[case.ab_dtype], _EB[case.d_dtype],
                                _EB[case.c_dtype] if case.C is not None else 0,
                                _EB[case.bias_dtype] if case.bias is not None else 0)
 
 
 def workload_config(case, flush):
+    if is_grouped(case):
+        h = head(case)
+        cfg = workload_config(h, flush)
+        epi = cfg["workload"].split("D = ")[1].rsplit(" (", 1)[0]
+        ab = sum(t.numel() * t.element_size() for p in case.problems for t in (p.A, p.B))
+        cfg.update(
+            workload=f"grouped gemm, {len(case.problems)} problems M_g x {h.N} x {h.K} "
+                     f"(M_g = {'/'.join(str(p.M) for p in case.problems)}) {h.ab_dtype}, A {h.opA}-major / "
+                     f"B {h.opB}-major, per problem D = {epi} ({case.name})",
+            M=sum(p.M for p in case.problems), N=h.N, K=h.K, problems=[[p.M, p.N, p.K] for p in case.problems])
+        if not flush:
+            cfg["l2"] = f"inputs larger than L2 (A+B {ab / 2**20:.0f} MiB > 129 MB), no flush"
+        return cfg
     epi = []
     if case.C is not None:
         epi.append(f"beta*C ({case.c_dtype})")
@@ -260,7 +292,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     from tiled_tensor_core_persistent_gb300 import inputs
-    case = WORKLOADS[args.workload][0](inputs)
+    whole = WORKLOADS[args.workload][0](inputs)
+    case = largest(whole)
     cores = os.cpu_count() or 1
     # size each step so the whole run stays within about a minute
     prob = oracle_problem(case)
@@ -277,11 +310,12 @@ def run_reference(args):
         t += cpu_oracle_rows(case, rng_rows(args.warmup + i), prob=prob)
     flops = 2.0 * rows_per_step * case.N * case.K * args.steps
     value = flops / t / 1e12
-    sample = f"{rows_per_step} full rows of D (x {case.N} cols x K={case.K}) per step"
+    sample = f"{rows_per_step} full rows of D (x {case.N} cols x K={case.K}) per step" + \
+        (f", of the grouped GEMM's largest problem ({case.M} rows)" if is_grouped(whole) else "")
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(case, WORKLOADS[args.workload][1]),
+            "data": "synthetic", "config": workload_config(whole, WORKLOADS[args.workload][1]),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -334,7 +368,10 @@ def run_ours(args):
     factory, flush = WORKLOADS[args.workload]
     case = factory(inputs)
     stream = torch.cuda.Stream(device=device)
-    dc = harness.DeviceCase(case, device=device, stream=stream)
+    if is_grouped(case):
+        dc = harness.GroupedDeviceCase(case, device=device, stream=stream)
+    else:
+        dc = harness.DeviceCase(case, device=device, stream=stream)
     torch.cuda.synchronize(device)
 
     # warm-up
@@ -371,7 +408,7 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    in_bytes = _EB[case.ab_dtype]
+    in_bytes = _EB[head(case).ab_dtype]
     # dense tensor peak of the operand type: fp8 = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
     # dense tensor peak of the operand type from the measured bf16 peak and the
     # nominal dense ratios of GB300: fp8 4.5 / 2.25 = 2, fp4 13.5 / 2.25 = 6
@@ -379,7 +416,11 @@ def run_ours(args):
     tensor_peak = bf16_peak * ratio
     nominal = 2250.0 * ratio
     alg_bytes = case_bytes(case)
-    intensity = analysis.boundary_intensity(case.M, case.N, case.K, in_bytes)
+    if is_grouped(case):
+        # the pages' intensity 2MNK / (b (MK + KN + MN)) over the whole batch
+        intensity = flops / (in_bytes * sum(p.M * p.K + p.K * p.N + p.M * p.N for p in case.problems))
+    else:
+        intensity = analysis.boundary_intensity(case.M, case.N, case.K, in_bytes)
     hbm_bound = intensity * hbm * 1e-3 < tensor_peak
     gbs = alg_bytes / (ms_per_step * 1e-3) / 1e9
     roof = {"bound": "hbm" if hbm_bound else "tensor",
@@ -402,21 +443,26 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # a bounded sample: about 15 s of oracle work on the host cores
-        prob = oracle_problem(case)
-        n_probe = min(16, case.M)
-        t_probe = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // n_probe)))[:n_probe], prob=prob)
-        nrows = int(min(case.M, max(n_probe, 15.0 / max(t_probe / n_probe, 1e-6))))
-        t = cpu_oracle_rows(case, list(range(0, case.M, max(1, case.M // nrows)))[:nrows], prob=prob)
-        cpu = {"value": 2.0 * nrows * case.N * case.K / t / 1e12, "unit": UNIT,
+        big = largest(case)
+        prob = oracle_problem(big)
+        n_probe = min(16, big.M)
+        t_probe = cpu_oracle_rows(big, list(range(0, big.M, max(1, big.M // n_probe)))[:n_probe], prob=prob)
+        nrows = int(min(big.M, max(n_probe, 15.0 / max(t_probe / n_probe, 1e-6))))
+        t = cpu_oracle_rows(big, list(range(0, big.M, max(1, big.M // nrows)))[:nrows], prob=prob)
+        cpu = {"value": 2.0 * nrows * big.N * big.K / t / 1e12, "unit": UNIT,
                "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{nrows} full rows of D ({nrows}x{case.N}x{case.K}), {t:.1f} s wall"}
+               "sample": f"{nrows} full rows of D ({nrows}x{big.N}x{big.K}), {t:.1f} s wall" +
+                         (f", of the grouped GEMM's largest problem ({big.M} rows)" if is_grouped(case) else "")}
 
-    plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
+    if is_grouped(case):
+        plan = tcg.grouped_plan([dict(M=p.M, N=p.N, K=p.K) for p in case.problems], head(case).ab_dtype)
+    else:
+        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
     if rank == 0:
         line = {"metric": metric_name(args.workload),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": case.ab_dtype, "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": head(case).ab_dtype, "data": "synthetic",
                 "config": dict(workload_config(case, flush), plan=plan),
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": args.steps}
@@ -433,30 +479,24 @@ def inputs_blocked(sf):
 
 def run_e2e(args, case, dc, stream, device, tcg):
     import torch
-    A_h = case.A.pin_memory()
-    B_h = case.B.pin_memory()
-    bias_h = case.bias.pin_memory() if case.bias is not None else None
-    C_h = case.C.pin_memory() if case.C is not None else None
-    sf_h = [(torch.from_numpy(inputs_blocked(x)).pin_memory(), dev) for x, dev in ((case.sfa, dc.sfa), (case.sfb, dc.sfb))
-            if x is not None]
-    D_h = torch.empty(dc.D_view.shape, dtype=dc.D_view.dtype).pin_memory()
-    h2d = A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size() + \
-        (bias_h.numel() * bias_h.element_size() if bias_h is not None else 0) + \
-        (C_h.numel() * C_h.element_size() if C_h is not None else 0) + sum(h.numel() for h, _ in sf_h)
-    d2h = D_h.numel() * D_h.element_size()
+    # (pinned host tensor, device tensor) pairs copied in before and out after every step
+    ins, outs = [], []
+    for p, d in (zip(case.problems, dc.parts) if is_grouped(case) else [(case, dc)]):
+        ins += [(t.pin_memory(), dev) for t, dev in ((p.A, d.A), (p.B, d.B), (p.bias, d.bias), (p.C, d.C))
+                if t is not None]
+        ins += [(torch.from_numpy(inputs_blocked(x)).pin_memory(), dev)
+                for x, dev in ((p.sfa, d.sfa), (p.sfb, d.sfb)) if x is not None]
+        outs.append((torch.empty(d.D_view.shape, dtype=d.D_view.dtype).pin_memory(), d.D_view))
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
 
     def step():
         with torch.cuda.stream(stream):
-            dc.A.copy_(A_h, non_blocking=True)
-            dc.B.copy_(B_h, non_blocking=True)
-            if bias_h is not None:
-                dc.bias.copy_(bias_h, non_blocking=True)
-            if C_h is not None:
-                dc.C.copy_(C_h, non_blocking=True)
-            for h, dev in sf_h:
+            for h, dev in ins:
                 dev.copy_(h, non_blocking=True)
             dc.run(stream)
-            D_h.copy_(dc.D_view, non_blocking=True)
+            for h, dev in outs:
+                h.copy_(dev, non_blocking=True)
 
     for _ in range(2):
         step()
@@ -472,7 +512,8 @@ def run_e2e(args, case, dc, stream, device, tcg):
     ms = ev0.elapsed_time(ev1) / n
     return {"value": case.flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
-            "path": "pinned host A, B, C, bias, block scales -> device (cudaMemcpyAsync), tcg_gemm, D -> pinned host"}
+            "path": "pinned host A, B, C, bias, block scales -> device (cudaMemcpyAsync), " +
+                    ("tcg_gemm_grouped" if is_grouped(case) else "tcg_gemm") + ", D -> pinned host"}
 
 
 def main():

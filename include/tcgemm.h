@@ -261,6 +261,81 @@ tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha,
                             tcg_epilogue epi, tcg_dtype ab_dtype, tcg_scales scales,
                             void* stream);
 
+/*
+ * Grouped GEMM ("CUTLASS" page, Part V, numeric-types deep dive: a
+ * mixture-of-experts layer becomes a grouped GEMM in which each expert is one
+ * problem of a batch of differently shaped problems; Part III: grouped GEMMs
+ * with irregular shapes).  One launch computes, for every problem g,
+ *
+ *     D_g = act( alpha_g * (A_g @ B_g) + beta * C_g + bias_g )
+ *
+ * Each problem has its own sizes, alpha, operands, C, bias and D; the operand
+ * type, the layouts of A and B, beta, the activation and the C / D / bias
+ * types are shared.  Problems are independent: no output may overlap another
+ * problem's inputs or output.
+ *
+ * tcg_problem: M, N, K >= 0 and the pointers / leading dimensions of one
+ * problem, with the meaning they have in tcg_gemm.  alpha: this problem's
+ * factor (for FP8 operands, alpha * scale_a * scale_b of its per-tensor
+ * scales).  bias: NULL or N elements of the shared bias type.  C is read only
+ * when beta != 0.
+ */
+typedef struct {
+    int M, N, K;
+    float alpha;
+    const void* A;
+    int lda;
+    const void* B;
+    int ldb;
+    const void* C;
+    int ldc;
+    void* D;
+    int ldd;
+    const void* bias;
+} tcg_problem;
+
+/*
+ * tcg_grouped_workspace_size -- bytes of workspace tcg_gemm_grouped needs for
+ * num_problems problems: the 256-byte status header plus a table of one
+ * parameter block per problem (tensor maps, sizes, pointers) and the first
+ * unit of each.  Zero-fill it once (tcg_workspace_init).  0 if num_problems < 0.
+ */
+size_t tcg_grouped_workspace_size(int num_problems);
+
+/*
+ * tcg_gemm_grouped -- every problem of problems[0 .. num_problems) in one
+ * persistent launch on `stream`: the tiles of all problems form one list of
+ * units that the CTAs (or CTA pairs) take in turn.
+ *   problems: host array, read during the call only.
+ *   opA, opB, beta, c_dtype, d_dtype, ab_dtype: shared, as in tcg_gemm;
+ *     ab_dtype BF16, F16, E4M3 or E5M2 (the block-scaled types: TCG_ERR_UNSUPPORTED).
+ *   epi: bias_dtype and act shared; epi.bias is ignored (each problem has its own).
+ *   Each problem must pass tcg_can_implement, and its A and B (when K > 0)
+ *   must be TMA-addressable: 16-byte aligned with ld * sizeof(element) a
+ *   multiple of 16 (no packed slow path here; else TCG_ERR_UNSUPPORTED).  C,
+ *   D and bias may be unaligned as in tcg_gemm.  Problems with M == 0 or
+ *   N == 0 are skipped; K == 0 gives act(beta * C + bias) for that problem.
+ *   workspace: at least tcg_grouped_workspace_size(num_problems) bytes,
+ *     16-byte aligned, else TCG_ERR_WORKSPACE.  The call copies its table
+ *     there with one host-to-device copy on `stream` (so it is not meant for
+ *     stream capture into a CUDA graph), and calls on one workspace must be
+ *     ordered (one stream).
+ * Errors: the first failing problem's tcg_can_implement code, then as
+ * tcg_gemm; nothing is queued on an error.  Device-side wait timeouts are
+ * read with tcg_device_status, as for tcg_gemm.
+ */
+tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* problems,
+                            tcg_layout opA, tcg_layout opB, float beta,
+                            tcg_dtype c_dtype, tcg_dtype d_dtype, tcg_epilogue epi,
+                            tcg_dtype ab_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * tcg_grouped_plan -- the launch plan tcg_gemm_grouped would use, in the
+ * layout of tcg_plan (units = the tiles of all problems; splits = 1).
+ * Needs the current device.
+ */
+tcg_status tcg_grouped_plan(int num_problems, const tcg_problem* problems, tcg_dtype ab_dtype, int out[10]);
+
 #ifdef __cplusplus
 }
 #endif

@@ -188,6 +188,17 @@ class Problem:
         return out
 
 
+def grouped(problems) -> list:
+    """A grouped GEMM: a batch of independent problems of different shapes,
+    each computed by the one-GEMM identity above with its own operands,
+    C, bias and output.  "CUTLASS" page, Part V (numeric-types deep dive): a
+    mixture-of-experts layer becomes a grouped GEMM in which each expert is
+    one problem of a batch of differently shaped problems; Part III: grouped
+    GEMMs with irregular shapes.  Returns the full fp64 result of every
+    problem, in order (an M == 0 or N == 0 problem gives an empty array)."""
+    return [p.full() for p in problems]
+
+
 def decode_bf16(bits: np.ndarray) -> np.ndarray:
     bits = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(bits.shape, dtype=np.float64)

@@ -132,3 +132,32 @@ def test_k_zero_needs_no_operands(lib):
 def test_workspace_size_without_device(lib):
     assert tcg.workspace_size(8192, 8192, 8192) >= 256
     assert tcg.workspace_size(-1, 4, 4) == 0
+
+
+# ---------------------------------------------------------------- grouped GEMM
+
+def grouped(lib, problems, ab="bf16", ws=0x60000, ws_bytes=1 << 20):
+    arr = tcg._problems(problems)
+    return lib.tcg_gemm_grouped(len(problems), arr, tcg.ROW, tcg.COL, 0.0, tcg.BF16, tcg.BF16,
+                                tcg.Epilogue(None, tcg.BF16, tcg.ACT_NONE), tcg.DTYPES[ab], ws, ws_bytes, None)
+
+
+def test_grouped_validation_without_device(lib):
+    ok = dict(M=300, N=200, K=128, A=A, lda=128, B=B, ldb=128, D=D, ldd=200)
+    assert lib.tcg_gemm_grouped(-1, None, 0, 1, 0.0, 0, 0, tcg.Epilogue(None, 0, 0), 0, None, 0, None) == 1
+    assert grouped(lib, [ok, dict(ok, lda=100)]) == 1                 # lda < K in the second problem
+    assert grouped(lib, [ok, dict(ok, lda=136, A=A + 2)]) == 2        # A not TMA-addressable: no slow path here
+    assert grouped(lib, [ok, dict(ok, ldb=129)]) == 2
+    assert grouped(lib, [ok], ab="mxe4m3") == 2                       # block-scaled types are not taken
+    assert grouped(lib, [dict(ok, A=A + 1)]) == 3                     # not aligned to the element
+    assert grouped(lib, [dict(ok, M=0), dict(ok, N=0)]) == 0          # nothing to compute
+    assert grouped(lib, []) == 0
+    # a valid request needs the device (none here)
+    assert grouped(lib, [ok, dict(ok, M=1, K=0, A=None, B=None)]) in (4, 6)
+
+
+def test_grouped_workspace_size(lib):
+    sizes = [tcg.grouped_workspace_size(g) for g in (0, 1, 16, 1000)]
+    assert all(s >= 256 and s % 256 == 0 for s in sizes)
+    assert sizes == sorted(sizes) and sizes[-1] > sizes[1]
+    assert tcg.grouped_workspace_size(-1) == 0

@@ -530,3 +530,61 @@ def test_fp4_quantiser_keeps_values_within_one_step():
     scale = np.repeat(oracle.decode_ue4m3(case.sfa), 16, axis=1)
     # the largest E2M1 step is 2 (between 4 and 6): half a step of the scaled grid, plus the scale's rounding
     assert np.all(np.abs(vals - x) <= 1.0 * scale + 0.07 * np.abs(x))
+
+
+# ---------------------------------------------------------------- grouped GEMM
+
+def _rank_one_problem(M, N, K, rng, layouts=("row", "col")):
+    """A = u v^T, B = w x^T with small integers: D = (v . w) u x^T exactly."""
+    u = rng.integers(-3, 4, M).astype(np.float64)
+    v = rng.integers(-3, 4, K).astype(np.float64)
+    w = rng.integers(-3, 4, K).astype(np.float64)
+    x = rng.integers(-3, 4, N).astype(np.float64)
+    A, lda = store(np.outer(u, v), layouts[0])
+    B, ldb = store(np.outer(w, x), layouts[1])
+    prob = oracle.Problem(M, N, K, bf16_bits(A), lda, op(layouts[0]), bf16_bits(B), ldb, op(layouts[1]))
+    return prob, float(v @ w) * np.outer(u, x)
+
+
+def test_grouped_rank_one_closed_forms():
+    """Every problem of a batch of different shapes gets its own closed form,
+    so a problem index mixed up anywhere (operands, sizes, output) fails."""
+    rng = np.random.default_rng(31)
+    shapes = [(5, 7, 3), (1, 12, 9), (9, 1, 4), (6, 6, 1), (3, 8, 17)]
+    layouts = [("row", "col"), ("col", "row"), ("row", "row"), ("col", "col"), ("row", "col")]
+    probs, refs = zip(*(_rank_one_problem(M, N, K, rng, lay) for (M, N, K), lay in zip(shapes, layouts)))
+    got = oracle.grouped(list(probs))
+    assert len(got) == len(shapes)
+    for g, (d, ref, (M, N, K)) in enumerate(zip(got, refs, shapes)):
+        assert d.shape == (M, N), g
+        assert np.array_equal(d, ref), g
+
+
+def test_grouped_problems_are_independent():
+    """Changing one problem's inputs changes that problem's output only."""
+    rng = np.random.default_rng(32)
+    p0, r0 = _rank_one_problem(4, 5, 6, rng)
+    p1, r1 = _rank_one_problem(3, 2, 7, rng)
+    p1b, r1b = _rank_one_problem(3, 2, 7, rng)
+    assert not np.array_equal(r1, r1b)
+    a = oracle.grouped([p0, p1])
+    b = oracle.grouped([p0, p1b])
+    assert np.array_equal(a[0], r0) and np.array_equal(b[0], r0)
+    assert np.array_equal(a[1], r1) and np.array_equal(b[1], r1b)
+
+
+def test_grouped_empty_and_k_zero_problems():
+    """An M == 0 problem contributes an empty result; a K == 0 problem is
+    act(beta * C + bias), like a single GEMM with K == 0."""
+    rng = np.random.default_rng(33)
+    empty = oracle.Problem(0, 4, 8, np.zeros((1, 8), np.uint16), 8, oracle.ROW,
+                           np.zeros((4, 8), np.uint16), 8, oracle.COL)
+    c_bits = bf16_bits(rng.uniform(-1, 1, (2, 3)))
+    bias_bits = bf16_bits(rng.uniform(-1, 1, 3))
+    k0 = oracle.Problem(2, 3, 0, np.zeros((2, 8), np.uint16), 8, oracle.ROW, np.zeros((3, 8), np.uint16), 8,
+                        oracle.COL, beta=0.5, C=c_bits, ldc=3, bias=bias_bits, act="relu")
+    p2, r2 = _rank_one_problem(2, 2, 2, rng)
+    got = oracle.grouped([empty, k0, p2])
+    assert got[0].shape == (0, 4)
+    assert np.array_equal(got[1], np.maximum(0.5 * bf16_values(c_bits) + bf16_values(bias_bits)[None, :], 0.0))
+    assert np.array_equal(got[2], r2)

@@ -34,7 +34,7 @@ STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "T
 
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
             "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc",
-            "tcg_debug_schedule"]
+            "tcg_debug_schedule", "tcg_grouped_workspace_size", "tcg_gemm_grouped", "tcg_grouped_plan"]
 
 
 class TcgError(RuntimeError):
@@ -51,6 +51,14 @@ class Scales(ctypes.Structure):
     _fields_ = [("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float),
                 ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p),
                 ("block_sfa", ctypes.c_void_p), ("block_sfb", ctypes.c_void_p)]
+
+
+class Problem(ctypes.Structure):
+    """tcg_problem: one problem of a grouped GEMM."""
+    _fields_ = [("M", ctypes.c_int), ("N", ctypes.c_int), ("K", ctypes.c_int), ("alpha", ctypes.c_float),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int), ("B", ctypes.c_void_p), ("ldb", ctypes.c_int),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int), ("D", ctypes.c_void_p), ("ldd", ctypes.c_int),
+                ("bias", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -98,6 +106,13 @@ def lib() -> ctypes.CDLL:
         L.tcg_debug_set.restype = None
         L.tcg_debug_schedule.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int), i32]
         L.tcg_debug_schedule.restype = i32
+        L.tcg_grouped_workspace_size.argtypes = [i32]
+        L.tcg_grouped_workspace_size.restype = sz
+        L.tcg_gemm_grouped.argtypes = [i32, ctypes.POINTER(Problem), i32, i32, f32, i32, i32, Epilogue, i32, P, sz,
+                                       P]
+        L.tcg_gemm_grouped.restype = i32
+        L.tcg_grouped_plan.argtypes = [i32, ctypes.POINTER(Problem), i32, ctypes.POINTER(ctypes.c_int)]
+        L.tcg_grouped_plan.restype = i32
         _lib = L
         return L
 
@@ -213,3 +228,41 @@ def debug_schedule(M, N, K, ab_dtype="bf16", num_sms=152, sk_mode=-1) -> list:
 def debug_set(fault_inject=0, wait_timeout_ns=0, force_splits=0, force_cta2=0) -> None:
     """TEST-ONLY knobs (see tcg_debug_set in tcgemm.h)."""
     lib().tcg_debug_set(int(fault_inject), int(wait_timeout_ns), int(force_splits), int(force_cta2))
+
+
+def _problems(problems):
+    """A tcg_problem array from dicts with keys M, N, K, alpha (default 1), A, lda, B, ldb, C, ldc,
+    D, ldd, bias."""
+    arr = (Problem * max(len(problems), 1))()
+    for i, q in enumerate(problems):
+        arr[i] = Problem(int(q["M"]), int(q["N"]), int(q["K"]), float(q.get("alpha", 1.0)), _addr(q.get("A")),
+                         int(q.get("lda", 0)),
+                         _addr(q.get("B")), int(q.get("ldb", 0)), _addr(q.get("C")), int(q.get("ldc", 0)),
+                         _addr(q.get("D")), int(q.get("ldd", 0)), _addr(q.get("bias")))
+    return arr
+
+
+def grouped_workspace_size(num_problems: int) -> int:
+    return int(lib().tcg_grouped_workspace_size(int(num_problems)))
+
+
+def gemm_grouped(problems, opA, opB, beta, c_dtype, d_dtype, *, bias_dtype="bf16", act="none",
+                 ab_dtype="bf16", workspace=None, workspace_bytes=0, stream=None) -> None:
+    """Queue every problem of a grouped GEMM in one launch (tcg_gemm_grouped in tcgemm.h).
+    problems: dicts with M, N, K, alpha, A, lda, B, ldb, C, ldc, D, ldd and bias (None allowed)."""
+    arr = _problems(problems)
+    epi = Epilogue(None, _enum(bias_dtype, DTYPES), _enum(act, ACTS))
+    st = lib().tcg_gemm_grouped(len(problems), arr, _enum(opA, LAYOUTS), _enum(opB, LAYOUTS), beta,
+                                _enum(c_dtype, DTYPES), _enum(d_dtype, DTYPES), epi, _enum(ab_dtype, DTYPES),
+                                _addr(workspace), int(workspace_bytes), _stream(stream))
+    if st != 0:
+        raise TcgError(st, "tcg_gemm_grouped", last_error())
+
+
+def grouped_plan(problems, ab_dtype="bf16") -> dict:
+    out = (ctypes.c_int * 10)()
+    st = lib().tcg_grouped_plan(len(problems), _problems(problems), _enum(ab_dtype, DTYPES), out)
+    if st != 0:
+        raise TcgError(st, "tcg_grouped_plan", last_error())
+    keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem"]
+    return dict(zip(keys, list(out)))

@@ -1,8 +1,8 @@
 """Compile the in-tree CUDA library (libtcgemm.so) for sm_103a with nvcc.
 
-One translation unit, one -gencode, no cmake: the same command runs on the
-x86 development machine (cross-compilation, no GPU needed) and on the Arm GPU
-machines.  The result lands in ``_build/`` next to this file.
+Three translation units compiled in parallel, one -gencode, no cmake: the
+same commands run on the x86 development machine (cross-compilation, no GPU
+needed) and on the Arm GPU machines.  The result lands in ``_build/`` next to this file.
 """
 from __future__ import annotations
 
@@ -17,6 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(OUT_DIR, "libtcgemm.so")
 GENCODE = "arch=compute_103a,code=sm_103a"
+UNITS = ("tcgemm_host", "launch_block_scaled", "launch_grouped")
 
 
 def _nvcc() -> str:
@@ -39,9 +40,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if os.path.getmtime(SO_PATH) >= newest:
             return SO_PATH
     tmp = SO_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-shared", "-Xptxas", "-v" if verbose else "-O3", "-o", tmp,
-           os.path.join(CSRC, "tcgemm_host.cu")]
-    subprocess.run(cmd, check=True)
+    flags = ["-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+             "-Xptxas", "-v" if verbose else "-O3"]
+    # The kernel's instantiations are split over these translation units,
+    # compiled in parallel, then linked into one shared library.
+    objs, procs = [], []
+    for unit in UNITS:
+        obj = os.path.join(OUT_DIR, f"{unit}.{os.getpid()}.o")
+        objs.append(obj)
+        procs.append(subprocess.Popen([_nvcc(), *flags, "-c", "-o", obj, os.path.join(CSRC, f"{unit}.cu")]))
+    failed = [UNITS[i] for i, pr in enumerate(procs) if pr.wait() != 0]
+    try:
+        if failed:
+            raise RuntimeError(f"nvcc failed on {', '.join(failed)}")
+        subprocess.run([_nvcc(), "-gencode", GENCODE, "-shared", "-o", tmp, *objs], check=True)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     os.replace(tmp, SO_PATH)
     return SO_PATH

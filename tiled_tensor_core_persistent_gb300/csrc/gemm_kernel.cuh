@@ -104,6 +104,13 @@ struct KernelParams {
     const uint8_t* sfa;
     const uint8_t* sfb;
     int num_sfcb;               // 4-scale column blocks per row (ceil(ceil(K / block) / 4))
+    // Grouped GEMM (the kGrouped kernels): num_groups independent problems,
+    // each with a complete parameter block of its own in global memory (its
+    // tensor maps, sizes, pointers and tile grid); problem g owns the units
+    // [group_tile0[g], group_tile0[g + 1]) of the launch.
+    const KernelParams* group;
+    const int* group_tile0;
+    int num_groups;
 };
 
 
@@ -143,7 +150,7 @@ __device__ __forceinline__ void record_timeout(const KernelParams& p, int where)
 // the limit passes or, if honor_abort, another role of this CTA already gave
 // up.  Drain waits pass honor_abort = false: they must see their own copies
 // land even after an abort, and are still bounded by the limit.
-__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const KernelParams& p,
+static __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const KernelParams& p,
                                         SmemCtl* ctl, int where, long long limit_ns,
                                         bool honor_abort = true) {
     const uint32_t a = ptx::smem_u32(bar);
@@ -180,6 +187,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 struct Unit {
     int m_blk, n_blk, tile, split, nsplit, kb0, kb1, slot_tile;
     int sk, tl, w_first;
+    int g;   // problem of a grouped GEMM (0 otherwise)
 };
 
 // Tile index -> (m_blk, n_blk) in the grouped raster order: groups of
@@ -204,6 +212,7 @@ __host__ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int 
     w.sk = 0;
     w.tl = 0;
     w.w_first = 0;
+    w.g = 0;
     tile_coords(p, w.tile, w.m_blk, w.n_blk);
     w.kb0 = static_cast<int>((static_cast<long long>(w.split) * p.num_kb) / w.nsplit);
     w.kb1 = static_cast<int>((static_cast<long long>(w.split + 1) * p.num_kb) / w.nsplit);
@@ -261,6 +270,7 @@ __host__ __device__ __forceinline__ bool work_next(const KernelParams& p, WorkIt
     const int tl = static_cast<int>(s.it / p.num_kb);
     w.sk = 1;
     w.tl = tl;
+    w.g = 0;
     w.tile = p.units_a / p.splits + tl;
     tile_coords(p, w.tile, w.m_blk, w.n_blk);
     w.kb0 = static_cast<int>(s.it - static_cast<long long>(tl) * p.num_kb);
@@ -273,6 +283,38 @@ __host__ __device__ __forceinline__ bool work_next(const KernelParams& p, WorkIt
     w.slot_tile = 0;
     s.it += w.kb1 - w.kb0;
     return true;
+}
+
+// Grouped GEMM ("CUTLASS" page, Part V: a mixture-of-experts layer as a
+// grouped GEMM, one problem per expert, of different shapes): the launch's
+// units are the tiles of every problem, problem after problem; a worker takes
+// every workers-th unit, finds its problem by binary search over the first
+// units, and decodes the tile in that problem's own grid and raster.
+template <bool kGrouped>
+__device__ __forceinline__ bool next_unit(const KernelParams& p, WorkIter& s, Unit& w) {
+    if constexpr (!kGrouped) {
+        return work_next(p, s, w);
+    } else {
+        if (s.u >= p.num_units) return false;
+        const int u = s.u;
+        s.u += s.workers;
+        int lo = 0, hi = p.num_groups - 1;   // the last problem whose first unit is <= u
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.group_tile0 + mid) <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        w = decode_unit(p.group[lo], u - __ldg(p.group_tile0 + lo));
+        w.g = lo;
+        return true;
+    }
+}
+
+// The parameters of a unit's problem: the launch's own, or its problem's block.
+template <bool kGrouped>
+__device__ __forceinline__ const KernelParams& unit_params(const KernelParams& p, const Unit& w) {
+    if constexpr (kGrouped) return p.group[w.g];
+    else return p;
 }
 
 
@@ -591,7 +633,11 @@ __device__ __forceinline__ void store_chunk_direct(const KernelParams& p, const 
 // (512 bytes per 128 rows and 4 scales: 1, 4 or 2 blocks per atom per
 // operand), which the MMA thread copies to TMEM with tcgen05.cp before the
 // stage's MMAs; the TMEM columns after the accumulators hold 4 columns per block.
-template <int BN, bool kFp8, bool kCta2, int kKAtoms, int kBlk = 0>
+//
+// kGrouped: the launch runs a grouped GEMM (see next_unit): every role reads
+// the sizes, tensor maps and epilogue pointers of each unit from its
+// problem's parameter block.
+template <int BN, bool kFp8, bool kCta2, int kKAtoms, int kBlk = 0, bool kGrouped = false>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const __grid_constant__ KernelParams p) {
     constexpr int kElemBytes = kFp8 ? 1 : 2;
     constexpr int kBK = kRowBytes / kElemBytes;       // K elements per 128-byte atom
@@ -606,6 +652,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
     constexpr bool kMx = kBlk != 0;
+    static_assert(!(kMx && kGrouped), "grouped GEMMs take unscaled or per-tensor-scaled operands");
     static_assert(!kMx || (kFp8 && (kCta2 ? (BN == 256 || BN == 192) : BN == 128)),
                   "block-scaled tiles are 8-bit 128 x 128 (one CTA) or 256 x 256 / 256 x 192 (a pair)");
     constexpr int kSfBlock = 512;                          // 128 rows x 4 scales
@@ -679,10 +726,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         // ------------------------------------------------------ TMA producer
         {
             const bool issuer = lane == 0;
-            if (issuer && p.num_kb > 0) {
+            if (!kGrouped && issuer && p.num_kb > 0) {
                 ptx::prefetch_tensormap(&p.tmA);
                 ptx::prefetch_tensormap(&p.tmB);
             }
+            int cur_g = -1;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
@@ -691,7 +739,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             bool ok = true;
             WorkIter wi = work_begin(p, first_unit, unit_stride);
             Unit w;
-            while (ok && work_next(p, wi, w)) {
+            while (ok && next_unit<kGrouped>(p, wi, w)) {
+                const KernelParams& q = unit_params<kGrouped>(p, w);
+                if (kGrouped && w.g != cur_g) {
+                    if (issuer) {
+                        ptx::fence_tensormap_acquire(&q.tmA);
+                        ptx::fence_tensormap_acquire(&q.tmB);
+                    }
+                    cur_g = w.g;
+                }
                 const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1;
                 const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
                 const int b_row = n_blk * BN + static_cast<int>(rank) * kBRows;
@@ -717,20 +773,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         if (!p.a_mn_major) {
 #pragma unroll
                             for (int at = 0; at < kKAtoms; ++at)
-                                load(sA + at * kBM * kRowBytes, &p.tmA, k0 + at * kBK, a_row);
+                                load(sA + at * kBM * kRowBytes, &q.tmA, k0 + at * kBK, a_row);
                         } else {
 #pragma unroll
                             for (int h = 0; h < kBM / kAtom; ++h)
-                                load(sA + h * kRowBytes * kStageK, &p.tmA, a_row + h * kAtom, k0);
+                                load(sA + h * kRowBytes * kStageK, &q.tmA, a_row + h * kAtom, k0);
                         }
                         if (!p.b_mn_major) {
 #pragma unroll
                             for (int at = 0; at < kKAtoms; ++at)
-                                load(sB + at * kBRows * kRowBytes, &p.tmB, k0 + at * kBK, b_row);
+                                load(sB + at * kBRows * kRowBytes, &q.tmB, k0 + at * kBK, b_row);
                         } else {
 #pragma unroll
                             for (int h = 0; h < kBRows / kAtom; ++h)
-                                load(sB + h * kRowBytes * kStageK, &p.tmB, b_row + h * kAtom, k0);
+                                load(sB + h * kRowBytes * kStageK, &q.tmB, b_row + h * kAtom, k0);
                         }
                         if constexpr (kMx && kCta2) {
                             // scale blocks of this stage's atoms, per atom: kSfA blocks of
@@ -830,7 +886,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const long long st_t0 = p.stats ? clock64() : 0;
             WorkIter wi = work_begin(p, first_unit, unit_stride);
             Unit w;
-            for (; ok && work_next(p, wi, w); ++t) {
+            for (; ok && next_unit<kGrouped>(p, wi, w); ++t) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
                 const int acc = kAccBufs == 2 ? (t & 1) : 0;
                 const uint32_t acc_phase = kAccBufs == 2 ? ((t >> 1) & 1) : (t & 1);
@@ -977,6 +1033,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         const bool has_c = p.beta != 0.0f;
         const bool c_tma = has_c && p.c_tma;
         long long st_ewait = 0, st_ebusy = 0;
+        const CUtensorMap* tm_c = &p.tmC;   // the current unit's C map
+        int cur_g = -1;
         // Request C chunk x (columns col0, this warp's 32 rows at row0) into
         // buffer x mod nbuf, once the D store that last used it has read it
         // (n_wait = stores issued after that one).  Whole warp, converged.
@@ -987,7 +1045,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 bulk_wait_read_at_most(mixed ? 0 : n_wait);
                 uint64_t* bar = &cbar[x & (nbuf - 1)];
                 ptx::mbar_arrive_expect_tx(bar, c_box_bytes);
-                ptx::tma_load_2d(ring + (x & (nbuf - 1)) * buf_bytes, &p.tmC, bar, col0, row0);
+                ptx::tma_load_2d(ring + (x & (nbuf - 1)) * buf_bytes, tm_c, bar, col0, row0);
             }
             ++c_pending;
         };
@@ -1001,7 +1059,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
         int t = 0;
         WorkIter wi = work_begin(p, first_unit, unit_stride);
         Unit w;
-        for (; work_next(p, wi, w); ++t) {
+        for (; next_unit<kGrouped>(p, wi, w); ++t) {
+            const KernelParams& q = unit_params<kGrouped>(p, w);
+            if (kGrouped && w.g != cur_g) {
+                tm_c = &q.tmC;
+                if (lane == 0) {
+                    if (c_tma) ptx::fence_tensormap_acquire(&q.tmC);
+                    if (q.d_tma) ptx::fence_tensormap_acquire(&q.tmD);
+                }
+                cur_g = w.g;
+            }
             const int m_blk = w.m_blk, n_blk = w.n_blk, kb0 = w.kb0, kb1 = w.kb1, split = w.split;
             const bool split_mode = w.nsplit > 1;
             constexpr int kRanks = kCta2 ? 2 : 1;
@@ -1011,18 +1078,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM;
             const int n0 = n_blk * BN;
             const int grow = m0 + row_in_tile;
-            const bool row_ok = grow < p.M;
-            const bool warp_rows_live = (m0 + g * 32) < p.M;
-            const int nchunks = min(BN / kEpiChunk, (p.N - n0 + kEpiChunk - 1) / kEpiChunk);
+            const bool row_ok = grow < q.M;
+            const bool warp_rows_live = (m0 + g * 32) < q.M;
+            const int nchunks = min(BN / kEpiChunk, (q.N - n0 + kEpiChunk - 1) / kEpiChunk);
             uint4 cq[9];
             if (has_c) {
                 // C rows of this tile on the first pass, then always of the next tile, into L2
-                if (t == 0) c_prefetch_l2(p, grow, n0, BN);
+                if (t == 0) c_prefetch_l2(q, grow, n0, BN);
                 WorkIter peek = wi;
                 Unit nw;
-                if (work_next(p, peek, nw))
-                    c_prefetch_l2(p, nw.m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile, nw.n_blk * BN, BN);
-                if (!c_tma && row_ok && !split_mode) c_prefetch(p, grow, n0, cq);
+                if (next_unit<kGrouped>(p, peek, nw))
+                    c_prefetch_l2(unit_params<kGrouped>(p, nw), nw.m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile, nw.n_blk * BN, BN);
+                if (!c_tma && row_ok && !split_mode) c_prefetch(q, grow, n0, cq);
             }
             // First C boxes of a tile that is not split, before the accumulator is ready.
             if (c_tma && !split_mode && warp_rows_live)
@@ -1082,7 +1149,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             // are dealt round-robin to the four epilogue warps, which then
             // sum and store in parallel.
             const int wq = warp - kEpiWarp0;
-            const int live_groups = max(0, min(4, (p.M - m0 + 31) / 32));
+            const int live_groups = max(0, min(4, (q.M - m0 + 31) / 32));
             auto item_of = [&](int k, int& rg, int& jj) -> bool {
                 if (!finish) return false;
                 if (!split_mode) {
@@ -1099,7 +1166,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             };
             if (has_c && !c_tma && split_mode) {
                 int rg, jj;
-                if (item_of(0, rg, jj) && m0 + rg * 32 + lane < p.M) c_prefetch(p, m0 + rg * 32 + lane, n0 + jj * kEpiChunk, cq);
+                if (item_of(0, rg, jj) && m0 + rg * 32 + lane < q.M) c_prefetch(q, m0 + rg * 32 + lane, n0 + jj * kEpiChunk, cq);
             }
             if (c_tma && split_mode)
                 for (int l = 0; l < lookahead; ++l) {
@@ -1113,7 +1180,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     if (!item_of(k, rg, j)) break;
                     const int col0 = n0 + j * kEpiChunk;
                     const int grow = m0 + rg * 32 + lane;
-                    const bool row_ok = grow < p.M;
+                    const bool row_ok = grow < q.M;
                     float v[32];
                     if (!split_mode) {
                         uint32_t r[32];
@@ -1154,16 +1221,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     for (int i = 0; i < 16; ++i) v2[i] = ptx::pack2(v[2 * i], v[2 * i + 1]);
                     {
                         // alpha * sA * sB, and the per-row / per-column scales
-                        float rs = p.alpha;
-                        if (p.row_scale && row_ok) rs *= p.row_scale[grow];
+                        float rs = q.alpha;
+                        if (q.row_scale && row_ok) rs *= q.row_scale[grow];
                         if (rs != 1.0f) {
                             const uint64_t al = ptx::pack2(rs, rs);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], al);
                         }
-                        if (p.col_scale) {
+                        if (q.col_scale) {
                             float cs[32];
-                            load_row32(p.col_scale, 1, col0, p.N, cs, p.cs_vec != 0);
+                            load_row32(q.col_scale, 1, col0, q.N, cs, q.cs_vec != 0);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) v2[i] = ptx::mul2(v2[i], ptx::pack2(cs[2 * i], cs[2 * i + 1]));
                         }
@@ -1175,10 +1242,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             wait_c(cc, false);
                             c_row_from_smem(buf, lane, p.c_f32, c);
                         } else if (row_ok) {
-                            c_values(p, grow, col0, cq, c);
+                            c_values(q, grow, col0, cq, c);
                             int rg2, j2;
-                            if (item_of(k + 1, rg2, j2) && m0 + rg2 * 32 + lane < p.M)
-                                c_prefetch(p, m0 + rg2 * 32 + lane, n0 + j2 * kEpiChunk, cq);
+                            if (item_of(k + 1, rg2, j2) && m0 + rg2 * 32 + lane < q.M)
+                                c_prefetch(q, m0 + rg2 * 32 + lane, n0 + j2 * kEpiChunk, cq);
                         }
                         if (c_tma || row_ok) {
                             const uint64_t be = ptx::pack2(p.beta, p.beta);
@@ -1186,9 +1253,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int i = 0; i < 16; ++i) v2[i] = ptx::fma2(be, ptx::pack2(c[2 * i], c[2 * i + 1]), v2[i]);
                         }
                     }
-                    if (p.bias) {
+                    if (q.bias) {
                         float b[32];
-                        load_row32(p.bias, p.bias_f32, col0, p.N, b, p.bias_vec != 0);
+                        load_row32(q.bias, q.bias_f32, col0, q.N, b, q.bias_vec != 0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v2[i] = ptx::add2(v2[i], ptx::pack2(b[2 * i], b[2 * i + 1]));
                     }
@@ -1208,16 +1275,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     if (!c_tma && lane == 0) bulk_wait_read_at_most(mixed ? 0 : nbuf - 1);
                     __syncwarp();
                     stage_row(buf, lane, p.d_f32, v);
-                    if (p.d_tma && (col0 + kEpiChunk <= p.N || p.d_inner_aligned)) {
+                    if (q.d_tma && (col0 + kEpiChunk <= q.N || q.d_inner_aligned)) {
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmD, buf, col0, m0 + rg * 32);
+                            ptx::tma_store_2d(&q.tmD, buf, col0, m0 + rg * 32);
                             ptx::bulk_commit_group();
                         }
                     } else {
                         __syncwarp();
-                        store_chunk_direct(p, buf, m0 + rg * 32, col0, lane);
+                        store_chunk_direct(q, buf, m0 + rg * 32, col0, lane);
                         __syncwarp();
                         mixed = true;
                     }

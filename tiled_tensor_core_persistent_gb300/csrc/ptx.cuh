@@ -108,6 +108,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// A tensor map that lives in global memory (written by an earlier copy, not a
+// kernel parameter): make the generic-proxy writes of its 128 bytes visible to
+// the tensor-map proxy before this thread's bulk tensor copies use it.
+__device__ __forceinline__ void fence_tensormap_acquire(const CUtensorMap* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on
 // `bar`.  (x, y) = coordinates of the box's first element (x innermost).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,

@@ -20,9 +20,11 @@
 #include <mutex>
 #include <tuple>
 #include <string>
+#include <vector>
 
 #include "../../include/tcgemm.h"
 #include "gemm_kernel.cuh"
+#include "launch.cuh"
 #include "pack_kernel.cuh"
 
 namespace {
@@ -419,23 +421,57 @@ size_t counter_bytes(const Plan& pl) {
     return (static_cast<size_t>(pl.num_m) * pl.num_n * pl.cluster * sizeof(int) + 255) / 256 * 256;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA, int kMx = 0>
-cudaError_t set_smem_attr() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        if (err == cudaSuccess && kCta2)
-            err = cudaFuncSetAttribute(tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>,
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    });
-    return err;
+// Plan of a grouped GEMM: one tile shape for every problem, 256 x 256 pair
+// tiles when the problems' pair tiles fill the device at least once, else
+// 128 x 256 tiles on single CTAs; no split K.  `tiles` receives each
+// problem's tile count.
+Plan make_grouped_plan(const std::vector<tcg_problem>& probs, tcg_dtype ab, const DeviceInfo& dev,
+                       std::vector<int>* tiles) {
+    Plan pl;
+    pl.bn = 256;
+    long long pair_tiles = 0;
+    for (const tcg_problem& q : probs)
+        pair_tiles += static_cast<long long>((q.M + 255) / 256) * ((q.N + pl.bn - 1) / pl.bn);
+    bool cta2 = pair_tiles * 2 >= dev.num_sms;
+    if (g_force_cta2 == 1) cta2 = true;
+    if (g_force_cta2 == 2) cta2 = false;
+    pl.cluster = cta2 ? 2 : 1;
+    pl.katoms = cta2 ? 2 : 1;
+    pl.group_m = g_env_group_m > 0 ? g_env_group_m : (cta2 ? 8 : 16);
+    int stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(pl.bn, cta2, pl.katoms);
+    stages = std::max(2, std::min(stages, 8));
+    if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
+    pl.stages = stages;
+    pl.smem = fixed_smem_bytes() + stages * stage_bytes(pl.bn, cta2, pl.katoms);
+    const int tile_m = cta2 ? 2 * tcg::kBM : tcg::kBM;
+    long long units = 0;
+    if (tiles) tiles->clear();
+    for (const tcg_problem& q : probs) {
+        const long long t = static_cast<long long>((q.M + tile_m - 1) / tile_m) * ((q.N + pl.bn - 1) / pl.bn);
+        if (tiles) tiles->push_back(static_cast<int>(t));
+        units += t;
+    }
+    pl.num_kb = 0;
+    pl.splits = 1;
+    pl.units = pl.units_a = static_cast<int>(std::min<long long>(units, 1LL << 30));
+    int slots = dev.num_sms;
+    if (cta2) {
+        slots = max_active_pairs(pl.bn, is_fp8(ab), pl.katoms, pl.smem);
+        if (slots <= 0) slots = dev.num_sms / 2;
+    }
+    pl.workers = std::max(1, std::min(pl.units, slots));
+    pl.grid = (cta2 ? 2 : 1) * pl.workers;
+    return pl;
+}
+
+size_t grouped_table_bytes(int n) {
+    return (static_cast<size_t>(n) * sizeof(tcg::KernelParams) + static_cast<size_t>(n + 1) * sizeof(int) + 255) /
+           256 * 256;
 }
 
 template <int BN, bool kFp8, int KA>
 int active_pairs_for(int smem) {
-    if (set_smem_attr<BN, kFp8, true, KA>() != cudaSuccess) return 0;
+    if (tcg::set_smem_attr<BN, kFp8, true, KA>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr[1];
@@ -476,28 +512,13 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     return n;
 }
 
-template <int BN, bool kFp8, bool kCta2, int KA, int kMx = 0>
+tcg::LaunchShape launch_shape(const Plan& pl) { return tcg::LaunchShape{pl.grid, pl.smem, pl.cluster}; }
+
+template <int BN, bool kFp8, bool kCta2, int KA>
 tcg_status launch_kernel(const tcg::KernelParams& kp, const Plan& pl, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA, kMx>();
-    if (e != cudaSuccess) return fail_launch("cudaFuncSetAttribute", e);
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(pl.grid, 1, 1);
-    cfg.blockDim = dim3(tcg::kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = stream;
-    if (kCta2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    e = cudaLaunchKernelEx(&cfg, tcg::gemm_persistent_kernel<BN, kFp8, kCta2, KA, kMx>, kp);
-    if (e != cudaSuccess) return fail_launch("cudaLaunchKernelEx", e);
-    return TCG_OK;
+    const char* what = "launch";
+    const cudaError_t e = tcg::launch_instance<BN, kFp8, kCta2, KA>(kp, launch_shape(pl), stream, &what);
+    return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
 }
 
 }  // namespace
@@ -768,23 +789,11 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = is_fp8(ab_dtype);
-    if (is_mx(ab_dtype) && pl.cluster == 2) {
-        if (ab_dtype == TCG_NVFP4)
-            return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 2>(kp, pl, stream)
-                                  : launch_kernel<256, true, true, 1, 2>(kp, pl, stream);
-        if (ab_dtype == TCG_MXFP4 && pl.bn == 192) return launch_kernel<192, true, true, 2, 3>(kp, pl, stream);
-        if (ab_dtype == TCG_MXFP4)
-            return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 3>(kp, pl, stream)
-                                  : launch_kernel<256, true, true, 1, 3>(kp, pl, stream);
-        if (pl.bn == 192) return launch_kernel<192, true, true, 2, 1>(kp, pl, stream);
-        return pl.katoms == 2 ? launch_kernel<256, true, true, 2, 1>(kp, pl, stream)
-                              : launch_kernel<256, true, true, 1, 1>(kp, pl, stream);
-    }
-    if (ab_dtype == TCG_NVFP4) return launch_kernel<128, true, false, 1, 2>(kp, pl, stream);
-    if (ab_dtype == TCG_MXFP4) return launch_kernel<128, true, false, 1, 3>(kp, pl, stream);
     if (is_mx(ab_dtype)) {
-        return pl.katoms == 2 ? launch_kernel<128, true, false, 2, 1>(kp, pl, stream)
-                              : launch_kernel<128, true, false, 1, 1>(kp, pl, stream);
+        const int blk = ab_dtype == TCG_NVFP4 ? 2 : (ab_dtype == TCG_MXFP4 ? 3 : 1);
+        const char* what = "launch";
+        const cudaError_t e = tcg::launch_block_scaled(kp, launch_shape(pl), pl.bn, pl.katoms, blk, stream, &what);
+        return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
     }
     if (pl.cluster == 2 && pl.katoms == 2)
         return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)
@@ -937,4 +946,178 @@ extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const v
     if (e != cudaSuccess) return fail_launch("cudaMemsetAsync(scratch)", e);
     return tcg_gemm(M, N, K, alpha, A, lda, opA, B, ldb, opB, beta, C, ldc, c_dtype, D, ldd, d_dtype, epi, ab_dtype,
                     scales, scratch, kNoAllocScratchBytes, stream_);
+}
+
+// =================================================================== grouped GEMM
+
+namespace {
+
+// The problems that produce output (M > 0 and N > 0), validated.
+tcg_status grouped_validate(int G, const tcg_problem* problems, tcg_layout opA, tcg_layout opB, float beta,
+                            tcg_dtype c_dtype, tcg_dtype d_dtype, tcg_epilogue epi, tcg_dtype ab_dtype,
+                            std::vector<tcg_problem>* live) {
+    if (G < 0 || (G > 0 && !problems)) return TCG_ERR_INVALID_ARG;
+    if (is_mx(ab_dtype)) return TCG_ERR_UNSUPPORTED;
+    const int has_c = beta != 0.0f;
+    const int eb = elem_bytes(ab_dtype);
+    live->clear();
+    for (int g = 0; g < G; ++g) {
+        const tcg_problem& q = problems[g];
+        tcg_epilogue e = epi;
+        e.bias = q.bias;
+        tcg_status st = tcg_can_implement(q.M, q.N, q.K, ab_dtype, q.A, q.lda, opA, q.B, q.ldb, opB, has_c, q.C,
+                                          q.ldc, c_dtype, q.D, q.ldd, d_dtype, e);
+        if (st != TCG_OK) return st;
+        if (q.M == 0 || q.N == 0) continue;
+        if (q.K > 0 && (!tma_addressable(q.A, q.lda, eb) || !tma_addressable(q.B, q.ldb, eb)))
+            return TCG_ERR_UNSUPPORTED;
+        live->push_back(q);
+    }
+    return TCG_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tcg_grouped_workspace_size(int num_problems) {
+    if (num_problems < 0) return 0;
+    return kHeaderBytes + grouped_table_bytes(num_problems);
+}
+
+extern "C" tcg_status tcg_grouped_plan(int num_problems, const tcg_problem* problems, tcg_dtype ab_dtype,
+                                       int out[10]) {
+    if (!out || num_problems < 0 || (num_problems > 0 && !problems) || !is_ab_type(ab_dtype))
+        return TCG_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    tcg_status st = device_info(dev);
+    if (st != TCG_OK) return st;
+    std::vector<tcg_problem> live;
+    for (int g = 0; g < num_problems; ++g)
+        if (problems[g].M > 0 && problems[g].N > 0) live.push_back(problems[g]);
+    const Plan pl = make_grouped_plan(live, ab_dtype, dev, nullptr);
+    const int vals[10] = {tcg::kBM, pl.bn, pl.katoms * tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
+                          pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem};
+    memcpy(out, vals, sizeof vals);
+    return TCG_OK;
+}
+
+extern "C" tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* problems, tcg_layout opA,
+                                       tcg_layout opB, float beta, tcg_dtype c_dtype, tcg_dtype d_dtype,
+                                       tcg_epilogue epi, tcg_dtype ab_dtype, void* workspace, size_t workspace_bytes,
+                                       void* stream_) {
+    std::vector<tcg_problem> live;
+    tcg_status st = grouped_validate(num_problems, problems, opA, opB, beta, c_dtype, d_dtype, epi, ab_dtype, &live);
+    if (st != TCG_OK) return st;
+    if (live.empty()) return TCG_OK;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != TCG_OK) return st;
+    if (dev.major != 10 || dev.minor != 3) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "compute capability %d.%d is not 10.3 (sm_103a)", dev.major, dev.minor);
+        g_last_error = buf;
+        return TCG_ERR_ARCH;
+    }
+    const int n = static_cast<int>(live.size());
+    const size_t table = grouped_table_bytes(n);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < kHeaderBytes + table) return TCG_ERR_WORKSPACE;
+    std::vector<int> tiles;
+    const Plan pl = make_grouped_plan(live, ab_dtype, dev, &tiles);
+    long long total = 0;
+    for (int t : tiles) total += t;
+    if (total > (1LL << 30)) return TCG_ERR_UNSUPPORTED;
+
+    // Launch-wide parameters; each problem's block starts as a copy of them.
+    const int has_c = beta != 0.0f;
+    const int eb = elem_bytes(ab_dtype);
+    bool all_c_tma = has_c;
+    for (const tcg_problem& q : live) all_c_tma = all_c_tma && tma_addressable(q.C, q.ldc, elem_bytes(c_dtype));
+    tcg::KernelParams base;
+    memset(&base, 0, sizeof base);
+    base.splits = 1;
+    base.group_m = pl.group_m;
+    base.a_mn_major = (opA == TCG_COL);
+    base.b_mn_major = (opB == TCG_ROW);
+    base.beta = beta;
+    base.ab_fmt = mma_format(ab_dtype);
+    base.c_f32 = (c_dtype == TCG_F32);
+    base.c_tma = all_c_tma;
+    base.bias_f32 = (epi.bias_dtype == TCG_F32);
+    base.act = static_cast<int>(epi.act);
+    base.d_f32 = (d_dtype == TCG_F32);
+    base.stages = pl.stages;
+    base.epi_nbuf = tcg::epi_warp_bytes(false) / (32 * 32 * std::max(elem_bytes(d_dtype), all_c_tma ? elem_bytes(c_dtype) : 0));
+    char* ws = static_cast<char*>(workspace);
+    base.status = reinterpret_cast<int*>(ws);
+    base.timeout_ns = g_timeout_ns > 0 ? g_timeout_ns : kDefaultTimeoutNs;
+    base.fault_inject = g_fault_inject;
+    base.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
+
+    std::vector<tcg::KernelParams> blocks(n);
+    std::vector<int> tile0(n + 1, 0);
+    const int bk = tcg::kRowBytes / eb;
+    const int tile_m = pl.cluster == 2 ? 2 * tcg::kBM : tcg::kBM;
+    for (int g = 0; g < n; ++g) {
+        const tcg_problem& q = live[g];
+        tcg::KernelParams& kp = blocks[g];
+        kp = base;
+        if (q.K > 0) {
+            if (opA == TCG_ROW)
+                st = encode_2d(&kp.tmA, ab_dtype, q.A, q.K, q.M, q.lda, bk, tcg::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+            else
+                st = encode_2d(&kp.tmA, ab_dtype, q.A, q.M, q.K, q.lda, bk, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st != TCG_OK) return st;
+            const int b_rows = pl.cluster == 2 ? pl.bn / 2 : pl.bn;
+            if (opB == TCG_COL)
+                st = encode_2d(&kp.tmB, ab_dtype, q.B, q.K, q.N, q.ldb, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+            else
+                st = encode_2d(&kp.tmB, ab_dtype, q.B, q.N, q.K, q.ldb, bk, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (st != TCG_OK) return st;
+        }
+        kp.d_tma = tma_addressable(q.D, q.ldd, elem_bytes(d_dtype));
+        if (kp.d_tma) {
+            st = encode_2d(&kp.tmD, d_dtype, q.D, q.N, q.M, q.ldd, tcg::kEpiChunk, 32,
+                           d_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+            if (st != TCG_OK) return st;
+        }
+        if (all_c_tma) {
+            st = encode_2d(&kp.tmC, c_dtype, q.C, q.N, q.M, q.ldc, tcg::kEpiChunk, 32,
+                           c_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+            if (st != TCG_OK) return st;
+        }
+        kp.M = q.M;
+        kp.N = q.N;
+        kp.K = q.K;
+        kp.alpha = q.alpha;
+        kp.num_m_blk = (q.M + tile_m - 1) / tile_m;
+        kp.num_n_blk = (q.N + pl.bn - 1) / pl.bn;
+        kp.num_kb = (q.K + pl.katoms * bk - 1) / (pl.katoms * bk);
+        kp.num_units = kp.units_a = tiles[g];
+        kp.C = has_c ? q.C : nullptr;
+        kp.ldc = q.ldc;
+        kp.c_vec = has_c && tma_addressable(q.C, q.ldc, elem_bytes(c_dtype));
+        kp.bias = q.bias;
+        kp.bias_vec = q.bias && aligned16(q.bias);
+        kp.D = q.D;
+        kp.ldd = q.ldd;
+        kp.d_inner_aligned = (static_cast<long long>(q.N) * elem_bytes(d_dtype)) % 16 == 0;
+        tile0[g + 1] = tile0[g] + tiles[g];
+    }
+    // One table in the workspace after the status header: the problems'
+    // parameter blocks, then their first units.
+    std::vector<unsigned char> host(table, 0);
+    memcpy(host.data(), blocks.data(), static_cast<size_t>(n) * sizeof(tcg::KernelParams));
+    memcpy(host.data() + static_cast<size_t>(n) * sizeof(tcg::KernelParams), tile0.data(),
+           static_cast<size_t>(n + 1) * sizeof(int));
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaMemcpyAsync(ws + kHeaderBytes, host.data(), table, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail_launch("cudaMemcpyAsync(grouped table)", e);
+
+    tcg::KernelParams kp = base;
+    kp.num_units = kp.units_a = pl.units;
+    kp.group = reinterpret_cast<const tcg::KernelParams*>(ws + kHeaderBytes);
+    kp.group_tile0 = reinterpret_cast<const int*>(ws + kHeaderBytes + static_cast<size_t>(n) * sizeof(tcg::KernelParams));
+    kp.num_groups = n;
+    kp.M = kp.N = kp.K = 1;   // launch-wide sizes are unused; the problems carry their own
+    const char* what = "launch";
+    e = tcg::launch_grouped(kp, launch_shape(pl), is_fp8(ab_dtype), stream, &what);
+    return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
 }

@@ -8,8 +8,8 @@ from __future__ import annotations
 
 import torch
 
-from . import gemm, workspace_size_for, workspace_init
-from .inputs import GemmCase
+from . import gemm, gemm_grouped, grouped_workspace_size, workspace_size_for, workspace_init
+from .inputs import GemmCase, GroupedCase
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn}
 
@@ -25,7 +25,7 @@ class DeviceCase:
     SENTINEL = 1234.5
 
     def __init__(self, case: GemmCase, device="cuda", guard_rows: int = 0, stream=None,
-                 offsets: dict | None = None):
+                 offsets: dict | None = None, with_workspace: bool = True):
         """offsets: element offsets {"A", "B", "C", "D", "bias"} of each buffer's
         start from a 256-byte aligned allocation (to exercise unaligned pointers)."""
         self.case = case
@@ -57,9 +57,12 @@ class DeviceCase:
         self.D_full = self.D_flat[self.d_off:].view(rows, ld)
         self.sentinel_stored = float(torch.tensor(self.SENTINEL, dtype=ddt).float())
         self.D_view = self.D_full[guard_rows:guard_rows + case.M]
-        self.ws_bytes = max(workspace_size_for(case.M, case.N, case.K, self.ab_dtype, self.A, case.lda,
-                                               case.opA, self.B, case.ldb, case.opB), 256)
-        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws_bytes = 0
+        self.workspace = None
+        if with_workspace:
+            self.ws_bytes = max(workspace_size_for(case.M, case.N, case.K, self.ab_dtype, self.A, case.lda,
+                                                   case.opA, self.B, case.ldb, case.opB), 256)
+            self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
 
     def run(self, stream=None) -> None:
         c = self.case
@@ -83,6 +86,36 @@ class DeviceCase:
         mask[g:g + M, :N] = False
         head = self.D_flat[:self.d_off].to(torch.float32).cpu()
         return bool((full[mask] == self.sentinel_stored).all()) and bool((head == self.sentinel_stored).all())
+
+
+class GroupedDeviceCase:
+    """A GroupedCase uploaded to the device: each problem's buffers as in
+    DeviceCase (without a workspace of its own), and one grouped workspace."""
+
+    def __init__(self, case: GroupedCase, device="cuda", guard_rows: int = 0, stream=None):
+        self.case = case
+        self.stream = stream
+        self.parts = [DeviceCase(p, device, guard_rows=guard_rows, with_workspace=False) for p in case.problems]
+        self.ws_bytes = grouped_workspace_size(len(case.problems))
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=torch.device(device))
+        first = case.problems[0]
+        self.shared = dict(opA=first.opA, opB=first.opB, beta=first.beta, c_dtype=first.c_dtype,
+                           d_dtype=first.d_dtype, bias_dtype=first.bias_dtype, act=first.act,
+                           ab_dtype=first.ab_dtype)
+        for p in case.problems:
+            for k, v in self.shared.items():
+                if getattr(p, k) != v:
+                    raise ValueError(f"grouped problems must share {k}")
+        self.problems = [dict(M=p.M, N=p.N, K=p.K, alpha=p.alpha * p.scale_a * p.scale_b, A=d.A, lda=p.lda,
+                              B=d.B, ldb=p.ldb, C=d.C, ldc=p.ldc, D=d.D_view, ldd=p.ldd, bias=d.bias)
+                         for p, d in zip(case.problems, self.parts)]
+
+    def run(self, stream=None) -> None:
+        sh = self.shared
+        gemm_grouped(self.problems, sh["opA"], sh["opB"], sh["beta"], sh["c_dtype"], sh["d_dtype"],
+                     bias_dtype=sh["bias_dtype"], act=sh["act"], ab_dtype=sh["ab_dtype"],
+                     workspace=self.workspace, workspace_bytes=self.ws_bytes,
+                     stream=stream if stream is not None else self.stream)
 
 
 def _upload(t: torch.Tensor, dev, offset: int) -> torch.Tensor:

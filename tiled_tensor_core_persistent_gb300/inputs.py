@@ -371,3 +371,46 @@ def fp8_8192_relu() -> GemmCase:
     """8192^3 e4m3 (N(0,1) quantised with amax/448 per tensor), bias N(0,0.1), ReLU, bf16 D."""
     return make_case("gemm8192_e4m3_bias_relu", 8192, 8192, 8192, seed=17, dist="normal",
                      ab_dtype="e4m3", bias_std=0.1, act="relu")
+
+
+# ---------------------------------------------------------------- grouped GEMM
+
+@dataclass
+class GroupedCase:
+    """A grouped GEMM: independent problems that share the operand type, the
+    layouts, alpha, beta, the activation and the C / D / bias types; each has
+    its own sizes, A, B, C, bias and D."""
+    name: str
+    problems: list
+
+    @property
+    def flops(self) -> int:
+        return sum(p.flops for p in self.problems)
+
+
+def make_grouped_case(name, shapes, *, seed, **kw) -> GroupedCase:
+    """One make_case per (M, N, K) of `shapes`; problem g draws from seed * 1000 + g."""
+    return GroupedCase(name, [make_case(f"{name}[{g}]", M, N, K, seed=seed * 1000 + g, **kw)
+                              for g, (M, N, K) in enumerate(shapes)])
+
+
+def moe_token_counts(tokens: int, experts: int, seed: int) -> list:
+    """Rows routed to each expert: a seeded multinomial over Dirichlet(1) expert
+    probabilities, so the counts are irregular (some small, none guaranteed
+    to be a multiple of a tile)."""
+    rng = np.random.default_rng(seed)
+    return [int(c) for c in rng.multinomial(tokens, rng.dirichlet(np.ones(experts)))]
+
+
+def grouped_moe(experts: int = 16, tokens: int = 32768, N: int = 4096, K: int = 4096,
+                ab_dtype: str = "bf16") -> GroupedCase:
+    """A mixture-of-experts layer as a grouped GEMM: `tokens` rows of activations
+    routed over `experts` experts (moe_token_counts, seed 41), expert e an
+    (M_e x K) @ (K x N) GEMM with its own weights; A, B ~ N(0,1)/sqrt(K) (bf16)
+    or N(0,1) quantised per tensor (fp8), bias ~ N(0, 0.1), GELU, bf16 D,
+    A row-major, B column-major."""
+    counts = moe_token_counts(tokens, experts, seed=41)
+    dist = "normal_sqrtk" if ab_dtype in ("bf16", "f16") else "normal"
+    return make_grouped_case(f"grouped_moe{experts}_{tokens}x{N}x{K}_{ab_dtype}_bias_gelu",
+                             [(m, N, K) for m in counts], seed=41, dist=dist, ab_dtype=ab_dtype,
+                             bias_std=0.1, act="gelu")
