@@ -16,7 +16,8 @@ collective on the data path); the reported time is the max over ranks.
 samples of the same workload, reported in the same unit.
 
 --workload picks one of the other parity workloads (4096^3 beta*C, 512^3,
-the ragged and skinny shapes, 8192^3 e4m3); those whose inputs fit in L2 are
+the ragged and skinny shapes, 8192^3 e4m3 / MXFP8 / NVFP4, the 16-expert
+grouped MoE GEMM through tcg_gemm_grouped); those whose inputs fit in L2 are
 timed one launch per event pair with a 512 MiB L2 flush in between.  The
 roofline object is then against HBM bandwidth (GB/s) when the pages'
 intensity 2MNK / (b (MK + KN + MN)) puts the shape below the ridge point.
@@ -353,6 +354,24 @@ def timed_launches(args, dc, stream, device, flush):
     return sum(a.elapsed_time(b) for a, b in evs)
 
 
+def launch_distribution(dc, stream, device, n):
+    """Per-launch times (ms) of n launches, each between its own pair of events
+    on the launching stream, back to back (outside the timed region): the
+    median and the p10 / p90 spread of single launches."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            dc.run(stream)
+            b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    pick = lambda q: ms[min(n - 1, int(q * (n - 1) + 0.5))]
+    return {"median_ms": statistics.median(ms), "p10_ms": pick(0.1), "p90_ms": pick(0.9), "n": n,
+            "how": "one event pair per launch, launches back to back, after the timed region"}
+
+
 def run_ours(args):
     import torch
     world, rank, local, pg = dist_setup(args)
@@ -398,6 +417,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {st} after the timed region: {tcg.last_error()}")
 
     ms_per_step = elapsed_ms / args.steps
+    launches = launch_distribution(dc, stream, device, min(100, max(args.steps, 10))) if rank == 0 else None
     flops = case.flops
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     per_launch_tflops = flops / (ms_per_step * 1e-3) / 1e12
@@ -464,7 +484,7 @@ def run_ours(args):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": head(case).ab_dtype, "data": "synthetic",
                 "config": dict(workload_config(case, flush), plan=plan),
-                "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+                "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e, "launch_ms": launches,
                 "gpu_launches": args.steps}
         print(json.dumps(line), flush=True)
     if pg is not None:
