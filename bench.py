@@ -453,6 +453,8 @@ def run_ours(args):
                           f"{peak_kind} bf16 burst (cuBLAS 8192^3)" + (f" x {ratio:g} for the operand type" if ratio != 1 else "")),
             "peak_sustained": None if hbm_bound else
             peaks.get("bf16_tflops_sustained", 0) * ratio or None,
+            "frac_of_sustained": None if hbm_bound or not peaks.get("bf16_tflops_sustained") else
+            per_launch_tflops / (peaks["bf16_tflops_sustained"] * ratio),
             "tflops": per_launch_tflops, "gbs": gbs,
             "frac_of_nominal_tensor": per_launch_tflops / nominal,
             "algorithmic": "2*M*N*K flop per launch; bytes = A + B + D (+ C, bias) once",
