@@ -153,3 +153,28 @@ def test_config_grouped_moe_bf16():
         assert_within(got_rows, prob.select(rows, np.arange(p.N, dtype=np.int32)), TOL["bf16"], f"{p.name} rows")
         got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
         assert_within(got_cols, prob.select(np.arange(p.M, dtype=np.int32), cols), TOL["bf16"], f"{p.name} cols")
+
+
+def test_grouped_many_small_problems():
+    """200 problems of random small shapes (zeros included): the unit -> problem
+    search over many problems, and tiles of neighbouring problems on one CTA."""
+    rng = np.random.default_rng(95)
+    shapes = [(int(rng.integers(0, 300)), int(rng.integers(1, 300)), int(rng.integers(0, 200)))
+              for _ in range(200)]
+    # a few empty ones on purpose, first and last included
+    shapes[0] = (0, 64, 64)
+    shapes[57] = (50, 0, 64)
+    shapes[-1] = (0, 0, 0)
+    for tiles in ("pair", "single"):
+        tcg.debug_set(force_cta2=1 if tiles == "pair" else 2)
+        try:
+            gcase = exact_case(shapes, seed=96, act="relu", bias_std=None)
+            dc = run(gcase, guard_rows=1)
+        finally:
+            tcg.debug_set()
+        for g, (p, part) in enumerate(zip(gcase.problems, dc.parts)):
+            if p.M == 0 or p.N == 0:
+                assert part.untouched_outside(), f"empty problem {g} was written"
+                continue
+            assert np.array_equal(part.result().numpy(), oracle_for(p).full()), f"{tiles}: problem {g} {p.M}x{p.N}x{p.K}"
+            assert part.untouched_outside(), f"{tiles}: problem {g} wrote outside its D"
