@@ -68,13 +68,18 @@ def test_grouped_integer_exact(tiles, with_c):
         assert part.untouched_outside(), f"problem {g} wrote outside its D"
 
 
+@pytest.mark.parametrize("tiles", ["auto", "pair"])
 @pytest.mark.parametrize("combo", range(4))
-def test_grouped_layouts_bf16(combo):
+def test_grouped_layouts_bf16(combo, tiles):
     opA, opB = inputs.LAYOUT_COMBOS[combo]
     gcase = inputs.make_grouped_case("grouped_layouts", [(200, 136, 72), (33, 264, 520), (640, 512, 96)],
                                      seed=60 + combo, dist="uniform", opA=opA, opB=opB, beta=0.5,
                                      c_dist="uniform", bias_std=0.1, act="gelu")
-    dc = run(gcase)
+    tcg.debug_set(force_cta2=1 if tiles == "pair" else 0)
+    try:
+        dc = run(gcase)
+    finally:
+        tcg.debug_set()
     for p, part in zip(gcase.problems, dc.parts):
         assert_within(part.result().numpy(), oracle_for(p).full(), TOL["bf16"], p.name)
         assert part.untouched_outside()
@@ -178,3 +183,24 @@ def test_grouped_many_small_problems():
                 continue
             assert np.array_equal(part.result().numpy(), oracle_for(p).full()), f"{tiles}: problem {g} {p.M}x{p.N}x{p.K}"
             assert part.untouched_outside(), f"{tiles}: problem {g} wrote outside its D"
+
+
+def test_grouped_unaligned_c_d_and_bias_per_problem():
+    """C, D and bias that the TMA cannot address are taken element-wise, per
+    problem, next to problems whose C and D go through the TMA."""
+    mk = lambda name, M, N, K, seed, **kw: inputs.make_case(name, M, N, K, seed=seed, dist="int4", d_dtype="f32",
+                                                            beta=0.5, c_dist="int4", act="relu", **kw)
+    probs = [mk("aligned", 300, 256, 128, 1),
+             mk("odd_ldc", 130, 200, 64, 2, ldc=201),
+             mk("odd_ldd", 257, 96, 72, 3, ldd=97),
+             mk("both", 64, 40, 200, 4, ldc=41, ldd=43)]
+    gcase = inputs.GroupedCase("grouped_unaligned", probs)
+    for tiles in ("pair", "single"):
+        tcg.debug_set(force_cta2=1 if tiles == "pair" else 2)
+        try:
+            dc = run(gcase, guard_rows=1)
+        finally:
+            tcg.debug_set()
+        for p, part in zip(gcase.problems, dc.parts):
+            assert np.array_equal(part.result().numpy(), oracle_for(p).full()), f"{tiles}: {p.name}"
+            assert part.untouched_outside(), f"{tiles}: {p.name} wrote outside its D"
