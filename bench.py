@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
                     help="the metric's workload (default) or one of the parity workloads, "
@@ -423,7 +423,11 @@ def run_ours(args):
     per_launch_tflops = flops / (ms_per_step * 1e-3) / 1e12
 
     # end to end through the public API: pinned host inputs -> device, GEMM, D -> pinned host
-    e2e = run_e2e(args, case, dc, stream, device, tcg) if args.e2e_steps > 0 else None
+    if is_grouped(case):
+        make_dc = lambda: harness.GroupedDeviceCase(case, device=device, stream=stream)
+    else:
+        make_dc = lambda: harness.DeviceCase(case, device=device, stream=stream)
+    e2e = run_e2e(args, case, dc, stream, device, tcg, make_dc) if args.e2e_steps > 0 else None
 
     peaks, peak_kind = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
@@ -499,43 +503,89 @@ def inputs_blocked(sf):
     return inputs.mx_blocked_layout(sf)
 
 
-def run_e2e(args, case, dc, stream, device, tcg):
+def run_e2e(args, case, dc, stream, device, tcg, make_dc):
+    """End to end through the public API: every step copies its inputs from
+    pinned host memory to the device, runs the GEMM and copies D back to pinned
+    host memory.  Steps are pipelined as a serving loop would run them: two
+    device buffer sets, the host-to-device copies on one stream, the GEMMs on
+    the launching stream and the device-to-host copies on a third, so step
+    i + 1's inputs travel while step i computes; a buffer set is refilled only
+    after its previous result has been copied out."""
     import torch
-    # (pinned host tensor, device tensor) pairs copied in before and out after every step
-    ins, outs = [], []
-    for p, d in (zip(case.problems, dc.parts) if is_grouped(case) else [(case, dc)]):
-        ins += [(t.pin_memory(), dev) for t, dev in ((p.A, d.A), (p.B, d.B), (p.bias, d.bias), (p.C, d.C))
-                if t is not None]
-        ins += [(torch.from_numpy(inputs_blocked(x)).pin_memory(), dev)
-                for x, dev in ((p.sfa, d.sfa), (p.sfb, d.sfb)) if x is not None]
-        outs.append((torch.empty(d.D_view.shape, dtype=d.D_view.dtype).pin_memory(), d.D_view))
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
-    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+    sets = [dc, make_dc()]
+    # pinned host inputs (one copy, read by every step) and one pinned host D per set
+    host_in = []
+    for p in (case.problems if is_grouped(case) else [case]):
+        host_in.append([t.pin_memory() if t is not None else None for t in (p.A, p.B, p.bias, p.C)] +
+                       [torch.from_numpy(inputs_blocked(x)).pin_memory() if x is not None else None
+                        for x in (p.sfa, p.sfb)])
 
-    def step():
-        with torch.cuda.stream(stream):
-            for h, dev in ins:
-                dev.copy_(h, non_blocking=True)
-            dc.run(stream)
-            for h, dev in outs:
-                h.copy_(dev, non_blocking=True)
+    def pairs(d):
+        parts = d.parts if is_grouped(case) else [d]
+        ins, outs = [], []
+        for hs, part in zip(host_in, parts):
+            devs = [part.A, part.B, part.bias, part.C, part.sfa, part.sfb]
+            ins += [(h, dv) for h, dv in zip(hs, devs) if h is not None]
+            outs.append((torch.empty(part.D_view.shape, dtype=part.D_view.dtype).pin_memory(), part.D_view))
+        return ins, outs
 
-    for _ in range(2):
-        step()
+    io = [pairs(d) for d in sets]
+    h2d = sum(h.numel() * h.element_size() for h, _ in io[0][0])
+    d2h = sum(h.numel() * h.element_size() for h, _ in io[0][1])
+    # (one stream per direction: chunking the copies over 2, 4 or 8 streams was
+    # measured no faster on GB300: 1.49, 1.51, 1.54, 1.61 ms per 8192^3 step)
+    s_in = torch.cuda.Stream(device=device)
+    s_out = torch.cuda.Stream(device=device)
+
+    def copies(pairs, st, to_device):
+        with torch.cuda.stream(st):
+            for h, dv in pairs:
+                if to_device:
+                    dv.copy_(h, non_blocking=True)
+                else:
+                    h.copy_(dv, non_blocking=True)
+
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
+
+    def step(i):
+        k = i & 1
+        if started[k]:
+            s_in.wait_event(out_done[k])          # set k's previous result has left the device
+        started[k] = True
+        copies(io[k][0], s_in, True)
+        in_done[k].record(s_in)
+        stream.wait_event(in_done[k])
+        sets[k].run(stream)
+        comp_done[k].record(stream)
+        s_out.wait_event(comp_done[k])
+        copies(io[k][1], s_out, False)
+        out_done[k].record(s_out)
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize(device)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     n = max(1, args.e2e_steps)
-    ev0.record(stream)
-    for _ in range(n):
-        step()
-    ev1.record(stream)
+    ev0.record(s_in)
+    for i in range(n):
+        step(i)
+    s_out.wait_event(in_done[(n - 1) & 1])
+    s_out.wait_event(comp_done[(n - 1) & 1])
+    ev1.record(s_out)
     torch.cuda.synchronize(device)
     ms = ev0.elapsed_time(ev1) / n
+    for d in sets:
+        st = tcg.device_status(d.workspace, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the end-to-end loop: {tcg.last_error()}")
     return {"value": case.flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
             "path": "pinned host A, B, C, bias, block scales -> device (cudaMemcpyAsync), " +
-                    ("tcg_gemm_grouped" if is_grouped(case) else "tcg_gemm") + ", D -> pinned host"}
+                    ("tcg_gemm_grouped" if is_grouped(case) else "tcg_gemm") + ", D -> pinned host; "
+                    "steps pipelined over two device buffer sets (copies of step i+1 overlap the GEMM of step i)"}
 
 
 def main():
