@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--role-stats", action="store_true",
+                    help="instead of the bench line: per-CTA time of each role (the kernel's cycle "
+                         "accounting, TCG_STATS=1) over --steps launches of the workload")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD,
                     help="the metric's workload (default) or one of the parity workloads, "
                          "measured the same way for the per-workload roofline table")
@@ -588,10 +591,58 @@ def run_e2e(args, case, dc, stream, device, tcg, make_dc):
                     "steps pipelined over two device buffer sets (copies of step i+1 overlap the GEMM of step i)"}
 
 
+def run_role_stats(args):
+    """The kernel's cycle accounting (KernelParams::stats): summed over the CTAs
+    of --steps launches, reported per issuing CTA and launch in microseconds at
+    the SM clock sampled meanwhile.  The accounting slows the kernel a little,
+    so these runs give no bench value."""
+    os.environ["TCG_STATS"] = "1"           # read once, when the library loads
+    import torch
+    import tiled_tensor_core_persistent_gb300 as tcg
+    from tiled_tensor_core_persistent_gb300 import _build, harness, inputs
+    _build.build()
+    tcg.lib()
+    case = WORKLOADS[args.workload][0](inputs)
+    dc = (harness.GroupedDeviceCase if is_grouped(case) else harness.DeviceCase)(case, device="cuda:0")
+    for _ in range(max(args.warmup, 3)):
+        dc.run()
+    torch.cuda.synchronize()
+    dc.workspace[:256].zero_()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        dc.run()
+    ev1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st = dc.workspace[64:128].view(torch.int64).cpu().tolist()
+    mhz = clocks.get("sm_mhz") or 1900.0
+    if is_grouped(case):
+        plan = tcg.grouped_plan([dict(M=p.M, N=p.N, K=p.K) for p in case.problems], head(case).ab_dtype)
+    else:
+        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
+    issuers = max(st[6], 1)                 # MMA-issuing CTAs (pair leaders) summed over the launches
+    ctas = issuers * plan["cluster"]        # every CTA: producers and epilogues count in each
+    per = {"mma_wait_full": (st[0], issuers), "mma_wait_acc": (st[1], issuers), "mma_loop_total": (st[5], issuers),
+           "producer_wait_empty": (st[2], ctas), "epilogue_wait_acc": (st[3], ctas), "epilogue_busy": (st[4], ctas)}
+    print(json.dumps({"workload": args.workload, "launches": args.steps,
+                      "ms_per_launch": ev0.elapsed_time(ev1) / args.steps, "sm_mhz": mhz, "plan": plan,
+                      "us_per_cta_and_launch": {k: c / n / mhz for k, (c, n) in per.items()},
+                      "note": "mma_* from the MMA issuer (first wait to last commit for mma_loop_total), "
+                              "producer_* from the TMA producer, epilogue_* from the first epilogue warp of each "
+                              "CTA (busy = accumulator ready to hand-back)"}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.role_stats:
+        return run_role_stats(args)
     return run_ours(args)
 
 

@@ -86,7 +86,6 @@ struct KernelParams {
     int c_vec;            // C rows may be read with 16-byte vector loads
     int c_tma;            // C is read through tmC into the epilogue buffers
     int epi_nbuf;         // epilogue buffers per warp (2 or 4, 8 KiB in all)
-    int bias_vec;         // bias may be read with 16-byte vector loads
     int cs_vec;           // col_scale may be read with 16-byte vector loads
     int stages;
     float* partials;      // split-K partials: [slot * ranks + rank][BN][kBM] (row fastest), slot from partial_slot()
@@ -127,7 +126,7 @@ enum : int {
 };
 
 // Shared-memory bookkeeping that lives after the operand stages.
-struct alignas(8) SmemCtl {
+struct alignas(16) SmemCtl {
     uint64_t full[16];
     uint64_t empty[16];
     uint64_t tmem_full[2];
@@ -137,6 +136,7 @@ struct alignas(8) SmemCtl {
     uint32_t tmem_base;
     int abort_flag;
     int splitk_last;
+    alignas(16) float bias_tile[256];  // the current tile's bias (fp32), shared by the epilogue warps
 };
 
 __device__ __forceinline__ void record_timeout(const KernelParams& p, int where) {
@@ -1095,6 +1095,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
             if (c_tma && !split_mode && warp_rows_live)
                 for (int l = 0; l < lookahead && l < nchunks; ++l)
                     issue_c(cc + l, n0 + l * kEpiChunk, m0 + g * 32, nbuf - 1 - l);
+            // The tile's bias, read from global memory once per tile into shared
+            // memory while the accumulator is still being computed (per chunk,
+            // 32 broadcast global loads left their L2 latency exposed: 7 % of
+            // the block-scaled kernels).  Barrier 2: every epilogue warp has
+            // finished the previous tile's chunks before the values change;
+            // barrier 1 below makes them visible.
+            if (q.bias) {
+                ptx::named_barrier_sync(2, kEpiThreads);
+                for (int c = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32; c < BN; c += kEpiThreads) {
+                    const int col = n0 + c;
+                    float bv = 0.0f;
+                    if (col < q.N)
+                        bv = q.bias_f32 ? static_cast<const float*>(q.bias)[col]
+                                        : bf16_bits_to_float(static_cast<const uint16_t*>(q.bias)[col]);
+                    ctl->bias_tile[c] = bv;
+                }
+            }
             const long long te = p.stats ? clock64() : 0;
             bool ok = wait_phase(&ctl->tmem_full[acc], acc_phase, p, ctl, 4, limit);
             const long long te1 = p.stats ? clock64() : 0;
@@ -1254,10 +1271,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                         }
                     }
                     if (q.bias) {
-                        float b[32];
-                        load_row32(q.bias, q.bias_f32, col0, q.N, b, q.bias_vec != 0);
+                        // broadcast reads of the tile's bias (columns past N hold 0)
+                        const float4* bt = reinterpret_cast<const float4*>(ctl->bias_tile + j * kEpiChunk);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v2[i] = ptx::add2(v2[i], ptx::pack2(b[2 * i], b[2 * i + 1]));
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 b4 = bt[i];
+                            v2[2 * i] = ptx::add2(v2[2 * i], ptx::pack2(b4.x, b4.y));
+                            v2[2 * i + 1] = ptx::add2(v2[2 * i + 1], ptx::pack2(b4.z, b4.w));
+                        }
                     }
                     if (p.act == 2) {
 #pragma unroll

@@ -770,7 +770,6 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         const int box = 32 * 32 * std::max(elem_bytes(d_dtype), kp.c_tma ? elem_bytes(c_dtype) : 0);
         kp.epi_nbuf = tcg::epi_warp_bytes(is_mx(ab_dtype) && pl.cluster == 2 && pl.bn == 256) / box;
     }
-    kp.bias_vec = epi.bias && aligned16(epi.bias);
     kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
     kp.bias = epi.bias;
     kp.bias_f32 = (epi.bias_dtype == TCG_F32);
@@ -1095,7 +1094,6 @@ extern "C" tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* prob
         kp.ldc = q.ldc;
         kp.c_vec = has_c && tma_addressable(q.C, q.ldc, elem_bytes(c_dtype));
         kp.bias = q.bias;
-        kp.bias_vec = q.bias && aligned16(q.bias);
         kp.D = q.D;
         kp.ldd = q.ldd;
         kp.d_inner_aligned = (static_cast<long long>(q.N) * elem_bytes(d_dtype)) % 16 == 0;
