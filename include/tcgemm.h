@@ -215,7 +215,8 @@ tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);
  *   wait_timeout_ns: limit of every bounded device-side wait (0 = default 2 s).
  *   force_splits / force_cta2: override the planner (0 = automatic).
  *     force_cta2: 1 = 2-CTA pair tiles, 2 = one-CTA tiles; for the
- *     block-scaled types 3 / 4 = pair tiles 256 / 192 wide (NVFP4: 256).
+ *     block-scaled types 3 / 4 = pair tiles 256 / 192 wide (NVFP4: 256
+ *     always; the default width is 256).
  */
 void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2);
 

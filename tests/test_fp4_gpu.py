@@ -108,7 +108,7 @@ def test_config_nvfp4_8192_bias_relu():
                          ids=lambda s: "x".join(map(str, s)))
 def test_fp4_pair_tiles_exact(shape, width, fmt):
     """Pair tiles with scale blocks by TMA: NVFP4 always 256 x 256 with one
-    accumulator, MXFP4 256 x 192 (two accumulators) or 256 x 256."""
+    accumulator, MXFP4 256 x 256 (one accumulator) or 256 x 192 (two)."""
     M, N, K = shape
     if fmt == "nvfp4" and width == 192:
         pytest.skip("NVFP4 pair tiles are 256 wide")

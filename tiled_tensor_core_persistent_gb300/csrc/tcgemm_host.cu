@@ -295,9 +295,10 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
         // columns of a second one), or 256 x 192 with two accumulators, so
         // that one tile's epilogue overlaps the next tile's MMAs (not for
         // NVFP4, whose four scale blocks per atom leave no room).  Measured
-        // on 8192^3 (TFLOP/s, 256 wide vs 192 wide): MXFP8 2241 vs 2141,
-        // MXFP4 3019 vs 3300.
-        int pbn = ab == TCG_MXFP4 ? 192 : 256;
+        // on 8192^3 (TFLOP/s, 256 wide vs 192 wide): MXFP8 2393 vs 2151,
+        // MXFP4 3353 vs 3313 (with the epilogue's staged bias and direct
+        // stores; before them MXFP4 was 3019 vs 3300), so 256 by default.
+        int pbn = 256;
         if (g_env_mx_bn == 192 || g_env_mx_bn == 256) pbn = g_env_mx_bn;
         if (g_force_cta2 == 3) pbn = 256;
         if (g_force_cta2 == 4) pbn = 192;
