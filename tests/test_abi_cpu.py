@@ -161,3 +161,22 @@ def test_grouped_workspace_size(lib):
     assert all(s >= 256 and s % 256 == 0 for s in sizes)
     assert sizes == sorted(sizes) and sizes[-1] > sizes[1]
     assert tcg.grouped_workspace_size(-1) == 0
+
+
+def test_header_compiles_as_c99_and_links(lib, tmp_path):
+    """A plain C99 program includes tcgemm.h, links libtcgemm.so and runs the
+    validation and sizing entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    so = tcg.library_path()
+    exe = tmp_path / "abi_check"
+    src = os.path.join(ROOT, "tests", "c", "abi_check.c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), src,
+                        "-o", str(exe), so, f"-Wl,-rpath,{os.path.dirname(so)}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "abi_check ok" in r.stdout
