@@ -154,9 +154,11 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the GEMM's sources (every file under csrc/ except the test-only
+    debug_* kernels, which take no part in a GEMM)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_tensor_core_persistent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(n for n in os.listdir(csrc) if not n.startswith("debug_")):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -337,6 +337,19 @@ tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* problems,
  */
 tcg_status tcg_grouped_plan(int num_problems, const tcg_problem* problems, tcg_dtype ab_dtype, int out[10]);
 
+/*
+ * tcg_debug_tma_swizzle128 -- TEST-ONLY: one TMA load of a rows x 128-byte
+ * tile (row-major, 128-byte rows, device memory at src) into 1024-byte-aligned
+ * shared memory with 128-byte swizzling, copied back unchanged to dst (rows x
+ * 128 bytes), so that a test can compare the hardware's swizzled layout (the
+ * one the GEMM kernel's shared-memory descriptors assume) with a host model.
+ * rows in [1, 64]; src and dst 16-byte aligned device memory; status: a device
+ * int the kernel sets to TCG_ERR_TIMEOUT if the load does not land within 1 s
+ * (otherwise left as it is).  Queued on stream.  TCG_ERR_INVALID_ARG for bad
+ * arguments, TCG_ERR_MISALIGNED for unaligned pointers.
+ */
+tcg_status tcg_debug_tma_swizzle128(const void* src, int rows, void* dst, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

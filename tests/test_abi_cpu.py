@@ -21,7 +21,7 @@ def declared_functions():
     with open(os.path.join(ROOT, "include", "tcgemm.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tcg_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tcg_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_surface():

@@ -34,7 +34,8 @@ STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "T
 
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
             "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc",
-            "tcg_debug_schedule", "tcg_grouped_workspace_size", "tcg_gemm_grouped", "tcg_grouped_plan"]
+            "tcg_debug_schedule", "tcg_grouped_workspace_size", "tcg_gemm_grouped", "tcg_grouped_plan",
+            "tcg_debug_tma_swizzle128"]
 
 
 class TcgError(RuntimeError):
@@ -113,6 +114,8 @@ def lib() -> ctypes.CDLL:
         L.tcg_gemm_grouped.restype = i32
         L.tcg_grouped_plan.argtypes = [i32, ctypes.POINTER(Problem), i32, ctypes.POINTER(ctypes.c_int)]
         L.tcg_grouped_plan.restype = i32
+        L.tcg_debug_tma_swizzle128.argtypes = [P, i32, P, P, P]
+        L.tcg_debug_tma_swizzle128.restype = i32
         _lib = L
         return L
 
@@ -266,3 +269,10 @@ def grouped_plan(problems, ab_dtype="bf16") -> dict:
         raise TcgError(st, "tcg_grouped_plan", last_error())
     keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem"]
     return dict(zip(keys, list(out)))
+
+
+def debug_tma_swizzle128(src, rows, dst, status, stream=None) -> None:
+    """TEST-ONLY: one TMA load with 128-byte swizzling and back (tcg_debug_tma_swizzle128)."""
+    st = lib().tcg_debug_tma_swizzle128(_addr(src), int(rows), _addr(dst), _addr(status), _stream(stream))
+    if st != 0:
+        raise TcgError(st, "tcg_debug_tma_swizzle128", last_error())

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(OUT_DIR, "libtcgemm.so")
 GENCODE = "arch=compute_103a,code=sm_103a"
-UNITS = ("tcgemm_host", "launch_block_scaled", "launch_grouped")
+UNITS = ("tcgemm_host", "launch_block_scaled", "launch_grouped", "debug_tma")
 
 
 def _nvcc() -> str:
