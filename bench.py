@@ -143,6 +143,23 @@ def workload_config(case, flush):
             "parallelism": "replicas (one independent GEMM per GPU)"}
 
 
+def run_env(device_index=None):
+    """Versions and device of this run (recorded beside the numbers)."""
+    import platform
+    import torch
+    env = {"python": platform.python_version(), "torch": torch.__version__, "cuda": torch.version.cuda,
+           "host": platform.machine(), "host_cores": os.cpu_count()}
+    if device_index is not None and torch.cuda.is_available():
+        env["device"] = torch.cuda.get_device_name(device_index)
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(device_index), "--query-gpu=driver_version",
+                                  "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+            env["driver"] = out.stdout.strip() or None
+        except Exception:
+            env["driver"] = None
+    return env
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -324,7 +341,8 @@ def run_reference(args):
             "data": "synthetic", "config": workload_config(whole, WORKLOADS[args.workload][1]),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "env": run_env()}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -496,7 +514,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": head(case).ab_dtype, "data": "synthetic",
                 "config": dict(workload_config(case, flush), plan=plan),
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e, "launch_ms": launches,
-                "gpu_launches": args.steps}
+                "gpu_launches": args.steps, "env": run_env(local)}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
