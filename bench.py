@@ -143,6 +143,17 @@ def workload_config(case, flush):
             "parallelism": "replicas (one independent GEMM per GPU)"}
 
 
+def launches_per_step(case, dc, tcg):
+    """Kernel launches of one library call: the GEMM, plus the packing kernel
+    when A or B is not TMA-addressable (the slow path sizes a larger workspace
+    for the packed copies)."""
+    if is_grouped(case) or case.K == 0 or dc.ab_dtype in ("mxe4m3", "mxe5m2", "nvfp4", "mxfp4"):
+        return 1
+    packs = tcg.workspace_size_for(case.M, case.N, case.K, dc.ab_dtype, dc.A, case.lda, case.opA, dc.B, case.ldb,
+                                   case.opB) > tcg.workspace_size(case.M, case.N, case.K, dc.ab_dtype)
+    return 2 if packs else 1
+
+
 def run_env(device_index=None):
     """Versions and device of this run (recorded beside the numbers)."""
     import platform
@@ -514,7 +525,7 @@ def run_ours(args):
                 "scaling": "weak", "vs_baseline": None, "dtype": head(case).ab_dtype, "data": "synthetic",
                 "config": dict(workload_config(case, flush), plan=plan),
                 "roofline": roof, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e, "launch_ms": launches,
-                "gpu_launches": args.steps, "env": run_env(local)}
+                "gpu_launches": args.steps * launches_per_step(case, dc, tcg), "env": run_env(local)}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
