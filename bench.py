@@ -47,7 +47,7 @@ def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -154,12 +154,29 @@ def launches_per_step(case, dc, tcg):
     return 2 if packs else 1
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), for the oracle's timings."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform_processor()
+
+
+def platform_processor():
+    import platform
+    return platform.processor() or None
+
+
 def run_env(device_index=None):
     """Versions and device of this run (recorded beside the numbers)."""
     import platform
     import torch
     env = {"python": platform.python_version(), "torch": torch.__version__, "cuda": torch.version.cuda,
-           "host": platform.machine(), "host_cores": os.cpu_count()}
+           "host": platform.machine(), "host_cores": os.cpu_count(), "cpu_model": cpu_model()}
     if device_index is not None and torch.cuda.is_available():
         env["device"] = torch.cuda.get_device_name(device_index)
         try:
