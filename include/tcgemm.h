@@ -23,8 +23,8 @@
  *   caller, are device memory of the current CUDA device, and must stay
  *   valid until the work queued on `stream` has finished.  The library keeps
  *   only a process-wide cache of TMA descriptors and launch attributes.
- * - Alignment ("CUTLASS" page, Part II, "ignoring alignment": a misaligned
- *   tensor either falls back to a slow path or refuses to run).  Every
+ * - Alignment ("CUTLASS" page, Part II, on alignment: a tensor that breaks
+ *   the alignment rules is either taken by a slower path or rejected).  Every
  *   pointer must be aligned to its element size, else TCG_ERR_MISALIGNED.
  *   The fast path wants each matrix 16-byte aligned with ld * sizeof(element)
  *   a multiple of 16 bytes (the TMA rule).  Otherwise the call still runs:
@@ -66,8 +66,8 @@ typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
  * infinities).  MXE4M3 / MXE5M2 are block-scaled FP8 (the OCP Microscaling
  * formats MXFP8): E4M3 / E5M2 elements plus one E8M0 scale (2^(e - 127)) per
  * 32 consecutive K of each A row and each B column, passed in
- * tcg_scales.block_sfa / block_sfb ("CUTLASS" page, Part V: block-scaled
- * narrow formats, where a small group of elements shares a scale factor). */
+ * tcg_scales.block_sfa / block_sfb ("CUTLASS" page, Part V: narrow formats
+ * in which a few neighbouring elements share one scale). */
 typedef enum {
     TCG_BF16 = 0, TCG_E4M3 = 1, TCG_F32 = 2, TCG_F16 = 3, TCG_E5M2 = 4,
     TCG_MXE4M3 = 5, TCG_MXE5M2 = 6, TCG_NVFP4 = 7, TCG_MXFP4 = 8
@@ -263,10 +263,10 @@ tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha,
                             void* stream);
 
 /*
- * Grouped GEMM ("CUTLASS" page, Part V, numeric-types deep dive: a
- * mixture-of-experts layer becomes a grouped GEMM in which each expert is one
- * problem of a batch of differently shaped problems; Part III: grouped GEMMs
- * with irregular shapes).  One launch computes, for every problem g,
+ * Grouped GEMM ("CUTLASS" page, Part V, numeric-types deep dive: the experts
+ * of a mixture-of-experts layer run as one grouped GEMM, one problem per
+ * expert, the problems of different sizes; Part III: grouped GEMMs with
+ * irregular shapes).  One launch computes, for every problem g,
  *
  *     D_g = act( alpha_g * (A_g @ B_g) + beta * C_g + bias_g )
  *

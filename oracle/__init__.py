@@ -191,9 +191,9 @@ class Problem:
 def grouped(problems) -> list:
     """A grouped GEMM: a batch of independent problems of different shapes,
     each computed by the one-GEMM identity above with its own operands,
-    C, bias and output.  "CUTLASS" page, Part V (numeric-types deep dive): a
-    mixture-of-experts layer becomes a grouped GEMM in which each expert is
-    one problem of a batch of differently shaped problems; Part III: grouped
+    C, bias and output.  "CUTLASS" page, Part V (numeric-types deep dive):
+    the experts of a mixture-of-experts layer run as one grouped GEMM, one
+    problem per expert, the problems of different sizes; Part III: grouped
     GEMMs with irregular shapes.  Returns the full fp64 result of every
     problem, in order (an M == 0 or N == 0 problem gives an empty array)."""
     return [p.full() for p in problems]

@@ -25,8 +25,8 @@
  * (the per-channel dequantisation scale of the same Stage 5 paragraph).
  *
  * Block-scaled operands (same page, Part V "data types and quantization":
- * block-scaled narrow formats, where a small group of elements shares a scale
- * factor, modelled as paired data-and-scale operands): each run of `blk`
+ * narrow formats in which a few neighbouring elements share one scale, an
+ * operand handled together with its scales): each run of `blk`
  * consecutive k of row i of A shares the scale sa(i, k / blk), and likewise
  * for column j of B with sb(j, k / blk).  The operand values are then
  * sa(i, k/blk) * a(i,k) and sb(j, k/blk) * b(k,j), and the sum runs over those

@@ -1,8 +1,8 @@
 """GPU parity of the block-scaled four-bit formats against the oracle.
 
-"CUTLASS" (stanleyjacob.dev), Part V: the newest tensor cores push
-quantisation to block-scaled four-bit formats, where a small group of
-elements shares a scale factor.  NVFP4: FP4 E2M1 elements, one unsigned E4M3
+"CUTLASS" (stanleyjacob.dev), Part V: the latest tensor cores take
+quantisation down to four-bit formats whose neighbouring elements share one
+scale per small block.  NVFP4: FP4 E2M1 elements, one unsigned E4M3
 scale per 16 consecutive K; MXFP4: one E8M0 scale per 32 (tcgen05
 kind::mxf4nvf4 with 4 or 2 scales per MMA).  Element codes and scale codes
 drawn from small sets make every product and partial sum exact in fp32, so

@@ -1,9 +1,9 @@
 """GPU parity of the grouped GEMM against the oracle.
 
-"CUTLASS" (stanleyjacob.dev), Part V (numeric-types deep dive): a
-mixture-of-experts layer becomes a grouped GEMM, each expert one problem of a
-batch of differently shaped problems; Part III: grouped GEMMs with irregular
-shapes.  One tcg_gemm_grouped launch computes every problem; each must equal
+"CUTLASS" (stanleyjacob.dev), Part V (numeric-types deep dive): the experts
+of a mixture-of-experts layer run as one grouped GEMM, one problem per
+expert, the problems of different sizes; Part III: grouped GEMMs with
+irregular shapes.  One tcg_gemm_grouped launch computes every problem; each must equal
 the oracle's result for that problem alone (bit for bit on integer inputs
 with fp32 D), and nothing outside any problem's D may be written.
 """

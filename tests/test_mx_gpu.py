@@ -1,8 +1,8 @@
 """GPU parity of block-scaled FP8 operands (MXE4M3 / MXE5M2) against the oracle.
 
-"CUTLASS" (stanleyjacob.dev), Part V, data types: block-scaled narrow formats,
-where a small group of elements shares a scale factor, modelled as paired
-data-and-scale operands.  Here: E4M3 / E5M2 elements with one E8M0 scale per
+"CUTLASS" (stanleyjacob.dev), Part V, data types: narrow formats in which a
+few neighbouring elements share one scale, an operand handled together with
+its scales.  Here: E4M3 / E5M2 elements with one E8M0 scale per
 32 consecutive K of each A row and B column (the OCP Microscaling layout),
 computed with the tensor cores' block-scaled MMA (tcgen05 kind::mxf8f6f4).
 Integer elements with scales 2^-1..2^1 make every partial sum exact in fp32,

@@ -1,8 +1,8 @@
 """GPU parity of the slow path for matrices the TMA cannot address.
 
-"CUTLASS" (stanleyjacob.dev), Part II, "ignoring alignment": leading
-dimensions and pointers usually must be aligned to 8 or 16 elements, and a
-misaligned tensor either falls back to a slow path or refuses to run.  Here
+"CUTLASS" (stanleyjacob.dev), Part II, on alignment: pointers and leading
+dimensions are normally expected on 8- or 16-element boundaries, and a tensor
+that is not is either taken by a slower path or rejected.  Here
 A and B with an unaligned base or row pitch are packed into the workspace
 first, and C, D and bias with one are read and written element-wise by the
 epilogue.  Every result is compared with the oracle, which reads the same

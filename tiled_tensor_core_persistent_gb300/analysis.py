@@ -1,7 +1,7 @@
 """Analytic performance models used to size tiles and to report rooflines.
 
 * Arithmetic intensity of a GEMM boundary, ``2MNK / (b (MK + KN + MN))``: each
-  input loaded once, the output written once, no read of an existing output
+  input loaded once, the output written once, and the old output never read
   ("CuTe DSL and CUDA Tile", section "A tile is a plan for reuse").
 * The square fp16-in / fp32-out GEMM intensity ``2N^3 / (2*2N^2 + 4N^2) = N/4``
   ("A10 CuTe, CUTLASS & CuTile", section 5 Performance Analysis).
@@ -47,7 +47,7 @@ def ridge_point(peak_flops: float, bandwidth: float) -> float:
 
 
 def pipeline_time(n: int, load: float, compute: float) -> float:
-    """n independent tiles, one load engine and one compute engine, ideal overlap."""
+    """n independent tiles with a single loader and a single arithmetic unit that overlap perfectly."""
     if n <= 0:
         return 0.0
     return load + compute + (n - 1) * max(load, compute)

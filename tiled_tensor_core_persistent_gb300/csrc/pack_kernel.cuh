@@ -4,10 +4,10 @@
 // multiple of 16 bytes.  An operand stored with any other pointer or leading
 // dimension (e.g. a tight bf16 row of 3001 elements) is first copied, once per
 // call, into 16-byte pitched rows of the caller's workspace; the GEMM then
-// streams the copy with the TMA as usual.  This is the "falls back to a slow
-// path" branch of the alignment rule in "CUTLASS" (stanleyjacob.dev), Part II:
-// one extra read and write of the operand at HBM bandwidth instead of a
-// refusal.
+// streams the copy with the TMA as usual.  Of the two answers the alignment
+// rule of "CUTLASS" (stanleyjacob.dev), Part II allows an unaligned tensor (a
+// slower path, or a refusal), this is the slower path: one extra read and
+// write of the operand at HBM bandwidth.
 #pragma once
 
 #include <cstdint>
