@@ -43,7 +43,7 @@ def _max_worker(rank, world, port, out):
 
 def test_max_over_ranks_and_barrier_gloo():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_max_worker, args=(world, free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 20.0, 1: 20.0}
 
