@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     TCG_OK = 0,
     TCG_ERR_INVALID_ARG = 1,   /* negative size, NULL pointer that is needed, bad enum, ld too small */
-    TCG_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. MN-major e4m3) */
+    TCG_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (e.g. MN-major e4m3) */
     TCG_ERR_MISALIGNED = 3,    /* a pointer not aligned to its element size */
     TCG_ERR_ARCH = 4,          /* current device is not compute capability 10.3 */
     TCG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than tcg_workspace_size_for */

@@ -36,7 +36,7 @@
  * page names no format.  The four-bit elements are FP4 E2M1 (OCP MX), two per
  * byte, the even element of each pair in the low nibble.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - bias is indexed by the output column j and added before act;
  *   - GELU is the exact erf form 0.5*x*(1+erf(x/sqrt(2)));
  *   - ReLU is x > 0 ? x : 0;
