@@ -588,3 +588,42 @@ def test_grouped_empty_and_k_zero_problems():
     assert got[0].shape == (0, 4)
     assert np.array_equal(got[1], np.maximum(0.5 * bf16_values(c_bits) + bf16_values(bias_bits)[None, :], 0.0))
     assert np.array_equal(got[2], r2)
+
+
+def test_moe_routing_recipe():
+    """The grouped workload's routing: every row goes to exactly one expert, the
+    counts are irregular and reproducible from the seed."""
+    counts = inputs.moe_token_counts(32768, 16, seed=41)
+    assert len(counts) == 16 and sum(counts) == 32768 and min(counts) >= 0
+    assert counts == inputs.moe_token_counts(32768, 16, seed=41)
+    assert len(set(counts)) > 8 and any(c % 128 for c in counts)
+    assert counts != inputs.moe_token_counts(32768, 16, seed=42)
+
+
+def test_integer_problems_match_numpy_for_random_shapes_and_layouts():
+    """Property over random small shapes, layouts and padded leading dimensions:
+    with integer inputs the oracle equals numpy's float64 matmul exactly."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = hypothesis.strategies
+
+    @hypothesis.settings(max_examples=60, deadline=None)
+    @hypothesis.given(M=st.integers(1, 9), N=st.integers(1, 9), K=st.integers(1, 12),
+                      la=st.sampled_from(["row", "col"]), lb=st.sampled_from(["row", "col"]),
+                      pad=st.integers(0, 3), seed=st.integers(0, 2**31 - 1))
+    def check(M, N, K, la, lb, pad, seed):
+        rng = np.random.default_rng(seed)
+        a = rng.integers(-4, 5, (M, K)).astype(np.float64)
+        b = rng.integers(-4, 5, (K, N)).astype(np.float64)
+
+        def padded(x, layout):
+            st_, ld = store(x, layout)
+            out = np.zeros((st_.shape[0], ld + pad), dtype=np.float64)
+            out[:, :ld] = st_
+            return bf16_bits(out), ld + pad
+
+        A, lda = padded(a, la)
+        B, ldb = padded(b, lb)
+        got = oracle.Problem(M, N, K, A, lda, op(la), B, ldb, op(lb)).full()
+        assert np.array_equal(got, a @ b)
+
+    check()
