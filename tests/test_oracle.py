@@ -9,7 +9,6 @@ dropped term, a wrong sign or index, or a transposed operand in the oracle
 fails at least one of them.
 """
 import json
-import math
 import os
 from fractions import Fraction
 

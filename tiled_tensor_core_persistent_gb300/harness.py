@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import torch
 
-from . import gemm, gemm_grouped, grouped_workspace_size, workspace_size_for, workspace_init
+from . import gemm, gemm_grouped, grouped_workspace_size, workspace_size_for
 from .inputs import GemmCase, GroupedCase
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn}
