@@ -268,30 +268,52 @@ def test_planner_picks_pairs_for_large_square():
     assert pl["cluster"] == 2 and pl["grid"] % 2 == 0 and pl["stages"] * pl["BK"] >= 384
 
 
-# ------------------------------------- tail split (last wave split over K)
+# ------------------------------------- Stream-K (TCG_SK, read when the library loads)
 
-@pytest.mark.parametrize("force_cta2", [1, 2], ids=["pair", "one_cta"])
-def test_tail_split_integer_exact_and_deterministic(force_cta2):
-    # the tail split is opt-in (TCG_TAIL=1 in the environment of this process)
-    if os.environ.get("TCG_TAIL") != "1":
-        pytest.skip("tail split is enabled by TCG_TAIL=1 (read when the library loads)")
-    try:
-        tcg.debug_set(force_cta2=force_cta2)
-        M, N, K = 2048 + 17, 2560, 1024 + 40
-        pl = tcg.plan(M, N, K)
-        per = 256 if force_cta2 == 1 else 128
-        tiles = -(-M // per) * -(-N // 256)
-        if pl["units"] == tiles:
-            pytest.skip(f"planner did not split the tail on this device: {pl}")
-        case = inputs.make_case("tail", M, N, K, seed=191 + force_cta2, dist="int4", d_dtype="f32",
-                                opA="col", opB="col")
-        dc = check_full(case, exact=True)
-        first = dc.D_view.clone()
-        dc.run()
-        torch.cuda.synchronize()
-        assert torch.equal(first, dc.D_view)
-    finally:
-        tcg.debug_set()
+_STREAM_K_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {tests!r})
+import tiled_tensor_core_persistent_gb300 as tcg
+from tiled_tensor_core_persistent_gb300 import harness, inputs
+from parity import TOL, assert_within, oracle_for
+tcg.lib()
+M, N, K = 2048 + 17, 2560, 1024 + 40
+tiles = -(-M // 256) * -(-N // 256)
+pl = tcg.plan(M, N, K)
+assert pl["units"] < tiles, ("no Stream-K units planned", pl)
+case = inputs.make_case("sk", M, N, K, seed=191, dist="int4", d_dtype="f32", opA="col", opB="col")
+dc = harness.DeviceCase(case, guard_rows=2)
+dc.run(); torch.cuda.synchronize()
+assert tcg.device_status(dc.workspace) == 0
+first = dc.D_view.clone()
+assert np.array_equal(dc.result().numpy(), oracle_for(case).full()), "not exact"
+assert dc.untouched_outside()
+dc.run(); torch.cuda.synchronize()
+assert torch.equal(first, dc.D_view), "not deterministic"
+case2 = inputs.make_case("sk_epi", 4096, 4096, 1024, seed=202, dist="uniform", beta=0.5, c_dist="uniform",
+                         bias_std=0.1, act="gelu")
+dc2 = harness.DeviceCase(case2)
+dc2.run(); torch.cuda.synchronize()
+assert tcg.device_status(dc2.workspace) == 0
+assert_within(dc2.result().numpy(), oracle_for(case2).full(), TOL["bf16"], "stream-k epilogue")
+print("stream-k ok", pl)
+"""
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_stream_k_modes_exact_deterministic_and_epilogue(mode):
+    """Stream-K schedules (off by default): integer-exact and run-to-run
+    identical on a ragged shape with column-major A and B, and the full
+    epilogue within tolerance.  The mode is read when the library loads, so
+    each runs in a child process with TCG_SK set."""
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _STREAM_K_CHILD.format(tests=here)],
+                       env=dict(os.environ, TCG_SK=str(mode)), capture_output=True, text=True, timeout=900,
+                       cwd=os.path.dirname(here))
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "stream-k ok" in r.stdout
 
 
 def test_tail_split_epilogue_bf16():
