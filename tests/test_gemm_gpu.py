@@ -316,6 +316,43 @@ def test_stream_k_modes_exact_deterministic_and_epilogue(mode):
     assert "stream-k ok" in r.stdout
 
 
+_OVERRIDE_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {tests!r})
+import tiled_tensor_core_persistent_gb300 as tcg
+from tiled_tensor_core_persistent_gb300 import harness, inputs
+from parity import oracle_for
+tcg.lib()
+for M, N, K, force in ((2048 + 17, 2560, 1024 + 40, 1), (700, 900, 500, 2), (1000, 128, 300, 0)):
+    tcg.debug_set(force_cta2=force)
+    case = inputs.make_case("ovr", M, N, K, seed=M + N + K, dist="int4", d_dtype="f32", beta=0.5, c_dist="int4",
+                            act="relu")
+    dc = harness.DeviceCase(case, guard_rows=2)
+    dc.run(); torch.cuda.synchronize()
+    assert tcg.device_status(dc.workspace) == 0
+    assert np.array_equal(dc.result().numpy(), oracle_for(case).full()), (M, N, K, tcg.plan(M, N, K))
+    assert dc.untouched_outside()
+    tcg.debug_set()
+print("overrides ok")
+"""
+
+
+@pytest.mark.parametrize("env", [{"TCG_KATOMS": "1"}, {"TCG_KATOMS": "2"}, {"TCG_STAGES": "2"},
+                                 {"TCG_GROUP_M": "3"}, {"TCG_NARROW": "0"}],
+                         ids=lambda e: ",".join(f"{k}={v}" for k, v in e.items()))
+def test_planner_overrides_stay_exact(env):
+    """The planner's tuning overrides (read when the library loads) select
+    other pipeline shapes and rasters; every one must stay integer-exact in
+    pair and one-CTA tiles.  Each runs in a child process."""
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _OVERRIDE_CHILD.format(tests=here)], env=dict(os.environ, **env),
+                       capture_output=True, text=True, timeout=900, cwd=os.path.dirname(here))
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "overrides ok" in r.stdout
+
+
 def test_tail_split_epilogue_bf16():
     case = inputs.make_case("tail_epi", 2048, 2560 + 256, 1024, seed=201, dist="uniform", beta=0.5,
                             c_dist="uniform", bias_std=0.1, act="gelu")
