@@ -534,7 +534,7 @@ def run_ours(args):
     if is_grouped(case):
         plan = tcg.grouped_plan([dict(M=p.M, N=p.N, K=p.K) for p in case.problems], head(case).ab_dtype)
     else:
-        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
+        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype, case.opA, case.opB)
     if rank == 0:
         line = {"metric": metric_name(args.workload),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -671,7 +671,7 @@ def run_role_stats(args):
     if is_grouped(case):
         plan = tcg.grouped_plan([dict(M=p.M, N=p.N, K=p.K) for p in case.problems], head(case).ab_dtype)
     else:
-        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype)
+        plan = tcg.plan(case.M, case.N, case.K, dc.ab_dtype, case.opA, case.opB)
     issuers = max(st[6], 1)                 # MMA-issuing CTAs (pair leaders) summed over the launches
     ctas = issuers * plan["cluster"]        # every CTA: producers and epilogues count in each
     per = {"mma_wait_full": (st[0], issuers), "mma_wait_acc": (st[1], issuers), "mma_loop_total": (st[5], issuers),

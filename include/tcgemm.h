@@ -36,7 +36,8 @@
  *   anything is queued; device-side errors (a bounded wait that ran out) are
  *   recorded in the workspace status word and read by tcg_device_status.
  * - No CPU fallback and no library GEMM: every FLOP runs in this library's
- *   sm_103a kernels.  On any other GPU tcg_gemm returns TCG_ERR_ARCH.
+ *   sm_103a kernels.  On any other GPU tcg_can_implement, tcg_gemm and the
+ *   other GEMM entry points return TCG_ERR_ARCH.
  */
 #ifndef TCGEMM_H
 #define TCGEMM_H
@@ -116,8 +117,8 @@ typedef struct {
 } tcg_scales;
 
 /*
- * tcg_can_implement -- argument validation only (no GPU access, no launch).
- * TCG_OK also for unaligned leading dimensions (the slow path above).
+ * tcg_can_implement -- argument validation, then the architecture check; no
+ * launch.  TCG_OK also for unaligned leading dimensions (the slow path above).
  *   M, N, K        : problem size, >= 0.
  *   ab_dtype       : TCG_BF16, TCG_F16, TCG_E4M3, TCG_E5M2, TCG_MXE4M3 or
  *                    TCG_MXE5M2 (A and B share it).  The 8-bit types
@@ -131,7 +132,12 @@ typedef struct {
  *                    ldc >= N, c_dtype TCG_BF16 or TCG_F32.
  *   D, ldd, d_dtype: output, row-major, ldd >= N, TCG_BF16 or TCG_F32.
  *   epi            : bias pointer (aligned to its element) / dtype / activation.
- * Returns TCG_OK or the first failing rule's code.  M == 0 or N == 0 is OK.
+ * Returns TCG_OK or the first failing rule's code.  M == 0 or N == 0 is OK
+ * on any device.  When the process sees a CUDA device, a non-empty problem
+ * that passes every argument rule is then checked against the current
+ * device: TCG_ERR_ARCH unless it is compute capability 10.3 (the
+ * tcg_arch_status mapping; the device's attributes are read once and
+ * cached).  Without any CUDA device only the arguments are checked.
  */
 tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype,
                              const void* A, int lda, tcg_layout opA,
@@ -139,6 +145,16 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype,
                              int has_c, const void* C, int ldc, tcg_dtype c_dtype,
                              const void* D, int ldd, tcg_dtype d_dtype,
                              tcg_epilogue epi);
+
+/*
+ * tcg_arch_status -- the architecture rule on its own, for a device of
+ * compute capability major.minor: TCG_OK for 10.3 (the sm_103a kernels this
+ * library is built for), TCG_ERR_ARCH for anything else.  "A10 CuTe,
+ * CUTLASS & CuTile" (gahan9.github.io), the pitfalls table: check the
+ * architecture a kernel was compiled for before running it.  Pure function,
+ * no device access.
+ */
+tcg_status tcg_arch_status(int major, int minor);
 
 /*
  * tcg_workspace_size -- bytes of device workspace tcg_gemm needs for this
@@ -198,14 +214,17 @@ tcg_status tcg_device_status(void* workspace, void* stream);
 const char* tcg_last_error(void);
 
 /*
- * tcg_plan -- the launch plan tcg_gemm would use (for tests and tools).
+ * tcg_plan -- the launch plan tcg_gemm would use for these sizes, operand
+ * type and A / B layouts (for tests and tools).
  * out[0..9] = {BM, BN, BK, stages, splits, grid CTAs, cluster size,
  *              units of work, raster group, dynamic smem bytes}.
- * units of work > tiles x splits when the last tiles are split over K to
- * fill the last wave.
+ * BN of a pair tile may be 160, 192 or 224 instead of 256 when B is
+ * column-major (K-contiguous) and the narrower tile fills the last wave
+ * better.  units of work > tiles x splits when the last tiles are split
+ * over K to fill the last wave.
  * Needs the current device (queries SM count and shared-memory limit).
  */
-tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]);
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[10]);
 
 /*
  * tcg_debug_set -- TEST-ONLY knobs, process-wide.

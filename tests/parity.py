@@ -57,3 +57,57 @@ def sample_indices(extent: int, count: int, seed: int, tile: int = 128) -> np.nd
         picks.update({b - 1, b})
     picks.update(rng.integers(0, extent, size=count).tolist())
     return np.array(sorted(p for p in picks if 0 <= p < extent), dtype=np.int32)
+
+
+def spread_indices(extent: int, count: int, seed: int, tile: int = 128) -> np.ndarray:
+    """`count` distinct indices of [0, extent) (all of them when extent <= count):
+    both edges, both sides of every tile boundary, the rest drawn at random."""
+    if extent <= count:
+        return np.arange(extent, dtype=np.int32)
+    picks = {0, 1, extent - 2, extent - 1}
+    for b in range(tile, extent, tile):
+        picks.update({b - 1, b})
+    rng = np.random.default_rng(seed)
+    if len(picks) > count:
+        # more boundaries than wanted: keep the edges and an even spread of the rest
+        inner = sorted(picks - {0, 1, extent - 2, extent - 1})
+        keep = np.linspace(0, len(inner) - 1, count - 4).round().astype(int)
+        picks = {0, 1, extent - 2, extent - 1} | {inner[i] for i in keep}
+    while len(picks) < count:
+        picks.update(rng.integers(0, extent, size=count - len(picks)).tolist())
+    return np.array(sorted(picks), dtype=np.int32)
+
+
+def check_rows_cols_corners(D, prob, M, N, tol, what, nrows=256, ncols=256, corner=256, seed=0,
+                            exact=False) -> float:
+    """The sampled comparison for outputs too large to compute whole on the
+    CPU: `nrows` full rows and `ncols` full columns of D (edges, both sides of
+    every 128-row / 128-column tile boundary, random positions) and the four
+    corner tiles of corner x corner elements, each element against the oracle.
+    D is the device M x N view; returns the worst error ratio."""
+    import torch
+    rows = spread_indices(M, nrows, seed)
+    cols = spread_indices(N, ncols, seed + 1)
+    all_rows = np.arange(M, dtype=np.int32)
+    all_cols = np.arange(N, dtype=np.int32)
+
+    def fetch(r, c):
+        rr = torch.from_numpy(r).long().to(D.device)
+        cc = torch.from_numpy(c).long().to(D.device)
+        return D.index_select(0, rr).index_select(1, cc).to(torch.float64).cpu().numpy()
+
+    def compare(got, ref, label):
+        if exact:
+            assert np.array_equal(got, ref), f"{what} {label}: max |diff| {np.abs(got - ref).max()}"
+            return 0.0
+        return assert_within(got, ref, tol, f"{what} {label}")
+
+    worst = compare(fetch(rows, all_cols), prob.select(rows, all_cols), "rows")
+    worst = max(worst, compare(fetch(all_rows, cols), prob.select(all_rows, cols), "cols"))
+    cm, cn = min(corner, M), min(corner, N)
+    for r0 in sorted({0, M - cm}):
+        for c0 in sorted({0, N - cn}):
+            r = np.arange(r0, r0 + cm, dtype=np.int32)
+            c = np.arange(c0, c0 + cn, dtype=np.int32)
+            worst = max(worst, compare(fetch(r, c), prob.select(r, c), f"corner ({r0}, {c0})"))
+    return worst

@@ -33,6 +33,27 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def declared_arities():
+    """Parameter count of every function prototype in the header."""
+    with open(os.path.join(ROOT, "include", "tcgemm.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(tcg_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header(lib):
+    """Every ctypes prototype of the binding takes as many arguments as the
+    header's declaration (a stale argtypes list would pass a wrong stack)."""
+    arities = declared_arities()
+    assert set(arities) == set(declared_functions())
+    for name, n in arities.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
+
+
 def test_exports_with_nm(lib):
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", tcg.library_path()], capture_output=True,
@@ -61,6 +82,26 @@ def test_valid_problem_is_ok(lib):
     assert ci(ab="f16") == 0
     assert ci(ab="e5m2", lda=128, ldb=128) == 0
     assert ci(ab="f16", opA="col", lda=304, opB="row", ldb=200) == 0
+
+
+def test_arch_rule_maps_only_sm103_to_ok(lib):
+    """The architecture rule: compute capability 10.3 runs, everything else is
+    TCG_ERR_ARCH (4), including the other Blackwell parts (10.0, 12.0) and
+    Hopper (9.0)."""
+    assert tcg.arch_status(10, 3) == 0
+    for major, minor in [(10, 0), (10, 1), (10, 2), (10, 4), (11, 0), (12, 0), (12, 1), (9, 0), (8, 0),
+                         (0, 0), (-1, 3), (103, 0)]:
+        assert tcg.arch_status(major, minor) == 4, (major, minor)
+
+
+def test_validation_without_a_device_checks_the_arguments_only(lib):
+    """With no CUDA device in the process the architecture rule is skipped and
+    a valid problem is OK (the argument rules still apply, see below)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert ci() == 0
+    assert ci(lda=100) == 1
 
 
 def test_empty_problem_is_ok(lib):

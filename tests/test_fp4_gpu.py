@@ -15,7 +15,7 @@ import torch
 from tiled_tensor_core_persistent_gb300 import harness, inputs
 import tiled_tensor_core_persistent_gb300 as tcg
 
-from parity import TOL, assert_within, oracle_for, sample_indices
+from parity import TOL, assert_within, check_rows_cols_corners, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -90,16 +90,12 @@ def test_fp4_layout_rules():
 
 
 def test_config_nvfp4_8192_bias_relu():
+    """The 8192^3 NVFP4 workload: 256 full rows, 256 full columns and the four
+    256 x 256 corner tiles against the oracle."""
     case = inputs.nvfp4_8192_relu()
     dc = run(case, guard_rows=0)
-    D = dc.D_view[:, :case.N]
-    prob = oracle_for(case)
-    rows = sample_indices(case.M, 32, 8)
-    cols = sample_indices(case.N, 32, 9)
-    got_rows = D[torch.from_numpy(rows).long().to(D.device)].to(torch.float64).cpu().numpy()
-    assert_within(got_rows, prob.select(rows, np.arange(case.N, dtype=np.int32)), TOL["nvfp4"], "rows")
-    got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
-    assert_within(got_cols, prob.select(np.arange(case.M, dtype=np.int32), cols), TOL["nvfp4"], "cols")
+    check_rows_cols_corners(dc.D_view[:, :case.N], oracle_for(case), case.M, case.N, TOL["nvfp4"], case.name,
+                            seed=19)
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])

@@ -1,9 +1,12 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
-Small cases are compared element by element over the whole output; the
-full-size workloads are compared on sampled full rows and full columns
-(edges, tile boundaries and random positions), which the oracle computes one
-element at a time.  Integer-valued inputs with fp32 D must match bit for bit.
+Every output the oracle can compute whole in seconds on the host cores is
+compared element by element: the small cases, the 512^3 and 4096^3
+workloads and all twelve ragged / skinny workloads (three shapes, four A / B
+layouts).  The 8192^3 workloads are compared on 256 full rows, 256 full
+columns (edges, both sides of every tile boundary, random positions) and
+the four 256 x 256 corner tiles, which the oracle computes one element at a
+time.  Integer-valued inputs with fp32 D must match bit for bit.
 """
 import os
 
@@ -14,7 +17,7 @@ import torch
 from tiled_tensor_core_persistent_gb300 import harness, inputs
 import tiled_tensor_core_persistent_gb300 as tcg
 
-from parity import TOL, assert_within, oracle_for, sample_indices
+from parity import TOL, assert_within, check_rows_cols_corners, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -49,22 +52,6 @@ def check_full(case, tol=None, exact=False, guard_rows=2):
     if guard_rows:
         assert dc.untouched_outside(), "wrote outside D's M x N window"
     return dc
-
-
-def check_sampled(case, nrows=96, ncols=96, tol=None, seed=0):
-    dc = run(case)
-    D = dc.D_view[:, :case.N]
-    prob = oracle_for(case)
-    tol = tol if tol is not None else TOL[case.ab_dtype]
-    rows = sample_indices(case.M, nrows, seed)
-    cols = sample_indices(case.N, ncols, seed + 1)
-    all_cols = np.arange(case.N, dtype=np.int32)
-    all_rows = np.arange(case.M, dtype=np.int32)
-    got_rows = D[torch.from_numpy(rows).long().to(D.device)].to(torch.float64).cpu().numpy()
-    w1 = assert_within(got_rows, prob.select(rows, all_cols), tol, case.name + " rows")
-    got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
-    w2 = assert_within(got_cols, prob.select(all_rows, cols), tol, case.name + " cols")
-    return max(w1, w2)
 
 
 # ------------------------------------------------------------ exact checks
@@ -168,24 +155,32 @@ def test_fp8_scaled_bias_relu_small():
 
 @pytest.mark.slow
 def test_config_4096_beta1():
-    check_sampled(inputs.square_4096_beta(), nrows=128, ncols=128)
+    """The whole 4096 x 4096 output against the oracle (about 15 s of oracle time)."""
+    check_full(inputs.square_4096_beta(), guard_rows=1)
+
+
+def check_large(case, seed=0):
+    dc = run(case)
+    return check_rows_cols_corners(dc.D_view[:, :case.N], oracle_for(case), case.M, case.N,
+                                   TOL[case.ab_dtype], case.name, seed=seed)
 
 
 @pytest.mark.slow
 def test_config_8192_bias_gelu():
-    check_sampled(inputs.square_8192_gelu(), nrows=64, ncols=64)
+    check_large(inputs.square_8192_gelu(), seed=4)
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("shape_idx", range(3), ids=["4095x3001x1537", "16x8192x8192", "8192x128x8192"])
 @pytest.mark.parametrize("combo_idx", range(4), ids=["rowrow", "rowcol", "colrow", "colcol"])
 def test_config_ragged(shape_idx, combo_idx):
-    check_sampled(inputs.ragged(shape_idx, combo_idx), nrows=48, ncols=48)
+    """Every element of each ragged / skinny workload, with guard rows around D."""
+    check_full(inputs.ragged(shape_idx, combo_idx), guard_rows=1)
 
 
 @pytest.mark.slow
 def test_config_fp8_8192_bias_relu():
-    check_sampled(inputs.fp8_8192_relu(), nrows=64, ncols=64)
+    check_large(inputs.fp8_8192_relu(), seed=17)
 
 
 # ----------------------------------------------------------------- split-K
@@ -415,3 +410,66 @@ def test_channel_scales_integer_exact():
     case.row_scale = torch.tensor([2.0 ** (i % 3) for i in range(case.M)], dtype=torch.float32)
     case.col_scale = torch.tensor([0.5 ** (j % 2) for j in range(case.N)], dtype=torch.float32)
     check_full(case, exact=True)
+
+
+# ----------------------------------------------- the kernel's GELU, pinned
+
+def gelu_sweep_case():
+    """A GEMM whose outputs are GELU over a dense grid of pre-activations.
+
+    A is one-hot (A[i, i mod K] = 1), so row i of A @ B is row (i mod K) of
+    B; the fp32 bias adds a fine offset per column.  The pre-activations
+    B[i mod K, j] + bias[j] cover [-10, 10] in steps of about 3e-4; the last
+    16 columns hold special values in the bias over a zero B column: +-0,
+    +-tiny (including an fp32 subnormal), moderate and huge magnitudes."""
+    M, N, K = 256, 1040, 64
+    specials = [0.0, -0.0, 1e-30, -1e-30, 1e-40, -1e-40, 3.0, -3.0, 5.5, -5.5, 20.0, -20.0,
+                1e4, -1e4, 3e38, -3e38]
+    nd = N - len(specials)
+    grid = torch.linspace(-10.0, 10.0, K * nd, dtype=torch.float32).view(K, nd)
+    Bl = torch.zeros(K, N, dtype=torch.float32)
+    Bl[:, :nd] = grid.to(torch.bfloat16).to(torch.float32)
+    gen = torch.Generator().manual_seed(301)
+    bias = torch.zeros(N, dtype=torch.float32)
+    bias[:nd] = (torch.rand(nd, generator=gen) * 2.0 - 1.0) * 0.01
+    bias[nd:] = torch.tensor(specials, dtype=torch.float32)
+    Al = torch.zeros(M, K, dtype=torch.float32)
+    Al[torch.arange(M), torch.arange(M) % K] = 1.0
+    A, lda = inputs._store(Al, "row", "bf16")
+    B, ldb = inputs._store(Bl, "col", "bf16")
+    return inputs.GemmCase("gelu_sweep", M, N, K, "row", "col", "bf16", "f32", A, lda, B, ldb,
+                           bias=bias, bias_dtype="f32", act="gelu", ldd=N)
+
+
+@pytest.mark.parametrize("force_cta2", [2, 1], ids=["one_cta", "pair"])
+def test_gelu_error_bound(force_cta2):
+    """The epilogue's GELU (Abramowitz & Stegun 7.1.26 for erf, with the
+    hardware's approximate reciprocal and 2^x) against the oracle's exact
+    0.5 x (1 + erf(x / sqrt 2)) in double, with fp32 D.  Bound per element:
+    |D - D_ref| <= 1e-6 * max(1, |x|).  From 7.1.26's |error in erf| <=
+    1.5e-7, about 2.4e-7 more from the approximate 2^x (relative, on
+    exp(-z^2) <= 1) and about 3e-7 from the approximate reciprocal and the fp32
+    polynomial, the error in erf stays under 1e-6; GELU multiplies it by
+    |x| / 2 and the pre-activation and result roundings add about 1.2e-7 |x|.
+    A wrong sign in the odd extension or a wrong coefficient fails it by
+    orders of magnitude."""
+    try:
+        tcg.debug_set(force_cta2=force_cta2)
+        case = gelu_sweep_case()
+        dc = run(case, guard_rows=1)
+        got = dc.result().numpy()
+        ref = oracle_for(case).full()
+        x = oracle_for(inputs.GemmCase("pre", case.M, case.N, case.K, "row", "col", "bf16", "f32", case.A,
+                                       case.lda, case.B, case.ldb, bias=case.bias, bias_dtype="f32",
+                                       act="none", ldd=case.N)).full()
+        assert np.isfinite(got).all()
+        err = np.abs(got - ref)
+        bound = 1e-6 * np.maximum(1.0, np.abs(x))
+        worst = float((err / bound).max())
+        assert worst <= 1.0, f"GELU error {worst:.3f} x the bound at x = {x.flat[int(np.argmax(err / bound))]!r}"
+        assert dc.untouched_outside()
+        # sanity of the sweep itself: both signs, the whole range, the specials
+        assert x.min() <= -9.99 and x.max() >= 9.99 and (np.abs(x) < 1e-3).any()
+        assert got[0, -1] == 0.0 and got[0, -2] == np.float32(3e38)
+    finally:
+        tcg.debug_set()

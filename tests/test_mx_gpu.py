@@ -15,7 +15,7 @@ import torch
 from tiled_tensor_core_persistent_gb300 import harness, inputs
 import tiled_tensor_core_persistent_gb300 as tcg
 
-from parity import TOL, assert_within, oracle_for, sample_indices
+from parity import TOL, assert_within, check_rows_cols_corners, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -115,17 +115,12 @@ def test_mx_requires_scales_and_fast_layout():
 
 def test_config_mxfp8_8192_bias_relu():
     """The 8192^3 MXFP8 workload (N(0,1) quantised per OCP MX, bias, ReLU, bf16 D):
-    sampled full rows and columns against the oracle."""
+    256 full rows, 256 full columns and the four 256 x 256 corner tiles
+    against the oracle."""
     case = inputs.mxfp8_8192_relu()
     dc = run(case, guard_rows=0)
-    D = dc.D_view[:, :case.N]
-    prob = oracle_for(case)
-    rows = sample_indices(case.M, 48, 5)
-    cols = sample_indices(case.N, 48, 6)
-    got_rows = D[torch.from_numpy(rows).long().to(D.device)].to(torch.float64).cpu().numpy()
-    assert_within(got_rows, prob.select(rows, np.arange(case.N, dtype=np.int32)), TOL["e4m3"], "rows")
-    got_cols = D[:, torch.from_numpy(cols).long().to(D.device)].to(torch.float64).cpu().numpy()
-    assert_within(got_cols, prob.select(np.arange(case.M, dtype=np.int32), cols), TOL["e4m3"], "cols")
+    check_rows_cols_corners(dc.D_view[:, :case.N], oracle_for(case), case.M, case.N, TOL["e4m3"], case.name,
+                            seed=18)
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])

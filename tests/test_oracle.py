@@ -223,7 +223,9 @@ def test_gelu_textbook_values():
         pts = json.load(f)["points"]
     x = np.array([p[0] for p in pts])
     phi = np.array([p[1] for p in pts])
-    np.testing.assert_allclose(oracle.act("gelu", x), x * phi, rtol=1e-14, atol=1e-16)
+    # the table's values are rounded to 15 decimals: |Phi - table| <= 5e-16
+    err = np.abs(oracle.act("gelu", x) - x * phi)
+    assert (err <= np.abs(x) * 6e-16 + 1e-16).all(), err
     assert oracle.act("gelu", np.array([0.0]))[0] == 0.0
     big = oracle.act("gelu", np.array([12.0, -12.0]))
     assert big[0] == 12.0 and abs(big[1]) < 1e-30

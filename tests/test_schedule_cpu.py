@@ -91,13 +91,35 @@ def test_all_tile_stream_k_is_balanced(shape):
     assert min(per_worker.values()) >= total // workers
 
 
-def test_partial_wave_stream_k_evens_out_the_last_wave():
-    # 4096^3 with 256 x 256 pair tiles: 256 tiles on 76 pairs leave a last wave of 28
+def test_partial_wave_is_evened_out():
+    """4096^3 with 256 x 256 pair tiles: 256 tiles on 76 pairs leave a last
+    wave of 28.  Both remedies even it out: the default schedule takes
+    256 x 224 tiles (ceil(4096 / 224) = 19 columns of tiles, 304 tiles = four
+    full waves), and the partial-wave Stream-K schedule (mode 2, 256 wide)
+    spreads the k-blocks of the last tiles over every pair."""
     rows0, w0, t0 = check(4096, 4096, 4096, "bf16", 152, 0)
+    assert max(r[3] for r in rows0) + 1 == 19 and len(rows0) == 16 * 19
+    assert max(w0.values()) == min(w0.values()) == 4 * 32      # four tiles of 32 two-atom k-blocks each
     rows2, w2, t2 = check(4096, 4096, 4096, "bf16", 152, 2)
-    assert t0 == t2
-    assert max(w2.values()) < max(w0.values())
+    assert max(r[3] for r in rows2) + 1 == 16 and t2 == 256 * 32
+    assert max(w2.values()) < 4 * 32
     assert max(w2.values()) - min(w2.values()) <= 1 + max(r[5] - r[4] for r in rows2)
+
+
+def test_wave_fitting_width_choices():
+    """The pair-tile widths the planner's wave model picks for the workloads
+    (on 152 SMs = 76 pairs): narrower tiles only where the last wave of
+    256-wide tiles is far from full, and only for a K-major B."""
+    def width(M, N, K, ab="bf16"):
+        rows = tcg.debug_schedule(M, N, K, ab, num_sms=152, sk_mode=0)
+        ntiles = max(r[3] for r in rows) + 1
+        fits = [bn for bn in (256, 224, 192, 160) if -(-N // bn) == ntiles]
+        assert len(fits) == 1, fits
+        return fits[0]
+    assert width(8192, 8192, 8192) == 256          # 13.5 waves: narrowing saves nothing
+    assert width(8192, 8192, 8192, "e4m3") == 256
+    assert width(4096, 4096, 4096) == 224          # 3.4 waves -> 4 full waves
+    assert width(4095, 3001, 1537) == 224          # 2.5 waves -> 2.9
 
 
 def test_fp8_schedule():

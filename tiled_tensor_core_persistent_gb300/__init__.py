@@ -35,7 +35,7 @@ STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "T
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
             "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc",
             "tcg_debug_schedule", "tcg_grouped_workspace_size", "tcg_gemm_grouped", "tcg_grouped_plan",
-            "tcg_debug_tma_swizzle128"]
+            "tcg_debug_tma_swizzle128", "tcg_arch_status"]
 
 
 class TcgError(RuntimeError):
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.tcg_can_implement.argtypes = [i32, i32, i32, i32, P, i32, i32, P, i32, i32, i32, P, i32, i32,
                                         P, i32, i32, Epilogue]
         L.tcg_can_implement.restype = i32
+        L.tcg_arch_status.argtypes = [i32, i32]
+        L.tcg_arch_status.restype = i32
         L.tcg_workspace_size.argtypes = [i32, i32, i32, i32]
         L.tcg_workspace_size.restype = sz
         L.tcg_workspace_size_for.argtypes = [i32, i32, i32, i32, P, i32, i32, P, i32, i32]
@@ -101,7 +103,7 @@ def lib() -> ctypes.CDLL:
         L.tcg_device_status.restype = i32
         L.tcg_last_error.argtypes = []
         L.tcg_last_error.restype = ctypes.c_char_p
-        L.tcg_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int)]
+        L.tcg_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int)]
         L.tcg_plan.restype = i32
         L.tcg_debug_set.argtypes = [i32, ctypes.c_longlong, i32, i32]
         L.tcg_debug_set.restype = None
@@ -156,6 +158,10 @@ def can_implement(M, N, K, ab_dtype, A, lda, opA, B, ldb, opB, has_c, C, ldc, c_
                                    _enum(c_dtype, DTYPES), _addr(D), ldd, _enum(d_dtype, DTYPES), epi)
 
 
+def arch_status(major: int, minor: int) -> int:
+    return lib().tcg_arch_status(int(major), int(minor))
+
+
 def workspace_size(M, N, K, ab_dtype="bf16") -> int:
     return int(lib().tcg_workspace_size(M, N, K, _enum(ab_dtype, DTYPES)))
 
@@ -207,9 +213,9 @@ def device_status(workspace, stream=None) -> int:
     return int(lib().tcg_device_status(_addr(workspace), _stream(stream)))
 
 
-def plan(M, N, K, ab_dtype="bf16") -> dict:
+def plan(M, N, K, ab_dtype="bf16", opA="row", opB="col") -> dict:
     out = (ctypes.c_int * 10)()
-    st = lib().tcg_plan(M, N, K, _enum(ab_dtype, DTYPES), out)
+    st = lib().tcg_plan(M, N, K, _enum(ab_dtype, DTYPES), _enum(opA, LAYOUTS), _enum(opB, LAYOUTS), out)
     if st != 0:
         raise TcgError(st, "tcg_plan", last_error())
     keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem"]

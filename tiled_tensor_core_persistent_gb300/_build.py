@@ -1,6 +1,6 @@
 """Compile the in-tree CUDA library (libtcgemm.so) for sm_103a with nvcc.
 
-Three translation units compiled in parallel, one -gencode, no cmake: the
+The translation units compile in parallel, one -gencode, no cmake: the
 same commands run on the x86 development machine (cross-compilation, no GPU
 needed) and on the Arm GPU machines.  The result lands in ``_build/`` next to this file.
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 SO_PATH = os.path.join(OUT_DIR, "libtcgemm.so")
 GENCODE = "arch=compute_103a,code=sm_103a"
-UNITS = ("tcgemm_host", "launch_block_scaled", "launch_grouped", "debug_tma")
+UNITS = ("tcgemm_host", "launch_block_scaled", "launch_grouped", "launch_narrow", "debug_tma")
 
 
 def _nvcc() -> str:

@@ -647,8 +647,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     constexpr int kKSteps = kBK / kMmaK;               // MMAs per atom
     constexpr int kAtom = kRowBytes / kElemBytes;      // MN elements per swizzle row
     constexpr int kBRows = kCta2 ? BN / 2 : BN;        // B rows (N) this CTA loads
-    // MN-major B boxes are whole 128-byte MN atoms (e4m3 operands are K-major only)
-    static_assert(kFp8 || kBRows % kAtom == 0, "B rows per CTA must be whole 128-byte MN atoms");
+    static_assert(kBRows % 8 == 0 && BN % kEpiChunk == 0, "B rows in whole 8-row swizzle groups, whole epilogue chunks");
+    // MN-major B boxes are whole 128-byte MN atoms, so an MN-major B needs
+    // kBRows to be a multiple of kAtom; the planner gives other widths (the
+    // wave-fitting pair tiles 256 x 160 / 192 / 224) K-major B only.  8-bit
+    // operands are K-major only.
+    constexpr bool kBMnOk = !kFp8 && kBRows % kAtom == 0;
     constexpr int kTileM = kCta2 ? 2 * kBM : kBM;      // D rows per unit of work
     constexpr int kABytes = kKAtoms * kBM * kRowBytes;
     constexpr int kBBytes = kKAtoms * kBRows * kRowBytes;
@@ -673,7 +677,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     static_assert(kStageBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     // bytes the stage's copies deliver (the scale area's padding is not loaded)
     constexpr uint32_t kTxBytes = (kCta2 ? 2 : 1) * (kABytes + kBBytes + (kMx ? kKAtoms * (kSfA + kSfB) * kSfBlock : 0));
-    constexpr uint32_t kTmemCols = kMx ? 512 : 2 * BN;
+    // TMEM is allocated in powers of two columns: two accumulators of BN
+    constexpr uint32_t kTmemCols = kMx ? 512 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512));
     constexpr int kSfCol0 = kAccBufs * BN;                 // first scale-factor column in TMEM
     static_assert(!kMx || kSfCol0 + 8 * (kSfA + kSfB) * kKAtoms <= 512, "scale columns fit in TMEM for 2 stages");
 
@@ -780,7 +785,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int h = 0; h < kBM / kAtom; ++h)
                                 load(sA + h * kRowBytes * kStageK, &q.tmA, a_row + h * kAtom, k0);
                         }
-                        if (!p.b_mn_major) {
+                        if (!kBMnOk || !p.b_mn_major) {
 #pragma unroll
                             for (int at = 0; at < kKAtoms; ++at)
                                 load(sB + at * kBRows * kRowBytes, &q.tmB, k0 + at * kBK, b_row);

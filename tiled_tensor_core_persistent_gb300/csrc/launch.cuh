@@ -1,10 +1,11 @@
 // launch.cuh -- launching one instantiation of the persistent GEMM kernel.
 //
-// The kernel's instantiations are spread over three translation units that
-// nvcc compiles in parallel: the plain operand types (tcgemm_host.cu), the
-// block-scaled types (launch_block_scaled.cu) and the grouped GEMM
-// (launch_grouped.cu).  Each unit launches only the instantiations it holds;
-// the host code reaches the other two through the functions declared below.
+// The kernel's instantiations are spread over translation units that nvcc
+// compiles in parallel: the plain operand types (tcgemm_host.cu), the
+// block-scaled types (launch_block_scaled.cu), the grouped GEMM
+// (launch_grouped.cu) and the wave-fitting pair widths (launch_narrow.cu).
+// Each unit launches only the instantiations it holds; the host code reaches
+// the others through the functions declared below.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -71,6 +72,11 @@ cudaError_t launch_instance(const KernelParams& kp, const LaunchShape& ls, cudaS
 // CTA with bn 128.  cudaErrorInvalidValue for a combination not built.
 cudaError_t launch_block_scaled(const KernelParams& kp, const LaunchShape& ls, int bn, int katoms, int blk,
                                 cudaStream_t stream, const char** what);
+
+// Wave-fitting pair tiles 256 x bn (bn 160, 192 or 224; 2 K atoms per stage,
+// K-major B) for 16-bit or 8-bit operands.  cudaErrorInvalidValue otherwise.
+cudaError_t launch_narrow_pair(const KernelParams& kp, const LaunchShape& ls, int bn, bool fp8, cudaStream_t stream,
+                               const char** what);
 
 // Grouped GEMM: 256 x 256 pairs with 2 K atoms per stage, or 128 x 256 CTAs
 // with 1, for 16-bit or 8-bit operands.

@@ -61,6 +61,9 @@ const int g_env_mx_bn = env_int("TCG_MX_BN");
 const int g_env_sk = getenv("TCG_SK") ? env_int("TCG_SK") : -1;
 // TCG_NARROW=0 keeps 128/256-wide tiles for small problems (default: narrow them).
 const int g_env_narrow = getenv("TCG_NARROW") ? env_int("TCG_NARROW") : 1;
+// TCG_PAIR_BN = width of 16/8-bit pair tiles (160, 192, 224 or 256) when B is
+// K-major; unset = chosen by the wave model in make_plan.
+const int g_env_pair_bn = env_int("TCG_PAIR_BN");
 
 tcg_status fail_launch(const char* what, cudaError_t e) {
     char buf[512];
@@ -159,6 +162,40 @@ tcg_status device_info(DeviceInfo& out) {
         d.valid = true;
     }
     out = d;
+    return TCG_OK;
+}
+
+// Whether this process sees any CUDA device (asked once).  Without one,
+// tcg_can_implement validates the arguments alone (the CPU tests and tools).
+bool have_device() {
+    static std::once_flag once;
+    static bool present = false;
+    std::call_once(once, [] {
+        int n = 0;
+        if (cudaGetDeviceCount(&n) == cudaSuccess) present = n > 0;
+        else cudaGetLastError();
+    });
+    return present;
+}
+
+tcg_status arch_check(const DeviceInfo& dev) {
+    const tcg_status st = tcg_arch_status(dev.major, dev.minor);
+    if (st != TCG_OK) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "compute capability %d.%d is not 10.3 (sm_103a)", dev.major, dev.minor);
+        g_last_error = buf;
+    }
+    return st;
+}
+
+// Per-call checks of the scale arguments that tcg_can_implement does not see.
+tcg_status check_scales(const tcg_scales& scales, tcg_dtype ab_dtype, int K) {
+    if (scales.col_scale && !aligned_to(scales.col_scale, 4)) return TCG_ERR_MISALIGNED;
+    if (scales.row_scale && !aligned_to(scales.row_scale, 4)) return TCG_ERR_MISALIGNED;
+    if (is_mx(ab_dtype) && K > 0) {
+        if (!scales.block_sfa || !scales.block_sfb) return TCG_ERR_INVALID_ARG;
+        if (!aligned16(scales.block_sfa) || !aligned16(scales.block_sfb)) return TCG_ERR_MISALIGNED;
+    }
     return TCG_OK;
 }
 
@@ -284,7 +321,36 @@ int fixed_smem_bytes(bool small_ring = false) {
 
 int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 
-Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1) {
+// Width of a wave-fitting pair tile (256 x bn, B K-major only): the width
+// among 256, 224, 192 and 160 that minimises the modelled time of the launch,
+// waves x (bn + per-tile fixed cost), where a tile's MMA time grows with bn x K
+// and the fixed cost (the accumulator hand-off and first loads, about two
+// microseconds, measured as a share of the MMA loop on GB300) is expressed in
+// the same units: 1e5 / K columns.  Wave quantisation ("CUTLASS", Part IV
+// Stage 2 and Part XI: the last, partly filled wave of tiles) is what a
+// narrower tile fixes, at the price of more operand bytes per FLOP, so a
+// narrower width is taken only when it saves at least 3 %.
+int wave_fit_bn(int num_m2, int N, int K, int slots) {
+    if (g_env_pair_bn == 160 || g_env_pair_bn == 192 || g_env_pair_bn == 224 || g_env_pair_bn == 256)
+        return g_env_pair_bn;
+    if (slots <= 0) return 256;
+    const double fixed = 1e5 / std::max(K, 1);
+    auto cost = [&](int bn) {
+        const long long tiles = static_cast<long long>(num_m2) * ((N + bn - 1) / bn);
+        const long long waves = (tiles + slots - 1) / slots;
+        return static_cast<double>(waves) * (bn + fixed);
+    };
+    int best = 256;
+    double best_cost = cost(256) * 0.97;
+    for (int bn : {224, 192, 160}) {
+        const double c = cost(bn);
+        if (c < best_cost) { best = bn; best_cost = c; }
+    }
+    return best;
+}
+
+Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1,
+               bool b_kmajor = true) {
     Plan pl;
     const int K = k_units(ab, K_elems);
     const int bk = tcg::kRowBytes / elem_bytes(ab);
@@ -384,6 +450,21 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // Stream-K: balance the k-block iterations of the last tiles over all
     // workers instead of leaving the last wave partly empty.
     const int sk_mode = sk_override >= 0 ? sk_override : (g_env_sk >= 0 ? g_env_sk : 0);
+    // Otherwise a narrower pair tile whose waves come out fuller (B K-major).
+    if (cta2 && !mx && b_kmajor && sk_mode == 0 && g_force_splits == 0 && pl.katoms == 2 && g_force_cta2 < 3) {
+        // K in bf16-equivalent elements (an 8-bit K element costs half the MMA time)
+        const int bn = wave_fit_bn(pl.num_m, N, K * elem_bytes(ab) / 2, slots);
+        if (bn != pl.bn) {
+            pl.bn = bn;
+            pl.num_n = (N + bn - 1) / bn;
+            stages = (dev.max_smem_optin - fixed_smem_bytes()) / stage_bytes(bn, true, pl.katoms);
+            stages = std::max(2, std::min(stages, 8));
+            if (g_env_stages > 1) stages = std::min(stages, g_env_stages);
+            pl.stages = stages;
+            pl.smem = fixed_smem_bytes() + stages * stage_bytes(bn, true, pl.katoms);
+            pl.units_a = pl.units = pl.num_m * pl.num_n;
+        }
+    }
     if (g_force_splits == 0 && pl.num_kb > 0 && sk_mode > 0) {
         const int rem = tiles % slots;
         if (sk_mode == 3) {
@@ -420,6 +501,27 @@ size_t partial_bytes(const Plan& pl) {
 size_t counter_bytes(const Plan& pl) {
     if (!any_split(pl)) return 0;
     return (static_cast<size_t>(pl.num_m) * pl.num_n * pl.cluster * sizeof(int) + 255) / 256 * 256;
+}
+
+// Workspace of one tcg_gemm call, in the order it is laid out: the status
+// header, then the split-K arrival counters and fp32 partials of its plan
+// (`base`), then the packed copies of A and B that the TMA cannot address as
+// stored (block-scaled operands are never packed: they must be aligned).
+struct WorkspaceNeed {
+    size_t base = 0, pack_a = 0, pack_b = 0;
+    size_t total() const { return base + pack_a + pack_b; }
+};
+
+WorkspaceNeed workspace_need(const Plan& pl, int M, int N, int K, tcg_dtype ab, const void* A, int lda,
+                             tcg_layout opA, const void* B, int ldb, tcg_layout opB) {
+    WorkspaceNeed w;
+    w.base = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    if (K > 0 && !is_mx(ab)) {
+        const int eb = elem_bytes(ab);
+        w.pack_a = pack_bytes(M, K, opA, A, lda, eb);
+        w.pack_b = pack_bytes(K, N, opB, B, ldb, eb);
+    }
+    return w;
 }
 
 // Plan of a grouped GEMM: one tile shape for every problem, 256 x 256 pair
@@ -506,9 +608,10 @@ int max_active_pairs(int bn, bool fp8, int katoms, int smem) {
     int n = 0;
     if (bn == 256 && katoms == 2) n = fp8 ? active_pairs_for<256, true, 2>(smem) : active_pairs_for<256, false, 2>(smem);
     if (bn == 256 && katoms == 1) n = fp8 ? active_pairs_for<256, true, 1>(smem) : active_pairs_for<256, false, 1>(smem);
-    // 192-wide (block-scaled) pairs: residency is set by the shared memory, the
-    // block size and the cluster shape, which the 256-wide kernel shares
-    if (bn == 192) n = active_pairs_for<256, true, 2>(smem);
+    // narrower pairs (192-wide block-scaled, the wave-fitting widths): residency
+    // is set by the shared memory, the block size and the cluster shape, which
+    // the 256-wide kernel shares
+    if (bn != 256) n = fp8 ? active_pairs_for<256, true, 2>(smem) : active_pairs_for<256, false, 2>(smem);
     cache[key] = n;
     return n;
 }
@@ -576,7 +679,20 @@ tcg_status tcg_can_implement(int M, int N, int K, tcg_dtype ab_dtype, const void
     if (!aligned_to(D, elem_bytes(d_dtype))) return TCG_ERR_MISALIGNED;
     if (has_c && !aligned_to(C, elem_bytes(c_dtype))) return TCG_ERR_MISALIGNED;
     if (epi.bias && !aligned_to(epi.bias, elem_bytes(epi.bias_dtype))) return TCG_ERR_MISALIGNED;
+    // The kernels exist for sm_103a only ("A10 CuTe, CUTLASS & CuTile", the
+    // pitfalls table: check the architecture a kernel was built for before
+    // running it).  Without any CUDA device only the arguments are validated.
+    if (have_device()) {
+        DeviceInfo dev;
+        const tcg_status st = device_info(dev);
+        if (st != TCG_OK) return st;
+        return arch_check(dev);
+    }
     return TCG_OK;
+}
+
+tcg_status tcg_arch_status(int major, int minor) {
+    return (major == 10 && minor == 3) ? TCG_OK : TCG_ERR_ARCH;
 }
 
 size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
@@ -590,8 +706,8 @@ size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
         dev.max_smem_optin = 232448;
     }
     if (M == 0 || N == 0) return kHeaderBytes;
-    Plan pl = make_plan(M, N, K, ab_dtype, dev);
-    return kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
+    return workspace_need(make_plan(M, N, K, ab_dtype, dev), M, N, K, ab_dtype, nullptr, 0, TCG_ROW, nullptr, 0,
+                          TCG_COL).base;
 }
 
 size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const void* A, int lda, tcg_layout opA,
@@ -599,9 +715,8 @@ size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const voi
     const size_t base = tcg_workspace_size(M, N, K, ab_dtype);
     if (base == 0 || M == 0 || N == 0 || K == 0) return base;
     if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return 0;
-    if (is_mx(ab_dtype)) return base;  // block-scaled operands are never packed
-    const int eb = elem_bytes(ab_dtype);
-    return base + pack_bytes(M, K, opA, A, lda, eb) + pack_bytes(K, N, opB, B, ldb, eb);
+    const WorkspaceNeed w = workspace_need(Plan{}, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB);
+    return base + w.pack_a + w.pack_b;
 }
 
 tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -611,12 +726,13 @@ tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
     return TCG_OK;
 }
 
-tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, int out[10]) {
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[10]) {
     if (M < 0 || N < 0 || K < 0 || !out) return TCG_ERR_INVALID_ARG;
+    if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return TCG_ERR_INVALID_ARG;
     DeviceInfo dev;
     tcg_status st = device_info(dev);
     if (st != TCG_OK) return st;
-    Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
     const int vals[10] = {tcg::kBM, pl.bn, pl.katoms * tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
                           pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem};
     memcpy(out, vals, sizeof vals);
@@ -634,24 +750,13 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     if (M == 0 || N == 0) return TCG_OK;
     DeviceInfo dev;
     if ((st = device_info(dev)) != TCG_OK) return st;
-    if (dev.major != 10 || dev.minor != 3) {
-        char buf[128];
-        snprintf(buf, sizeof buf, "compute capability %d.%d is not 10.3 (sm_103a)", dev.major, dev.minor);
-        g_last_error = buf;
-        return TCG_ERR_ARCH;
-    }
-    if (scales.col_scale && !aligned_to(scales.col_scale, 4)) return TCG_ERR_MISALIGNED;
-    if (scales.row_scale && !aligned_to(scales.row_scale, 4)) return TCG_ERR_MISALIGNED;
-    if (is_mx(ab_dtype) && K > 0) {
-        if (!scales.block_sfa || !scales.block_sfb) return TCG_ERR_INVALID_ARG;
-        if (!aligned16(scales.block_sfa) || !aligned16(scales.block_sfb)) return TCG_ERR_MISALIGNED;
-    }
-    Plan pl = make_plan(M, N, K, ab_dtype, dev);
+    if ((st = arch_check(dev)) != TCG_OK) return st;
+    if ((st = check_scales(scales, ab_dtype, K)) != TCG_OK) return st;
+    Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
     const int eb = elem_bytes(ab_dtype);
-    const size_t base_need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl);
-    const size_t pack_a = (K > 0 && !is_mx(ab_dtype)) ? pack_bytes(M, K, opA, A, lda, eb) : 0;
-    const size_t pack_b = (K > 0 && !is_mx(ab_dtype)) ? pack_bytes(K, N, opB, B, ldb, eb) : 0;
-    const size_t need = base_need + pack_a + pack_b;
+    const WorkspaceNeed wn = workspace_need(pl, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB);
+    const size_t base_need = wn.base, pack_a = wn.pack_a, pack_b = wn.pack_b;
+    const size_t need = wn.total();
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) {
         if (pack_a + pack_b > 0) {
             char buf[200];
@@ -795,6 +900,11 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         const cudaError_t e = tcg::launch_block_scaled(kp, launch_shape(pl), pl.bn, pl.katoms, blk, stream, &what);
         return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
     }
+    if (pl.cluster == 2 && pl.katoms == 2 && pl.bn != 256) {
+        const char* what = "launch";
+        const cudaError_t e = tcg::launch_narrow_pair(kp, launch_shape(pl), pl.bn, fp8, stream, &what);
+        return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
+    }
     if (pl.cluster == 2 && pl.katoms == 2)
         return fp8 ? launch_kernel<256, true, true, 2>(kp, pl, stream)
                    : launch_kernel<256, false, true, 2>(kp, pl, stream);
@@ -910,6 +1020,9 @@ extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const v
     if (M == 0 || N == 0) return TCG_OK;
     DeviceInfo dev;
     if ((st = device_info(dev)) != TCG_OK) return st;
+    // Everything tcg_gemm would refuse is refused before the scratch is touched.
+    if ((st = arch_check(dev)) != TCG_OK) return st;
+    if ((st = check_scales(scales, ab_dtype, K)) != TCG_OK) return st;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return fail_launch("cudaGetDevice", e);
@@ -926,10 +1039,8 @@ extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const v
         }
         scratch = g_noalloc_ptr[device];
     }
-    const Plan pl = make_plan(M, N, K, ab_dtype, dev);
-    const int eb = elem_bytes(ab_dtype);
-    const size_t need = kHeaderBytes + counter_bytes(pl) + partial_bytes(pl) +
-                        (K > 0 ? pack_bytes(M, K, opA, A, lda, eb) + pack_bytes(K, N, opB, B, ldb, eb) : 0);
+    const Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
+    const size_t need = workspace_need(pl, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB).total();
     if (need > kNoAllocScratchBytes) {
         char buf[200];
         snprintf(buf, sizeof buf,
@@ -1010,12 +1121,7 @@ extern "C" tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* prob
     if (live.empty()) return TCG_OK;
     DeviceInfo dev;
     if ((st = device_info(dev)) != TCG_OK) return st;
-    if (dev.major != 10 || dev.minor != 3) {
-        char buf[128];
-        snprintf(buf, sizeof buf, "compute capability %d.%d is not 10.3 (sm_103a)", dev.major, dev.minor);
-        g_last_error = buf;
-        return TCG_ERR_ARCH;
-    }
+    if ((st = arch_check(dev)) != TCG_OK) return st;
     const int n = static_cast<int>(live.size());
     const size_t table = grouped_table_bytes(n);
     if (!workspace || !aligned16(workspace) || workspace_bytes < kHeaderBytes + table) return TCG_ERR_WORKSPACE;
