@@ -57,7 +57,8 @@ typedef enum {
     TCG_ERR_ARCH = 4,          /* current device is not compute capability 10.3 */
     TCG_ERR_WORKSPACE = 5,     /* workspace NULL, misaligned or smaller than tcg_workspace_size_for */
     TCG_ERR_LAUNCH = 6,        /* a CUDA runtime/driver call failed (message: tcg_last_error) */
-    TCG_ERR_TIMEOUT = 7        /* a bounded device-side wait ran out (reported by tcg_device_status) */
+    TCG_ERR_TIMEOUT = 7,       /* a bounded device-side wait ran out (reported by tcg_device_status) */
+    TCG_ERR_CHECK = 8          /* debug build only: a device-side consistency check failed (tcg_device_status) */
 } tcg_status;
 
 typedef enum { TCG_ROW = 0, TCG_COL = 1 } tcg_layout;
@@ -204,9 +205,18 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha,
 
 /*
  * tcg_device_status -- synchronises `stream`, reads the workspace status word
- * (TCG_OK or TCG_ERR_TIMEOUT) written by earlier tcg_gemm calls on this
- * workspace, and clears it.  Returns TCG_ERR_LAUNCH if the stream itself
- * reports a CUDA error.
+ * (TCG_OK, TCG_ERR_TIMEOUT, or in the debug build TCG_ERR_CHECK) written by
+ * earlier tcg_gemm calls on this workspace, and clears it.  Returns
+ * TCG_ERR_LAUNCH if the stream itself reports a CUDA error.
+ *
+ * Debug build: libtcgemm_debug.so (the same sources compiled with
+ * TCG_DEBUG_CHECKS) checks the kernel's pipeline bookkeeping on the device:
+ * stage, accumulator, epilogue-buffer, TMEM-column, partial-slot and counter
+ * indices in range, every unit of work inside the tile grid, and after each
+ * mbarrier wait that the following phase has not completed as well.  A
+ * failed check ends the CTA without a trap and records TCG_ERR_CHECK with the
+ * check's code and the block, which tcg_device_status returns (message in
+ * tcg_last_error).
  */
 tcg_status tcg_device_status(void* workspace, void* stream);
 
@@ -216,26 +226,36 @@ const char* tcg_last_error(void);
 /*
  * tcg_plan -- the launch plan tcg_gemm would use for these sizes, operand
  * type and A / B layouts (for tests and tools).
- * out[0..9] = {BM, BN, BK, stages, splits, grid CTAs, cluster size,
- *              units of work, raster group, dynamic smem bytes}.
+ * out[0..10] = {BM, BN, BK, stages, splits, grid CTAs, cluster size,
+ *               units of work, raster group, dynamic smem bytes, swapped}.
  * BN of a pair tile may be 160, 192 or 224 instead of 256 when B is
  * column-major (K-contiguous) and the narrower tile fills the last wave
- * better.  units of work > tiles x splits when the last tiles are split
- * over K to fill the last wave.
+ * better.  swapped = 1 (only on request: TCG_SWAP=1 in the environment when
+ * the library loads, or the test knob below): a GEMM with at most 64 rows and
+ * a row-major A runs as the transposed product D^T = B^T A^T (written back
+ * into the row-major D);
+ * BM, BN, splits and units then count the transposed problem's tiles (BM
+ * over D's columns, BN = 32 or 64 over D's rows).  units of work > tiles x
+ * splits when the last tiles are split over K to fill the last wave.
  * Needs the current device (queries SM count and shared-memory limit).
  */
-tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[10]);
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[11]);
 
 /*
  * tcg_debug_set -- TEST-ONLY knobs, process-wide.
  *   fault_inject = 1: in the next launches, CTA 0's producer skips its first
  *     stage (no loads, no arrival), so the MMA issuer's bounded wait runs out
  *     and the kernel records TCG_ERR_TIMEOUT instead of hanging.
+ *   fault_inject = 2: debug build only: CTA 0's producer fails a check before
+ *     its first stage (code 199), so the kernel records TCG_ERR_CHECK and
+ *     ends the way a timeout does; the release build ignores it.
  *   wait_timeout_ns: limit of every bounded device-side wait (0 = default 2 s).
  *   force_splits / force_cta2: override the planner (0 = automatic).
  *     force_cta2: 1 = 2-CTA pair tiles, 2 = one-CTA tiles; for the
  *     block-scaled types 3 / 4 = pair tiles 256 / 192 wide (NVFP4: 256
- *     always; the default width is 256).
+ *     always; the default width is 256); 5 = one-CTA tiles, and a GEMM with
+ *     at most 64 rows, a row-major A and at least 256 columns runs as the
+ *     transposed product D^T = B^T A^T (see tcg_plan).
  */
 void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits, int force_cta2);
 
@@ -243,9 +263,11 @@ void tcg_debug_set(int fault_inject, long long wait_timeout_ns, int force_splits
  * tcg_debug_schedule -- TEST-ONLY, needs no GPU: the work schedule tcg_gemm
  * would run on a device with num_sms SMs.  sk_mode: -1 = the default, 0 = no
  * Stream-K, 1 = last partial wave plus one full wave as Stream-K, 2 = last
- * partial wave only, 3 = all tiles.  Writes up to max_rows rows of 9 ints,
+ * partial wave only, 3 = all tiles.  Writes up to max_rows rows of 10 ints,
  * one per unit of work in the order each worker runs them:
- *   {worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, partial slot}
+ *   {worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, partial slot, half}
+ * (half: 0 for a whole tile; 1 / 2 for the first / second half of a
+ * 256-wide tile's columns, when the last wave runs as half-width units)
  * (k-blocks are pipeline stages; partial slot -1 for an unsplit tile) and
  * returns the number of units (which may exceed max_rows), or -1 for
  * invalid sizes.

@@ -48,7 +48,7 @@ int main(void) {
     CHECK(tcg_gemm_grouped(2, probs, TCG_ROW, TCG_COL, 0.0f, TCG_BF16, TCG_BF16, epi, TCG_BF16, NULL, 0,
                            NULL) == TCG_ERR_INVALID_ARG);
 
-    int rows[9 * 64];
+    int rows[10 * 64];
     const int n = tcg_debug_schedule(4096, 4096, 4096, TCG_BF16, 152, 0, rows, 64);
     CHECK(n > 0);
     printf("abi_check ok: %d units in the 4096^3 schedule, %s\n", n, tcg_last_error());

@@ -221,3 +221,17 @@ def test_header_compiles_as_c99_and_links(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "abi_check ok" in r.stdout
+
+
+def test_debug_variant_builds_and_exports_the_same_symbols(lib):
+    """libtcgemm_debug.so (the kernel's device-side checks compiled in) builds
+    from the same sources and exports the same C ABI."""
+    import subprocess
+    path = _build.build(debug=True)
+    assert path.endswith("libtcgemm_debug.so")
+
+    def exported(p):
+        out = subprocess.run(["nm", "-D", "--defined-only", p], capture_output=True, text=True).stdout
+        return {m.group(1) for m in re.finditer(r"\bT (tcg_[a-z0-9_]+)$", out, flags=re.M)}
+
+    assert exported(path) == exported(tcg.library_path()) == set(declared_functions())

@@ -473,3 +473,110 @@ def test_gelu_error_bound(force_cta2):
         assert got[0, -1] == 0.0 and got[0, -2] == np.float32(3e38)
     finally:
         tcg.debug_set()
+
+
+# --------------------- split-K pieces summed by the finishing CTA (both paths)
+
+@pytest.mark.parametrize("combo", inputs.LAYOUT_COMBOS, ids=lambda c: c[0] + c[1])
+def test_skinny_pair_split_k_integer_exact(combo):
+    """A tall, narrow, long-K problem runs on 256 x 128 pair tiles with split
+    K; the finishing CTA of each tile takes its own piece from TMEM and the
+    others from global memory, in piece order.  Integer inputs: exact, and
+    run-to-run identical."""
+    M, N, K = 2000, 120, 3000
+    pl = tcg.plan(M, N, K, "bf16", combo[0], combo[1])
+    assert pl["cluster"] == 2 and pl["BN"] == 128 and pl["splits"] > 1, pl
+    case = inputs.make_case("skinny_pair", M, N, K, seed=401, dist="int4", opA=combo[0], opB=combo[1],
+                            d_dtype="f32", beta=0.5, c_dist="int4", c_dtype="f32", bias_std=1.0,
+                            bias_dtype="f32", act="relu")
+    case.bias = torch.round(case.bias)
+    dc = check_full(case, exact=True)
+    first = dc.D_view.clone()
+    dc.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first, dc.D_view)
+
+
+def test_split_k_own_quadrant_fixup_integer_exact():
+    """One-CTA split-K tiles whose four row groups all hold rows (M a multiple
+    of 128 plus a ragged last tile): the finishing CTA adds its own piece
+    from TMEM.  Exact on integer inputs, in every split count."""
+    for splits in (2, 3, 4):
+        try:
+            tcg.debug_set(force_splits=splits)
+            case = inputs.make_case(f"ownq{splits}", 300, 384, 2048, seed=410 + splits, dist="int4",
+                                    d_dtype="f32")
+            assert tcg.plan(case.M, case.N, case.K)["splits"] == splits
+            check_full(case, exact=True)
+        finally:
+            tcg.debug_set()
+
+
+# ------------- GEMMs with few rows: the transposed product D^T = B^T A^T
+# (taken on request only: measured no faster than the plain plan, whose
+# skinny problems are all bound by B's bytes; the test knob force_cta2 = 5
+# asks for it)
+
+SWAP_SHAPES = [(1, 256, 64), (7, 300, 200), (16, 1000, 1000), (31, 520, 4096), (32, 2048, 64), (33, 384, 777),
+               (48, 8192, 1024), (64, 700, 2048)]
+
+
+@pytest.fixture
+def transposed():
+    tcg.debug_set(force_cta2=5)
+    yield
+    tcg.debug_set()
+
+
+@pytest.mark.parametrize("shape", SWAP_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("opB", ["col", "row"])
+def test_few_rows_transposed_product_integer_exact(shape, opB, transposed):
+    """At most 64 rows and a row-major A: the transposed product (the
+    kernel's tiles run over D's columns; the epilogue writes each tile back
+    into row-major D and reads C the same way, bias per column).  Integer
+    inputs with fp32 D, beta * C, an integer bias and ReLU: exact, with guard
+    rows around D."""
+    M, N, K = shape
+    pl = tcg.plan(M, N, K, "bf16", "row", opB)
+    assert pl["swap"] == 1 and pl["BN"] == (32 if M <= 32 else 64), pl
+    case = inputs.make_case(f"swap{M}x{N}x{K}", M, N, K, seed=M * 31 + N + K, dist="int4", opB=opB,
+                            d_dtype="f32", beta=0.5, c_dist="int4", c_dtype="f32", bias_std=2.0,
+                            bias_dtype="f32", act="relu")
+    case.bias = torch.round(case.bias)
+    check_full(case, exact=True)
+
+
+def test_few_rows_transposed_product_bf16_epilogue_and_split_k(transposed):
+    """The transposed product with long K (split into pieces summed in a fixed
+    order), bf16 C and D, bias and GELU, within the bf16 tolerance and
+    run-to-run identical."""
+    case = inputs.make_case("swap_epi", 16, 3000, 6144, seed=421, dist="uniform", beta=0.5, c_dist="uniform",
+                            bias_std=0.1, act="gelu")
+    pl = tcg.plan(case.M, case.N, case.K)
+    assert pl["swap"] == 1 and pl["splits"] > 1, pl
+    dc = check_full(case)
+    first = dc.D_view.clone()
+    dc.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), dc.D_view.view(torch.int16))
+
+
+def test_few_rows_transposed_product_fp8_and_scales_exact(transposed):
+    """e4m3 operands and power-of-two row / column scales (swapped into the
+    transposed frame by the host): exact on integer inputs."""
+    case = inputs.make_case("swap_f8", 24, 640, 512, seed=431, dist="int4", ab_dtype="e4m3", d_dtype="f32")
+    case.row_scale = torch.tensor([2.0 ** (i % 3) for i in range(case.M)], dtype=torch.float32)
+    case.col_scale = torch.tensor([0.5 ** (j % 2) for j in range(case.N)], dtype=torch.float32)
+    assert tcg.plan(case.M, case.N, case.K, "e4m3")["swap"] == 1
+    check_full(case, exact=True)
+
+
+def test_few_rows_default_and_column_major_a_keep_the_plain_plan():
+    assert tcg.plan(16, 8192, 8192)["swap"] == 0
+    tcg.debug_set(force_cta2=5)
+    try:
+        case = inputs.make_case("noswap", 16, 640, 512, seed=441, dist="int4", opA="col", d_dtype="f32")
+        assert tcg.plan(case.M, case.N, case.K, "bf16", "col", "col")["swap"] == 0
+        check_full(case, exact=True)
+    finally:
+        tcg.debug_set()

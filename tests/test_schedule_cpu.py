@@ -36,21 +36,30 @@ def check(M, N, K, ab, sms, mode):
     assert rows, "empty schedule"
     plan_tiles = {}
     pieces = defaultdict(list)
-    for wid, tile, m, n, kb0, kb1, split, nsplit, slot in rows:
+    for wid, tile, m, n, kb0, kb1, split, nsplit, slot, half in rows:
         assert 0 <= kb0 < kb1, (tile, kb0, kb1)
         key = (m, n)
         assert plan_tiles.setdefault(tile, key) == key, "a tile index maps to two output tiles"
-        pieces[tile].append((split, kb0, kb1, nsplit, slot, wid))
+        pieces[(tile, half)].append((split, kb0, kb1, nsplit, slot, wid))
+    # a tile runs whole, or as its two column halves (the last wave's tail), never both
+    halves = defaultdict(set)
+    for tile, half in pieces:
+        halves[tile].add(half)
+    assert all(h == {0} or h == {1, 2} for h in halves.values()), halves
+    half_tiles = sorted(t for t, h in halves.items() if h == {1, 2})
+    assert half_tiles == list(range(len(halves) - len(half_tiles), len(halves))), "halves are the last tiles"
     # the tile index -> (m, n) map is one to one and covers the whole output grid
     assert len(set(plan_tiles.values())) == len(plan_tiles)
     num_m = max(m for m, _ in plan_tiles.values()) + 1
     num_n = max(n for _, n in plan_tiles.values()) + 1
     assert set(plan_tiles.values()) == {(m, n) for m in range(num_m) for n in range(num_n)}
     assert sorted(plan_tiles) == list(range(num_m * num_n))
+    # and that grid spans the problem (no tile is taller or wider than 256)
+    assert num_m * 256 >= M and num_n * 256 >= N, (num_m, num_n)
     slots = []
     num_kb = None
     per_worker = defaultdict(int)
-    for tile, ps in pieces.items():
+    for (tile, half), ps in pieces.items():
         ps.sort()
         nsplit = ps[0][3]
         assert all(p[3] == nsplit for p in ps)
@@ -93,13 +102,14 @@ def test_all_tile_stream_k_is_balanced(shape):
 
 def test_partial_wave_is_evened_out():
     """4096^3 with 256 x 256 pair tiles: 256 tiles on 76 pairs leave a last
-    wave of 28.  Both remedies even it out: the default schedule takes
-    256 x 224 tiles (ceil(4096 / 224) = 19 columns of tiles, 304 tiles = four
-    full waves), and the partial-wave Stream-K schedule (mode 2, 256 wide)
-    spreads the k-blocks of the last tiles over every pair."""
+    wave of 28.  Both remedies even it out: the default schedule runs those
+    28 tiles as 56 half-width units (three full waves, then one of half
+    tiles on 56 of the 76 pairs), and the partial-wave Stream-K schedule
+    (mode 2) spreads the k-blocks of the last tiles over every pair."""
     rows0, w0, t0 = check(4096, 4096, 4096, "bf16", 152, 0)
-    assert max(r[3] for r in rows0) + 1 == 19 and len(rows0) == 16 * 19
-    assert max(w0.values()) == min(w0.values()) == 4 * 32      # four tiles of 32 two-atom k-blocks each
+    assert max(r[3] for r in rows0) + 1 == 16 and len(rows0) == 228 + 56
+    assert sum(1 for r in rows0 if r[9]) == 56 and all(r[1] >= 228 for r in rows0 if r[9])
+    assert max(w0.values()) == 4 * 32 and min(w0.values()) == 3 * 32   # the busiest pairs end with a half tile
     rows2, w2, t2 = check(4096, 4096, 4096, "bf16", 152, 2)
     assert max(r[3] for r in rows2) + 1 == 16 and t2 == 256 * 32
     assert max(w2.values()) < 4 * 32
@@ -107,19 +117,20 @@ def test_partial_wave_is_evened_out():
 
 
 def test_wave_fitting_width_choices():
-    """The pair-tile widths the planner's wave model picks for the workloads
-    (on 152 SMs = 76 pairs): narrower tiles only where the last wave of
-    256-wide tiles is far from full, and only for a K-major B."""
-    def width(M, N, K, ab="bf16"):
+    """The last-wave remedies the planner's wave model picks for the workloads
+    (on 152 SMs = 76 pairs): a half-width tail where the last wave of
+    256-wide tiles would use at most half of the pairs, a narrower tile
+    (K-major B only) where it would not."""
+    def plan(M, N, K, ab="bf16"):
         rows = tcg.debug_schedule(M, N, K, ab, num_sms=152, sk_mode=0)
         ntiles = max(r[3] for r in rows) + 1
         fits = [bn for bn in (256, 224, 192, 160) if -(-N // bn) == ntiles]
         assert len(fits) == 1, fits
-        return fits[0]
-    assert width(8192, 8192, 8192) == 256          # 13.5 waves: narrowing saves nothing
-    assert width(8192, 8192, 8192, "e4m3") == 256
-    assert width(4096, 4096, 4096) == 224          # 3.4 waves -> 4 full waves
-    assert width(4095, 3001, 1537) == 224          # 2.5 waves -> 2.9
+        return fits[0], len({r[1] for r in rows if r[9]})
+    assert plan(8192, 8192, 8192) == (256, 36)     # 13 full waves, then 36 tiles as 72 half units
+    assert plan(8192, 8192, 8192, "e4m3") == (256, 36)
+    assert plan(4096, 4096, 4096) == (256, 28)     # 3 full waves + 56 half units
+    assert plan(4095, 3001, 1537) == (224, 0)      # 40 leftover tiles: 80 halves would not fit one wave
 
 
 def test_fp8_schedule():

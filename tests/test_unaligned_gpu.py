@@ -162,6 +162,7 @@ def test_split_k_few_rows_with_c():
     try:
         case = inputs.make_case("split_m16", 16, 520, 1536, seed=151, dist="int4", beta=1.0, c_dist="int4",
                                 c_dtype="f32", d_dtype="f32")
+        assert tcg.plan(case.M, case.N, case.K)["swap"] == 0
         dc = run(case)
         assert np.array_equal(dc.result().numpy(), oracle_for(case).full())
         assert dc.untouched_outside()

@@ -92,8 +92,8 @@ def test_noalloc_matches_workspace_entry_point_twice(which):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
-    case = inputs.make_case("noalloc_big", 16, 8192, 8192, seed=181, dist="uniform")
-    tcg.debug_set(force_splits=16)  # 32 tiles x 16 splits of fp32 partials = 64 MiB
+    case = inputs.make_case("noalloc_big", 128, 8192, 8192, seed=181, dist="uniform")
+    tcg.debug_set(force_splits=16)  # 32 tiles x 16 splits of 128 x 256 fp32 partials = 64 MiB
     dc = harness.DeviceCase(case)
     with pytest.raises(tcg.TcgError) as err:
         noalloc(case, dc, dc.D_view)

@@ -30,7 +30,8 @@ LAYOUTS = {"row": ROW, "col": COL}
 ACTS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
 
 STATUS = {0: "TCG_OK", 1: "TCG_ERR_INVALID_ARG", 2: "TCG_ERR_UNSUPPORTED", 3: "TCG_ERR_MISALIGNED",
-          4: "TCG_ERR_ARCH", 5: "TCG_ERR_WORKSPACE", 6: "TCG_ERR_LAUNCH", 7: "TCG_ERR_TIMEOUT"}
+          4: "TCG_ERR_ARCH", 5: "TCG_ERR_WORKSPACE", 6: "TCG_ERR_LAUNCH", 7: "TCG_ERR_TIMEOUT",
+          8: "TCG_ERR_CHECK"}
 
 EXPORTED = ["tcg_can_implement", "tcg_workspace_size", "tcg_workspace_size_for", "tcg_workspace_init", "tcg_gemm",
             "tcg_device_status", "tcg_last_error", "tcg_plan", "tcg_debug_set", "tcg_gemm_noalloc",
@@ -67,7 +68,8 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.SO_PATH
+    """libtcgemm.so, or libtcgemm_debug.so (device-side checks) when TCG_DEBUG=1."""
+    return _build.so_path()
 
 
 def lib() -> ctypes.CDLL:
@@ -214,24 +216,24 @@ def device_status(workspace, stream=None) -> int:
 
 
 def plan(M, N, K, ab_dtype="bf16", opA="row", opB="col") -> dict:
-    out = (ctypes.c_int * 10)()
+    out = (ctypes.c_int * 11)()
     st = lib().tcg_plan(M, N, K, _enum(ab_dtype, DTYPES), _enum(opA, LAYOUTS), _enum(opB, LAYOUTS), out)
     if st != 0:
         raise TcgError(st, "tcg_plan", last_error())
-    keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem"]
+    keys = ["BM", "BN", "BK", "stages", "splits", "grid", "cluster", "units", "group_m", "smem", "swap"]
     return dict(zip(keys, list(out)))
 
 
 def debug_schedule(M, N, K, ab_dtype="bf16", num_sms=152, sk_mode=-1) -> list:
     """TEST-ONLY: the units of work tcg_gemm would run (see tcg_debug_schedule):
-    a list of (worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, slot)."""
+    a list of (worker, tile, m_blk, n_blk, kb0, kb1, split, nsplit, slot, half)."""
     L = lib()
     n = L.tcg_debug_schedule(M, N, K, _enum(ab_dtype, DTYPES), num_sms, sk_mode, None, 0)
     if n < 0:
         raise TcgError(1, "tcg_debug_schedule")
-    buf = (ctypes.c_int * (9 * max(n, 1)))()
+    buf = (ctypes.c_int * (10 * max(n, 1)))()
     L.tcg_debug_schedule(M, N, K, _enum(ab_dtype, DTYPES), num_sms, sk_mode, buf, n)
-    return [tuple(buf[9 * i:9 * i + 9]) for i in range(n)]
+    return [tuple(buf[10 * i:10 * i + 10]) for i in range(n)]
 
 
 def debug_set(fault_inject=0, wait_timeout_ns=0, force_splits=0, force_cta2=0) -> None:

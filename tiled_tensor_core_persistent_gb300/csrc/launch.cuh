@@ -3,7 +3,8 @@
 // The kernel's instantiations are spread over translation units that nvcc
 // compiles in parallel: the plain operand types (tcgemm_host.cu), the
 // block-scaled types (launch_block_scaled.cu), the grouped GEMM
-// (launch_grouped.cu) and the wave-fitting pair widths (launch_narrow.cu).
+// (launch_grouped.cu), the narrower pair tiles (launch_narrow.cu) and the
+// transposed-output tiles of the operand-swapped product (launch_swapped.cu).
 // Each unit launches only the instantiations it holds; the host code reaches
 // the others through the functions declared below.
 #pragma once
@@ -25,24 +26,24 @@ struct LaunchShape {
 
 constexpr int kMaxDynamicSmem = 232448;   // 227 KiB per block
 
-template <int BN, bool kFp8, bool kCta2, int KA, int kBlk = 0, bool kGrouped = false>
+template <int BN, bool kFp8, bool kCta2, int KA, int kBlk = 0, bool kGrouped = false, bool kTrans = false>
 cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped>,
+        err = cudaFuncSetAttribute(gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped, kTrans>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
         if (err == cudaSuccess && kCta2)
-            err = cudaFuncSetAttribute(gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped>,
+            err = cudaFuncSetAttribute(gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped, kTrans>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     });
     return err;
 }
 
 // One launch; on failure *what names the call that failed.
-template <int BN, bool kFp8, bool kCta2, int KA, int kBlk = 0, bool kGrouped = false>
+template <int BN, bool kFp8, bool kCta2, int KA, int kBlk = 0, bool kGrouped = false, bool kTrans = false>
 cudaError_t launch_instance(const KernelParams& kp, const LaunchShape& ls, cudaStream_t stream, const char** what) {
-    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA, kBlk, kGrouped>();
+    cudaError_t e = set_smem_attr<BN, kFp8, kCta2, KA, kBlk, kGrouped, kTrans>();
     if (e != cudaSuccess) {
         *what = "cudaFuncSetAttribute";
         return e;
@@ -62,7 +63,7 @@ cudaError_t launch_instance(const KernelParams& kp, const LaunchShape& ls, cudaS
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped>, kp);
+    e = cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<BN, kFp8, kCta2, KA, kBlk, kGrouped, kTrans>, kp);
     if (e != cudaSuccess) *what = "cudaLaunchKernelEx";
     return e;
 }
@@ -73,10 +74,17 @@ cudaError_t launch_instance(const KernelParams& kp, const LaunchShape& ls, cudaS
 cudaError_t launch_block_scaled(const KernelParams& kp, const LaunchShape& ls, int bn, int katoms, int blk,
                                 cudaStream_t stream, const char** what);
 
-// Wave-fitting pair tiles 256 x bn (bn 160, 192 or 224; 2 K atoms per stage,
-// K-major B) for 16-bit or 8-bit operands.  cudaErrorInvalidValue otherwise.
+// Pair tiles narrower than 256 (2 K atoms per stage) for 16-bit or 8-bit
+// operands: 256 x 128 (split K, any B layout) and the wave-fitting 256 x 160
+// / 192 / 224 (K-major B).  cudaErrorInvalidValue otherwise.
 cudaError_t launch_narrow_pair(const KernelParams& kp, const LaunchShape& ls, int bn, bool fp8, cudaStream_t stream,
                                const char** what);
+
+// Transposed-output tiles 128 x bn (bn 32 or 64, one CTA, one or two K atoms
+// per stage) of the operand-swapped product D^T = B^T A^T, for GEMMs with at most
+// 64 rows.  cudaErrorInvalidValue otherwise.
+cudaError_t launch_swapped(const KernelParams& kp, const LaunchShape& ls, int bn, int katoms, bool fp8,
+                           cudaStream_t stream, const char** what);
 
 // Grouped GEMM: 256 x 256 pairs with 2 K atoms per stage, or 128 x 256 CTAs
 // with 1, for 16-bit or 8-bit operands.

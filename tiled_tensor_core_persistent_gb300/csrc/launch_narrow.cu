@@ -1,6 +1,6 @@
-// launch_narrow.cu -- the wave-fitting pair-tile instantiations of the
-// persistent GEMM kernel (256 x 160 / 192 / 224, K-major B), in a
-// translation unit of their own.
+// launch_narrow.cu -- the pair-tile instantiations narrower than 256: the
+// wave-fitting widths (256 x 160 / 192 / 224, K-major B) and the 256 x 128
+// split-K tiles of tall, narrow problems, in a translation unit of their own.
 #include "launch.cuh"
 
 namespace tcg {
@@ -9,6 +9,9 @@ cudaError_t launch_narrow_pair(const KernelParams& kp, const LaunchShape& ls, in
                                const char** what) {
     if (ls.cluster == 2) {
         switch (bn) {
+            case 128:
+                return fp8 ? launch_instance<128, true, true, 2>(kp, ls, stream, what)
+                           : launch_instance<128, false, true, 2>(kp, ls, stream, what);
             case 160:
                 return fp8 ? launch_instance<160, true, true, 2>(kp, ls, stream, what)
                            : launch_instance<160, false, true, 2>(kp, ls, stream, what);

@@ -61,6 +61,15 @@ const int g_env_mx_bn = env_int("TCG_MX_BN");
 const int g_env_sk = getenv("TCG_SK") ? env_int("TCG_SK") : -1;
 // TCG_NARROW=0 keeps 128/256-wide tiles for small problems (default: narrow them).
 const int g_env_narrow = getenv("TCG_NARROW") ? env_int("TCG_NARROW") : 1;
+// TCG_SKINNY_PAIRS=0 keeps one-CTA tiles for split-K problems with at most 128 columns.
+const int g_env_skinny_pairs = getenv("TCG_SKINNY_PAIRS") ? env_int("TCG_SKINNY_PAIRS") : 1;
+// TCG_SWAP=1 runs GEMMs with at most 64 rows as the transposed product (use_swap).
+const int g_env_swap = env_int("TCG_SWAP");
+// TCG_TMA_STORE=1 stages every chunk of D in shared memory for a TMA store (the
+// path of a ragged last chunk) instead of storing whole chunks from registers.
+const int g_env_tma_store = env_int("TCG_TMA_STORE");
+// TCG_HALF_TAIL=0 never runs the last wave as half-width tiles, =2 always when it fits.
+const int g_env_half_tail = getenv("TCG_HALF_TAIL") ? env_int("TCG_HALF_TAIL") : 1;
 // TCG_PAIR_BN = width of 16/8-bit pair tiles (160, 192, 224 or 256) when B is
 // K-major; unset = chosen by the wave model in make_plan.
 const int g_env_pair_bn = env_int("TCG_PAIR_BN");
@@ -308,6 +317,8 @@ struct Plan {
     int units_a = 0;    // units of the data-parallel phase (tiles x splits)
     int sk_tiles = 0;   // tiles of the Stream-K phase (the last ones in raster order)
     int workers = 0;    // CTAs or CTA pairs
+    bool swap = false;  // the transposed product D^T = B^T A^T (sizes and tiles in its frame)
+    int half_tail = 0;  // last tiles run as two half-width units each (wave_fit)
 };
 
 int stage_bytes(int bn, bool cta2, int katoms, int sf_blocks = 0) {
@@ -321,41 +332,81 @@ int fixed_smem_bytes(bool small_ring = false) {
 
 int max_active_pairs(int bn, bool fp8, int katoms, int smem);
 
-// Width of a wave-fitting pair tile (256 x bn, B K-major only): the width
-// among 256, 224, 192 and 160 that minimises the modelled time of the launch,
-// waves x (bn + per-tile fixed cost), where a tile's MMA time grows with bn x K
-// and the fixed cost (the accumulator hand-off and first loads, about two
-// microseconds, measured as a share of the MMA loop on GB300) is expressed in
-// the same units: 1e5 / K columns.  Wave quantisation ("CUTLASS", Part IV
-// Stage 2 and Part XI: the last, partly filled wave of tiles) is what a
-// narrower tile fixes, at the price of more operand bytes per FLOP, so a
-// narrower width is taken only when it saves at least 3 %.
-int wave_fit_bn(int num_m2, int N, int K, int slots) {
-    if (g_env_pair_bn == 160 || g_env_pair_bn == 192 || g_env_pair_bn == 224 || g_env_pair_bn == 256)
-        return g_env_pair_bn;
-    if (slots <= 0) return 256;
+// The last wave of 256-wide pair tiles, by the wave model: the modelled
+// time of a launch is its waves x (tile width + a per-tile fixed cost), a
+// tile's MMA time growing with width x K and the fixed cost (the accumulator
+// hand-off and first loads, about two microseconds, measured as a share of
+// the MMA loop on GB300) expressed in the same units, 1e5 / K columns.  Wave
+// quantisation ("CUTLASS", Part IV Stage 2 and Part XI: the last, partly
+// filled wave of tiles) has two remedies here, each taken only when it saves
+// at least 3 % over plain 256-wide tiles:
+//   * a half-width tail: when the last wave would use at most half of the
+//     workers, its tiles run as two 256 x 128 units each (same kernel, no
+//     partial sums), so that wave ends in half the time;
+//   * a narrower tile for the whole launch (224, 192 or 160 wide; B K-major
+//     only), at the price of more operand bytes per FLOP.
+struct WaveFit {
+    int bn = 256;
+    int half_tail = 0;   // tiles of the last wave run as two half-width units
+};
+
+WaveFit wave_fit(int num_m2, int N, int K, int slots, bool narrow_ok) {
+    WaveFit best;
+    if (g_env_pair_bn == 160 || g_env_pair_bn == 192 || g_env_pair_bn == 224 || g_env_pair_bn == 256) {
+        best.bn = narrow_ok || g_env_pair_bn == 256 ? g_env_pair_bn : 256;
+        return best;
+    }
+    if (slots <= 0) return best;
     const double fixed = 1e5 / std::max(K, 1);
-    auto cost = [&](int bn) {
-        const long long tiles = static_cast<long long>(num_m2) * ((N + bn - 1) / bn);
-        const long long waves = (tiles + slots - 1) / slots;
-        return static_cast<double>(waves) * (bn + fixed);
-    };
-    int best = 256;
-    double best_cost = cost(256) * 0.97;
-    for (int bn : {224, 192, 160}) {
-        const double c = cost(bn);
-        if (c < best_cost) { best = bn; best_cost = c; }
+    const long long tiles = static_cast<long long>(num_m2) * ((N + 255) / 256);
+    const long long full = tiles / slots, rem = tiles % slots;
+    const double plain = static_cast<double>((tiles + slots - 1) / slots) * (256 + fixed);
+    double best_cost = plain * 0.97;
+    if (g_env_half_tail != 0 && rem > 0 && 2 * rem <= slots) {
+        const double c = static_cast<double>(full) * (256 + fixed) + (128 + fixed);
+        if (c < best_cost || g_env_half_tail == 2) {
+            best.half_tail = static_cast<int>(rem);
+            best_cost = c;
+        }
+    }
+    if (narrow_ok) {
+        for (int bn : {224, 192, 160}) {
+            const long long t = static_cast<long long>(num_m2) * ((N + bn - 1) / bn);
+            const double c = static_cast<double>((t + slots - 1) / slots) * (bn + fixed);
+            if (c < best_cost) {
+                best.bn = bn;
+                best.half_tail = 0;
+                best_cost = c;
+            }
+        }
     }
     return best;
 }
 
+// A GEMM with few rows (M <= 64 of one 128-row tile) can run as the
+// transposed product D^T = B^T A^T: its 128-row tiles run over D's N columns
+// and its narrow N (32 or 64) covers D's rows, so the tensor cores compute no
+// padding rows and the split-K partials shrink to 128 x 32.  It needs a
+// K-contiguous A (A^T becomes the kernel's K-major B) and plain operands.
+// Measured on GB300 it does not pay: every such problem is bound by the
+// bytes of B, which the plain plan streams as fast (16 x 8192 x 8192, bias,
+// beta = 0.5: 38.9 us plain with split K 4, 43.0 - 53 us transposed in every
+// split and stage configuration), so it is taken only on request
+// (TCG_SWAP=1, or the test knob force_cta2 = 5).
+bool use_swap(int M, int N, tcg_dtype ab, tcg_layout opA) {
+    return (g_env_swap == 1 || g_force_cta2 == 5) && !is_mx(ab) && M > 0 && M <= 64 && N >= 256 &&
+           opA == TCG_ROW;
+}
+
 Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, int sk_override = -1,
-               bool b_kmajor = true) {
+               bool b_kmajor = true, bool swap = false) {
     Plan pl;
+    pl.swap = swap;
     const int K = k_units(ab, K_elems);
     const int bk = tcg::kRowBytes / elem_bytes(ab);
     const bool mx = is_mx(ab);   // block-scaled: 128 x 128 (one CTA) or 256 x BN (a pair) tiles
     pl.bn = (N <= 128) ? 128 : 256;
+    if (swap) pl.bn = N <= 32 ? 32 : 64;   // the kernel's N is D's row count
     if (mx) {
         // Pair tiles: 256 x 256 with one accumulator (the scales take the TMEM
         // columns of a second one), or 256 x 192 with two accumulators, so
@@ -385,7 +436,7 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // tiles would fill less than half of the SMs.  Measured on GB300: 512^3
     // 12.4 -> 10.3 us; for long K, split-K beats narrowing (16x8192x8192:
     // 49 vs 60 us).
-    if (!mx && g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && g_force_cta2 < 3 && pl.num_kb < 16) {
+    if (!mx && !swap && g_env_narrow && g_force_splits == 0 && g_force_cta2 != 1 && g_force_cta2 < 3 && pl.num_kb < 16) {
         while (pl.bn > 64 && num_m1 * ((N + pl.bn - 1) / pl.bn) * 2 < dev.num_sms) pl.bn /= 2;
     }
     const int num_n = (N + pl.bn - 1) / pl.bn;
@@ -405,11 +456,25 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // one full wave of pairs; they halve the operand bytes each SM streams.
     const int num_m2 = (M + 2 * tcg::kBM - 1) / (2 * tcg::kBM);
     bool cta2 = splits == 1 && pl.bn == 256 && M > tcg::kBM && num_m2 * num_n * 2 >= dev.num_sms;
+    // Long K, a tall A and at most 128 output columns (e.g. 8192 x 128 x 8192):
+    // 256 x 128 pair tiles with split K.  Each CTA streams its own 128 rows of
+    // A and only half of B's 128 columns, so a stage holds 16 KiB of A (from
+    // DRAM) and 8 KiB of B (from L2) per K atom instead of 16 + 16, and twice
+    // as many bytes of A are in flight per SM.
+    if (!mx && !swap && splits > 1 && pl.bn == 128 && N <= 128 && num_m2 >= 8 && g_env_skinny_pairs && g_env_katoms != 1 &&
+        g_force_splits == 0 && g_force_cta2 == 0) {
+        const int tiles2 = num_m2 * num_n;
+        splits = std::max(1, std::min(std::min((dev.num_sms / 2) / tiles2, pl.num_kb / 8), 16));
+        cta2 = splits > 1;
+    }
     if (g_force_cta2 == 1 || g_force_cta2 >= 3) cta2 = splits == 1 && pl.bn == 256;
     if (mx) cta2 = pl.bn > 128;
-    if (g_force_cta2 == 2) cta2 = false;
+    if (g_force_cta2 == 2 || g_force_cta2 == 5 || swap) cta2 = false;
     pl.cluster = cta2 ? 2 : 1;
     pl.katoms = cta2 ? (g_env_katoms == 1 ? 1 : 2) : (g_env_katoms == 2 && pl.bn >= 128 ? 2 : 1);
+    // the transposed product's small stages: two K atoms each (16 x 8192 x 8192:
+    // 43 vs 50 us with one); its pipeline then holds four
+    if (swap) pl.katoms = g_env_katoms == 1 ? 1 : 2;
     // block-scaled: two K atoms per stage on pair tiles, else one.  Measured on
     // 8192^3: MXFP8 pairs 1841 -> 2199 TFLOP/s (6 x 1 atom -> 3 x 2), NVFP4
     // pairs 2217 -> 2515 (5 x 1 -> 2 x 2)
@@ -432,7 +497,8 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     if (g_env_group_m > 0) pl.group_m = g_env_group_m;
     const bool small_ring = mx && cta2 && pl.bn == 256;   // 256-wide block-scaled pairs: half-size epilogue ring
     int stages = (dev.max_smem_optin - fixed_smem_bytes(small_ring)) / stage_bytes(pl.bn, cta2, pl.katoms, sfb);
-    stages = std::max(2, std::min(stages, 8));
+    // (the transposed plan's small stages stream B from DRAM: deeper)
+    stages = std::max(2, std::min(stages, swap ? 12 : 8));
     if (mx) {
         // TMEM: accumulators (2 x 128 or 2 x 192 columns, or one 256-column pair
         // accumulator) plus 4 columns per scale block per stage atom
@@ -450,10 +516,17 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     // Stream-K: balance the k-block iterations of the last tiles over all
     // workers instead of leaving the last wave partly empty.
     const int sk_mode = sk_override >= 0 ? sk_override : (g_env_sk >= 0 ? g_env_sk : 0);
-    // Otherwise a narrower pair tile whose waves come out fuller (B K-major).
-    if (cta2 && !mx && b_kmajor && sk_mode == 0 && g_force_splits == 0 && pl.katoms == 2 && g_force_cta2 < 3) {
+    // Otherwise a half-width tail or a narrower pair tile (wave_fit).
+    if (cta2 && !mx && pl.bn == 256 && pl.splits == 1 && sk_mode == 0 && g_force_splits == 0 && pl.katoms == 2 &&
+        g_force_cta2 < 3) {
         // K in bf16-equivalent elements (an 8-bit K element costs half the MMA time)
-        const int bn = wave_fit_bn(pl.num_m, N, K * elem_bytes(ab) / 2, slots);
+        const WaveFit wf = wave_fit(pl.num_m, N, K * elem_bytes(ab) / 2, slots, b_kmajor);
+        const int bn = wf.bn;
+        if (wf.half_tail > 0) {
+            pl.half_tail = wf.half_tail;
+            pl.units_a = pl.num_m * pl.num_n - wf.half_tail;
+            pl.units = pl.units_a + 2 * wf.half_tail;
+        }
         if (bn != pl.bn) {
             pl.bn = bn;
             pl.num_n = (N + bn - 1) / bn;
@@ -484,6 +557,13 @@ Plan make_plan(int M, int N, int K_elems, tcg_dtype ab, const DeviceInfo& dev, i
     pl.workers = pl.sk_tiles > 0 ? slots : std::max(1, std::min(pl.units, slots));
     pl.grid = (cta2 ? 2 : 1) * pl.workers;
     return pl;
+}
+
+// The plan tcg_gemm runs for this problem and these layouts: the transposed
+// product for GEMMs with few rows (use_swap), else the plain one.
+Plan plan_gemm(int M, int N, int K, tcg_dtype ab, const DeviceInfo& dev, tcg_layout opA, tcg_layout opB) {
+    if (use_swap(M, N, ab, opA)) return make_plan(N, M, K, ab, dev, -1, true, true);
+    return make_plan(M, N, K, ab, dev, -1, opB == TCG_COL);
 }
 
 size_t partial_slots(const Plan& pl) {
@@ -706,8 +786,13 @@ size_t tcg_workspace_size(int M, int N, int K, tcg_dtype ab_dtype) {
         dev.max_smem_optin = 232448;
     }
     if (M == 0 || N == 0) return kHeaderBytes;
-    return workspace_need(make_plan(M, N, K, ab_dtype, dev), M, N, K, ab_dtype, nullptr, 0, TCG_ROW, nullptr, 0,
-                          TCG_COL).base;
+    // the larger of the plain plan and, for a GEMM with few rows, the transposed one
+    size_t base = workspace_need(make_plan(M, N, K, ab_dtype, dev), M, N, K, ab_dtype, nullptr, 0, TCG_ROW, nullptr,
+                                 0, TCG_COL).base;
+    if (use_swap(M, N, ab_dtype, TCG_ROW))
+        base = std::max(base, workspace_need(make_plan(N, M, K, ab_dtype, dev, -1, true, true), M, N, K, ab_dtype,
+                                             nullptr, 0, TCG_ROW, nullptr, 0, TCG_COL).base);
+    return base;
 }
 
 size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const void* A, int lda, tcg_layout opA,
@@ -716,7 +801,7 @@ size_t tcg_workspace_size_for(int M, int N, int K, tcg_dtype ab_dtype, const voi
     if (base == 0 || M == 0 || N == 0 || K == 0) return base;
     if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return 0;
     const WorkspaceNeed w = workspace_need(Plan{}, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB);
-    return base + w.pack_a + w.pack_b;
+    return base + w.pack_a + w.pack_b;   // base covers the plain and the transposed plan
 }
 
 tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
@@ -726,15 +811,15 @@ tcg_status tcg_workspace_init(void* workspace, size_t bytes, void* stream) {
     return TCG_OK;
 }
 
-tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[10]) {
+tcg_status tcg_plan(int M, int N, int K, tcg_dtype ab_dtype, tcg_layout opA, tcg_layout opB, int out[11]) {
     if (M < 0 || N < 0 || K < 0 || !out) return TCG_ERR_INVALID_ARG;
     if ((opA != TCG_ROW && opA != TCG_COL) || (opB != TCG_ROW && opB != TCG_COL)) return TCG_ERR_INVALID_ARG;
     DeviceInfo dev;
     tcg_status st = device_info(dev);
     if (st != TCG_OK) return st;
-    Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
-    const int vals[10] = {tcg::kBM, pl.bn, pl.katoms * tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
-                          pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem};
+    Plan pl = plan_gemm(M, N, K, ab_dtype, dev, opA, opB);
+    const int vals[11] = {tcg::kBM, pl.bn, pl.katoms * tcg::kRowBytes / elem_bytes(ab_dtype), pl.stages, pl.splits,
+                          pl.grid, pl.cluster, pl.units, pl.group_m, pl.smem, pl.swap ? 1 : 0};
     memcpy(out, vals, sizeof vals);
     return TCG_OK;
 }
@@ -752,7 +837,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     if ((st = device_info(dev)) != TCG_OK) return st;
     if ((st = arch_check(dev)) != TCG_OK) return st;
     if ((st = check_scales(scales, ab_dtype, K)) != TCG_OK) return st;
-    Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
+    Plan pl = plan_gemm(M, N, K, ab_dtype, dev, opA, opB);
     const int eb = elem_bytes(ab_dtype);
     const WorkspaceNeed wn = workspace_need(pl, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB);
     const size_t base_need = wn.base, pack_a = wn.pack_a, pack_b = wn.pack_b;
@@ -811,7 +896,18 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     memset(&kp, 0, sizeof kp);
     const int bk = tcg::kRowBytes / elem_bytes(ab_dtype);
     const int atom = bk;  // MN elements per 128-byte swizzle row
-    if (K > 0) {
+    if (K > 0 && pl.swap) {
+        // The transposed product: the kernel's A is B^T (N x K: rows of K when
+        // B is column-major, else rows of N), its B is A^T (K x M, K-major:
+        // A is row-major), in boxes of BK x BN rows.
+        if (opB == TCG_COL)
+            st = encode_2d(&kp.tmA, ab_dtype, B, K, N, ldb, bk, tcg::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+        else
+            st = encode_2d(&kp.tmA, ab_dtype, B, N, K, ldb, atom, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TCG_OK) return st;
+        st = encode_2d(&kp.tmB, ab_dtype, A, K, M, lda, bk, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TCG_OK) return st;
+    } else if (K > 0) {
         // A: K-major -> rows of K, box BK x BM; MN-major -> rows of M, box atom x BK
         if (opA == TCG_ROW)
             st = encode_2d(&kp.tmA, ab_dtype, A, K, M, lda, bk, tcg::kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -825,25 +921,36 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
             st = encode_2d(&kp.tmB, ab_dtype, B, N, K, ldb, atom, pl.katoms * bk, CU_TENSOR_MAP_SWIZZLE_128B);
         if (st != TCG_OK) return st;
     }
-    kp.d_tma = tma_addressable(D, ldd, elem_bytes(d_dtype));
+    kp.d_tma = !pl.swap && tma_addressable(D, ldd, elem_bytes(d_dtype));
     if (kp.d_tma) {
         st = encode_2d(&kp.tmD, d_dtype, D, N, M, ldd, tcg::kEpiChunk, 32,
                        d_dtype == TCG_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != TCG_OK) return st;
     }
 
-    kp.M = M; kp.N = N; kp.K = K;
+    kp.M = pl.swap ? N : M;
+    kp.N = pl.swap ? M : N;
+    kp.K = K;
     kp.num_m_blk = pl.num_m; kp.num_n_blk = pl.num_n; kp.num_kb = pl.num_kb;
     kp.splits = pl.splits; kp.num_units = pl.units; kp.group_m = pl.group_m;
     kp.units_a = pl.units_a;
     kp.sk_tiles = pl.sk_tiles;
     kp.sk_iters = static_cast<long long>(pl.sk_tiles) * pl.num_kb;
     kp.sk_slot_base = pl.splits > 1 ? pl.units_a : 0;
-    kp.a_mn_major = (opA == TCG_COL); kp.b_mn_major = (opB == TCG_ROW);
+    kp.half_tail = pl.half_tail;
+    if (pl.half_tail > 0 && K > 0 && opB == TCG_COL) {
+        // the tail's half-width units load half of each CTA's B rows
+        st = encode_2d(&kp.tmB2, ab_dtype, B, K, N, ldb, bk, (pl.cluster == 2 ? pl.bn / 2 : pl.bn) / 2,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != TCG_OK) return st;
+    }
+    kp.a_mn_major = pl.swap ? (opB == TCG_ROW) : (opA == TCG_COL);
+    kp.b_mn_major = pl.swap ? 0 : (opB == TCG_ROW);
     kp.alpha = alpha * scales.scale_a * scales.scale_b;
     kp.ab_fmt = mma_format(ab_dtype);
-    kp.row_scale = scales.row_scale;
-    kp.col_scale = scales.col_scale;
+    // (the transposed product's rows are D's columns)
+    kp.row_scale = pl.swap ? scales.col_scale : scales.row_scale;
+    kp.col_scale = pl.swap ? scales.row_scale : scales.col_scale;
     kp.sfa = static_cast<const uint8_t*>(scales.block_sfa);
     kp.sfb = static_cast<const uint8_t*>(scales.block_sfb);
     kp.num_sfcb = ((K_elems + sf_group(ab_dtype) - 1) / sf_group(ab_dtype) + 3) / 4;
@@ -864,7 +971,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.C = has_c ? C : nullptr;
     kp.ldc = ldc;
     kp.c_f32 = (c_dtype == TCG_F32);
-    kp.c_vec = has_c && tma_addressable(C, ldc, elem_bytes(c_dtype));
+    kp.c_vec = !pl.swap && has_c && tma_addressable(C, ldc, elem_bytes(c_dtype));
     kp.c_tma = kp.c_vec;
     if (kp.c_tma) {
         st = encode_2d(&kp.tmC, c_dtype, C, N, M, ldc, tcg::kEpiChunk, 32,
@@ -876,7 +983,7 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
         const int box = 32 * 32 * std::max(elem_bytes(d_dtype), kp.c_tma ? elem_bytes(c_dtype) : 0);
         kp.epi_nbuf = tcg::epi_warp_bytes(is_mx(ab_dtype) && pl.cluster == 2 && pl.bn == 256) / box;
     }
-    kp.cs_vec = scales.col_scale && aligned16(scales.col_scale);
+    kp.cs_vec = !pl.swap && scales.col_scale && aligned16(scales.col_scale);
     kp.bias = epi.bias;
     kp.bias_f32 = (epi.bias_dtype == TCG_F32);
     kp.act = static_cast<int>(epi.act);
@@ -884,16 +991,24 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.D = D;
     kp.ldd = ldd;
     kp.d_inner_aligned = (static_cast<long long>(N) * elem_bytes(d_dtype)) % 16 == 0;
+    kp.d_stage_all = g_env_tma_store;
     kp.stages = pl.stages;
     char* ws = static_cast<char*>(workspace);
     kp.status = reinterpret_cast<int*>(ws);
     kp.tile_counters = any_split(pl) ? reinterpret_cast<int*>(ws + kHeaderBytes) : nullptr;
+    kp.num_slots = static_cast<int>(partial_slots(pl));
+    kp.num_counters = any_split(pl) ? pl.num_m * pl.num_n * pl.cluster : 0;
     kp.partials = any_split(pl) ? reinterpret_cast<float*>(ws + kHeaderBytes + counter_bytes(pl)) : nullptr;
     kp.timeout_ns = g_timeout_ns > 0 ? g_timeout_ns : kDefaultTimeoutNs;
     kp.fault_inject = g_fault_inject;
     kp.stats = g_env_stats ? reinterpret_cast<unsigned long long*>(ws + 64) : nullptr;
 
     const bool fp8 = is_fp8(ab_dtype);
+    if (pl.swap) {
+        const char* what = "launch";
+        const cudaError_t e = tcg::launch_swapped(kp, launch_shape(pl), pl.bn, pl.katoms, fp8, stream, &what);
+        return e == cudaSuccess ? TCG_OK : fail_launch(what, e);
+    }
     if (is_mx(ab_dtype)) {
         const int blk = ab_dtype == TCG_NVFP4 ? 2 : (ab_dtype == TCG_MXFP4 ? 3 : 1);
         const char* what = "launch";
@@ -945,16 +1060,18 @@ int tcg_debug_schedule(int M, int N, int K, tcg_dtype ab_dtype, int num_sms, int
     kp.sk_tiles = pl.sk_tiles;
     kp.sk_iters = static_cast<long long>(pl.sk_tiles) * pl.num_kb;
     kp.sk_slot_base = pl.splits > 1 ? pl.units_a : 0;
+    kp.half_tail = pl.half_tail;
     int n = 0;
     for (int wid = 0; wid < pl.workers; ++wid) {
         tcg::WorkIter it = tcg::work_begin(kp, wid, pl.workers);
         tcg::Unit w;
         while (tcg::work_next(kp, it, w)) {
             if (n < max_rows && rows) {
-                int* r = rows + 9 * n;
+                int* r = rows + 10 * n;
                 r[0] = wid; r[1] = w.tile; r[2] = w.m_blk; r[3] = w.n_blk; r[4] = w.kb0; r[5] = w.kb1;
                 r[6] = w.split; r[7] = w.nsplit;
                 r[8] = w.nsplit > 1 ? tcg::partial_slot(kp, w, w.split, pl.workers) : -1;
+                r[9] = w.nh;
             }
             ++n;
         }
@@ -972,7 +1089,10 @@ tcg_status tcg_device_status(void* workspace, void* stream_) {
     if (e != cudaSuccess) return fail_launch("cudaMemcpy(status)", e);
     if (words[0] != 0) {
         char buf[160];
-        snprintf(buf, sizeof buf, "device wait ran out (role/stage code %d, block %d)", words[1], words[2]);
+        if (words[0] == TCG_ERR_CHECK)
+            snprintf(buf, sizeof buf, "device-side check failed (check code %d, block %d)", words[1], words[2]);
+        else
+            snprintf(buf, sizeof buf, "device wait ran out (role/stage code %d, block %d)", words[1], words[2]);
         g_last_error = buf;
         e = cudaMemset(workspace, 0, sizeof words);
         if (e != cudaSuccess) return fail_launch("cudaMemset(status)", e);
@@ -1039,7 +1159,7 @@ extern "C" tcg_status tcg_gemm_noalloc(int M, int N, int K, float alpha, const v
         }
         scratch = g_noalloc_ptr[device];
     }
-    const Plan pl = make_plan(M, N, K, ab_dtype, dev, -1, opB == TCG_COL);
+    const Plan pl = plan_gemm(M, N, K, ab_dtype, dev, opA, opB);
     const size_t need = workspace_need(pl, M, N, K, ab_dtype, A, lda, opA, B, ldb, opB).total();
     if (need > kNoAllocScratchBytes) {
         char buf[200];
