@@ -14,9 +14,10 @@
 //     issues BK/MMA_K tcgen05.mma into a TMEM accumulator, and commits the
 //     stage back to the producer.  Warp 1 also owns TMEM allocation.
 //   * Warps 2-5: epilogue.  TMEM -> registers (tcgen05.ld), alpha / beta*C /
-//     bias / activation in fp32, cast, then 16-byte stores of each thread's
-//     row straight to D; a ragged last chunk goes through a swizzled staging
-//     tile and a TMA store (out-of-range columns clipped by the hardware).
+//     bias / activation in fp32, cast, then into a swizzled staging tile in
+//     shared memory and out through a TMA store (out-of-range columns
+//     clipped by the hardware); the block-scaled kernels store whole chunks
+//     with 16-byte stores of each thread's row straight from registers.
 //   * Two TMEM accumulators: the epilogue of tile i overlaps the mainloop of
 //     tile i+1 (the idea behind the ping-pong schedule, "CUTLASS", Part V
 //     deep dive on collective builder and kernel schedules).
@@ -102,6 +103,7 @@ struct KernelParams {
     long long sk_iters;
     int sk_slot_base;     // first partial slot of the Stream-K phase (2 per worker)
     int half_tail;        // last tiles run as two half-width units each (decode_unit)
+    int k_serp;           // odd waves walk K downwards (work_next)
     int a_mn_major, b_mn_major;
     float alpha, beta;
     const void* C;
@@ -249,6 +251,7 @@ struct Unit {
     int sk, tl, w_first;
     int g;   // problem of a grouped GEMM (0 otherwise)
     int nh;  // 0: the whole tile; 1 / 2: its first / second half of BN / 2 columns (the tail)
+    int rev; // walk the K range downwards (every other wave, when KernelParams::k_serp)
 };
 
 // A unit's first column and width.
@@ -275,6 +278,7 @@ __host__ __device__ __forceinline__ void tile_coords(const KernelParams& p, int 
 __host__ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
     Unit w;
     w.nh = 0;
+    w.rev = 0;
     if (p.half_tail > 0 && u >= p.units_a) {
         const int hu = u - p.units_a;
         w.tile = p.units_a + hu / 2;
@@ -346,6 +350,10 @@ __host__ __device__ __forceinline__ WorkIter work_begin(const KernelParams& p, i
 __host__ __device__ __forceinline__ bool work_next(const KernelParams& p, WorkIter& s, Unit& w) {
     if (s.u < p.num_units) {
         w = decode_unit(p, s.u);
+        // K-serpentine: the workers' odd waves of units walk K downwards, so a
+        // wave starts on the K slabs the previous wave loaded last (most
+        // likely still in L2) when it revisits the same rows of A
+        w.rev = p.k_serp && ((s.u / s.workers) & 1);
         s.u += s.workers;
         return true;
     }
@@ -355,6 +363,7 @@ __host__ __device__ __forceinline__ bool work_next(const KernelParams& p, WorkIt
     w.tl = tl;
     w.g = 0;
     w.nh = 0;
+    w.rev = 0;
     w.tile = p.units_a / p.splits + tl;
     tile_coords(p, w.tile, w.m_blk, w.n_blk);
     w.kb0 = static_cast<int>(s.it - static_cast<long long>(tl) * p.num_kb);
@@ -857,7 +866,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
                 const bool half = kHalfOk && w.nh != 0;
                 const int b_row = unit_n0(w, BN) + static_cast<int>(rank) * (half ? kBRows / 2 : kBRows);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int ki = kb0; ki < kb1; ++ki) {
+                    const int kb = w.rev ? kb0 + kb1 - 1 - ki : ki;
                     const long long tw = p.stats ? clock64() : 0;
                     if (!dcheck(stage >= 0 && stage < S && S <= 16, p, ctl, kChkStage)) { ok = false; break; }
                     if (!warp_wait(&ctl->empty[stage], phase ^ 1u, p, ctl, 1, limit)) { ok = false; break; }
@@ -1020,7 +1030,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                 const uint32_t idesc = (kHalfOk && w.nh != 0)
                                            ? ((idesc_full & ~(0x3Fu << 17)) | (static_cast<uint32_t>((BN / 2) >> 3) << 17))
                                            : idesc_full;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                // (the stages arrive in the producer's K order; only the first
+                // of the unit's MMAs starts a new accumulation)
+                for (int ki = kb0; ki < kb1; ++ki) {
                     const long long tf = p.stats ? clock64() : 0;
                     if (!dcheck(stage >= 0 && stage < S && S <= 16, p, ctl, kChkStage)) { ok = false; break; }
                     if (!warp_wait(&ctl->full[stage], phase, p, ctl, 3, limit)) { ok = false; break; }
@@ -1066,7 +1078,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                     for (int k = 0; k < kKAtoms * kKSteps; ++k) {
                         const uint64_t ad = a_desc + static_cast<uint64_t>(a_off(k));
                         const uint64_t bd = b_desc + static_cast<uint64_t>(b_off(k));
-                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                        const uint32_t accum = (ki > kb0 || k > 0) ? 1u : 0u;
                         if constexpr (kMx) {
                             // MMA kk of atom `at`: its scale blocks and the byte the first
                             // of its scales sits at inside each 32-bit TMEM word
@@ -1502,13 +1514,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
     #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = apply_act(1, v[i]);
                         }
-                        // A whole chunk of a D whose rows start on 16-byte boundaries
+                        // Unless the host asks for every chunk to be staged for a TMA
+                        // store (the default of the kernels with two accumulators), a
+                        // whole chunk of a D whose rows start on 16-byte boundaries
                         // goes from registers straight to global memory: each thread
-                        // writes its row's 64 (bf16) or 128 (f32) contiguous bytes.
-                        // Against staging it for a TMA store this measured NVFP4 and
-                        // MXFP8 8192^3 +2.5 % (their epilogue is on the critical
-                        // path) and the bf16 workloads unchanged.  A ragged last
-                        // chunk keeps the staged store, which clips at N.
+                        // writes its row's 64 (bf16) or 128 (f32) contiguous bytes,
+                        // which the block-scaled kernels, whose epilogue is on the
+                        // critical path, measured 3.5 % faster at 8192^3.  A ragged
+                        // last chunk is always staged (the TMA store clips at N).
                         if (q.d_tma && col0 + kEpiChunk <= q.N && !p.d_stage_all) {
                             if (row_ok) {
                                 char* rowp = static_cast<char*>(q.D) +
