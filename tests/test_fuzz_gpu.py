@@ -5,7 +5,8 @@ Shapes are drawn so that the plans cover every way the planner splits work
 on the GPU it runs on: whole 256 x 256 pair tiles, a last wave run as
 half-width units, the wave-fitting 224 / 192 / 160-wide pair tiles, one-CTA
 tiles, split K (with the round-robin and the own-row-group sums), 256 x 128
-pair tiles with split K, and the K-serpentine order of odd waves.  Integer
+pair tiles with split K (among them wide GEMMs with at most 32 rows), and
+the K-serpentine order of odd waves.  Integer
 operands in [-4, 4], integer C and bias, fp32 D: every result is exact, so
 any element that differs from the oracle is a bug.  Layouts, operand types
 (bf16, f16, e4m3, e5m2), beta and the activation are drawn with the shape.
@@ -35,7 +36,8 @@ def _built():
 
 def draw_cases(n, seed=2026):
     rng = np.random.default_rng(seed)
-    kinds = ["pairs_many_waves", "pairs_one_wave_tail", "wide_tail", "one_cta_small", "split_long_k", "tall_narrow"]
+    kinds = ["pairs_many_waves", "pairs_one_wave_tail", "wide_tail", "one_cta_small", "split_long_k", "tall_narrow",
+             "few_rows_long_k"]
     cases = []
     for i in range(n):
         kind = kinds[i % len(kinds)]
@@ -49,20 +51,24 @@ def draw_cases(n, seed=2026):
             M, N, K = int(rng.integers(1, 700)), int(rng.integers(1, 900)), int(rng.integers(1, 700))
         elif kind == "split_long_k":
             M, N, K = int(rng.integers(1, 400)), int(rng.integers(8, 600)), int(rng.integers(1500, 5000))
-        else:
+        elif kind == "tall_narrow":
             M, N, K = int(rng.integers(2048, 2600)), int(rng.integers(8, 129)), int(rng.integers(1600, 4000))
+        else:
+            M, N, K = int(rng.integers(1, 33)), int(rng.integers(4900, 9000)), int(rng.integers(1100, 3000))
         ab = ["bf16", "bf16", "f16", "e4m3", "e5m2"][int(rng.integers(0, 5))]
         if ab in ("e4m3", "e5m2"):
             opA, opB = "row", "col"
         else:
             opA, opB = inputs.LAYOUT_COMBOS[int(rng.integers(0, 4))]
+        if kind == "few_rows_long_k":
+            opA = "row"
         beta = [0.0, 0.5, 1.0][int(rng.integers(0, 3))]
         act = ["none", "relu"][int(rng.integers(0, 2))]
         cases.append(dict(kind=kind, M=M, N=N, K=K, ab=ab, opA=opA, opB=opB, beta=beta, act=act, seed=5000 + i))
     return cases
 
 
-CASES = draw_cases(30)
+CASES = draw_cases(35)
 
 
 @pytest.mark.parametrize("c", CASES, ids=lambda c: f"{c['kind']}-{c['M']}x{c['N']}x{c['K']}-{c['ab']}-{c['opA']}{c['opB']}")
@@ -99,7 +105,9 @@ def test_the_random_problems_cover_every_plan_feature():
             seen.add("one_cta")
         if pl["cluster"] == 1 and pl["splits"] > 1:
             seen.add("split_k")
+        if c["M"] <= 32 and pl["cluster"] == 1 and pl["splits"] > 1 and c["N"] >= 4096:
+            seen.add("few_rows_split_k")
         if pl["units"] > pl["grid"] // pl["cluster"]:
             seen.add("several_waves")
     assert {"half_tail", "whole_pairs", "narrow_pairs", "skinny_pairs", "one_cta", "split_k",
-            "several_waves"} <= seen, seen
+            "several_waves", "few_rows_split_k"} <= seen, seen
