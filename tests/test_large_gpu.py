@@ -1,10 +1,11 @@
-"""A GEMM whose output has more than 2^31 elements (49152 x 49152 fp32 D,
-9.7 GB): every offset into D past 2^31 elements must be formed in 64 bits,
-in the TMA-store epilogue (ldd = N) and in the element-wise one (ldd = N + 1,
-whose rows are not 16-byte multiples).  Integer operands with fp32 D, so the
-sampled outputs (full rows including the last ones, full columns and the four
-corner tiles) must equal the oracle exactly; the guard rows around D and the
-padding column must still hold the sentinel.  36,864 pair tiles per launch."""
+"""Extreme sizes.  A GEMM whose output has more than 2^31 elements (49152 x
+49152 fp32 D, 9.7 GB): every offset into D past 2^31 elements must be formed
+in 64 bits, in the TMA-store epilogue (ldd = N) and in the element-wise one
+(ldd = N + 1, whose rows are not 16-byte multiples); 36,864 pair tiles per
+launch.  A K of 2^20 (split K) and a D of 2^20 - 3 rows.  Integer operands
+with fp32 D, so the sampled outputs (full rows including the last ones, full
+columns and the four corner tiles) must equal the oracle exactly; the guard
+rows around D (and the padding column) must still hold the sentinel."""
 import pytest
 import torch
 
@@ -45,6 +46,47 @@ def test_output_beyond_2_31_elements(pad):
         assert bool((dc.D_full[0] == s).all()) and bool((dc.D_full[-1] == s).all()), "guard rows written"
         if pad:
             assert bool((dc.D_view[:, N] == s).all()), "padding column written"
+    finally:
+        del dc
+        torch.cuda.empty_cache()
+
+
+def test_long_k_split_exact():
+    """K = 2^20 (split K, a long run of k-blocks per piece): integer operands
+    keep every fp32 partial sum exact, so the sampled outputs equal the
+    oracle's."""
+    M, N, K = 200, 300, 1 << 20
+    case = inputs.make_case("long_k", M, N, K, seed=710, dist="int4", d_dtype="f32")
+    assert tcg.plan(M, N, K)["splits"] > 1
+    dc = harness.DeviceCase(case, guard_rows=1)
+    try:
+        dc.run()
+        torch.cuda.synchronize()
+        assert tcg.device_status(dc.workspace) == 0, tcg.last_error()
+        check_rows_cols_corners(dc.D_view[:, :N], oracle_for(case), M, N, 0.0, case.name, nrows=24, ncols=24,
+                                corner=32, seed=7, exact=True)
+        s = dc.sentinel_stored
+        assert bool((dc.D_full[0] == s).all()) and bool((dc.D_full[-1] == s).all()), "guard rows written"
+    finally:
+        del dc
+        torch.cuda.empty_cache()
+
+
+def test_a_million_rows_exact():
+    """M = 2^20 - 3 rows of a narrow D (4096 pair-tile rows, ragged last
+    tile): exact on sampled rows including the last ones, on full columns and
+    corners; guard rows untouched."""
+    M, N, K = (1 << 20) - 3, 72, 40
+    case = inputs.make_case("many_rows", M, N, K, seed=711, dist="int4", d_dtype="f32")
+    dc = harness.DeviceCase(case, guard_rows=1)
+    try:
+        dc.run()
+        torch.cuda.synchronize()
+        assert tcg.device_status(dc.workspace) == 0, tcg.last_error()
+        check_rows_cols_corners(dc.D_view[:, :N], oracle_for(case), M, N, 0.0, case.name, nrows=64, ncols=24,
+                                corner=64, seed=8, exact=True)
+        s = dc.sentinel_stored
+        assert bool((dc.D_full[0] == s).all()) and bool((dc.D_full[-1] == s).all()), "guard rows written"
     finally:
         del dc
         torch.cuda.empty_cache()
