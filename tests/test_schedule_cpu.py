@@ -146,3 +146,16 @@ def test_block_scaled_pair_tile_grid(ab, width):
     assert max(r[2] for r in rows) + 1 == M // 256
     assert max(r[3] for r in rows) + 1 == -(-N // width)
     assert tcg.debug_schedule(M, N, K, ab, num_sms=152, sk_mode=0)[0][7] == 1   # K is not split
+
+
+@pytest.mark.parametrize("shape", [(49152, 49152, 64), (200, 300, 1 << 20), ((1 << 20) - 3, 72, 40)],
+                         ids=["36864_pair_tiles", "k_2pow20", "m_2pow20"])
+@pytest.mark.parametrize("mode", [0, 3])
+def test_schedule_at_extreme_sizes(shape, mode):
+    """The extreme sizes the GPU tests run (36,864 pair tiles; K = 2^20 with
+    split K; about a million rows): every iteration once, slots distinct."""
+    M, N, K = shape
+    rows, per_worker, total = check(M, N, K, "bf16", 152, mode)
+    num_kb = max(r[5] for r in rows)
+    units = len({(r[1], r[9]) for r in rows})   # whole tiles, or the two halves of a tail tile
+    assert total == units * num_kb
