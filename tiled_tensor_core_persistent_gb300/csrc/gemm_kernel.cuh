@@ -116,6 +116,7 @@ struct KernelParams {
     void* D;              // row-major output, for the ragged column tail
     long long ldd;
     int d_inner_aligned;  // N * sizeof(D element) is a multiple of 16 bytes
+    int d_v32;            // D's base and row pitch are multiples of 32 bytes (32-byte register stores)
     int d_tma;            // D has a TMA store map (16-byte aligned base and row pitch)
     int d_stage_all;      // every chunk of D staged in shared memory and stored by TMA (else registers -> global)
     int c_vec;            // C rows may be read with 16-byte vector loads
@@ -1522,18 +1523,37 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_persistent_kernel(const _
                             for (int i = 0; i < 32; ++i) v[i] = apply_act(1, v[i]);
                         }
                         // Unless the host asks for every chunk to be staged for a TMA
-                        // store (the default of the kernels with two accumulators), a
-                        // whole chunk of a D whose rows start on 16-byte boundaries
-                        // goes from registers straight to global memory: each thread
-                        // writes its row's 64 (bf16) or 128 (f32) contiguous bytes,
-                        // which the block-scaled kernels, whose epilogue is on the
-                        // critical path, measured 3.5 % faster at 8192^3.  A ragged
-                        // last chunk is always staged (the TMA store clips at N).
+                        // store, a whole chunk of a D whose rows start on 16-byte
+                        // boundaries goes from registers straight to global memory:
+                        // each thread writes its row's 64 (bf16) or 128 (f32)
+                        // contiguous bytes, in 32-byte stores when D allows them.
+                        // A ragged last chunk is always staged (the TMA store clips
+                        // at N).
                         if (q.d_tma && col0 + kEpiChunk <= q.N && !p.d_stage_all) {
                             if (row_ok) {
                                 char* rowp = static_cast<char*>(q.D) +
                                              (static_cast<long long>(grow) * q.ldd + col0) * (p.d_f32 ? 4 : 2);
-                                if (p.d_f32) {
+                                if (q.d_v32) {
+                                    // 32-byte stores: each writes whole 32-byte sectors
+                                    // (col0 is a multiple of 32 elements, so rowp is
+                                    // 32-byte aligned when D's base and pitch are)
+                                    uint32_t w[8];
+                                    if (p.d_f32) {
+    #pragma unroll
+                                        for (int c = 0; c < 4; ++c) {
+    #pragma unroll
+                                            for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * c + i]);
+                                            ptx::st_global_v8(rowp + 32 * c, w);
+                                        }
+                                    } else {
+    #pragma unroll
+                                        for (int c = 0; c < 2; ++c) {
+    #pragma unroll
+                                            for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * c + 2 * i], v[16 * c + 2 * i + 1]);
+                                            ptx::st_global_v8(rowp + 32 * c, w);
+                                        }
+                                    }
+                                } else if (p.d_f32) {
     #pragma unroll
                                     for (int c = 0; c < 8; ++c)
                                         *reinterpret_cast<float4*>(rowp + 16 * c) =

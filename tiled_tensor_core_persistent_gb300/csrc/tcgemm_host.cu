@@ -67,10 +67,13 @@ const int g_env_skinny_pairs = getenv("TCG_SKINNY_PAIRS") ? env_int("TCG_SKINNY_
 const int g_env_swap = env_int("TCG_SWAP");
 // TCG_TMA_STORE=1 / 0: every chunk of D staged in shared memory for a TMA store,
 // or whole chunks stored from registers (a ragged last chunk is always staged).
-// Unset: the TMA store, except for the block-scaled kernels.
+// Unset: from registers.
 const int g_env_tma_store = getenv("TCG_TMA_STORE") ? env_int("TCG_TMA_STORE") : -1;
 // TCG_KSERP=0: every unit walks K upwards (default: odd waves downwards, see work_next).
 const int g_env_kserp = getenv("TCG_KSERP") ? env_int("TCG_KSERP") : 1;
+// TCG_ST32=0: the register-store epilogue writes 16-byte pieces even where
+// D allows 32-byte stores (default 1).
+const int g_env_st32 = getenv("TCG_ST32") ? env_int("TCG_ST32") : 1;
 // TCG_HALF_TAIL=0 never runs the last wave as half-width tiles, =2 always when it fits.
 const int g_env_half_tail = getenv("TCG_HALF_TAIL") ? env_int("TCG_HALF_TAIL") : 1;
 // TCG_PAIR_BN = width of 16/8-bit pair tiles (160, 192, 224 or 256) when B is
@@ -1001,12 +1004,18 @@ tcg_status tcg_gemm(int M, int N, int K, float alpha, const void* A, int lda, tc
     kp.D = D;
     kp.ldd = ldd;
     kp.d_inner_aligned = (static_cast<long long>(N) * elem_bytes(d_dtype)) % 16 == 0;
-    // D's store path, measured on GB300 (8192^3, median of 30 launches): the
-    // bf16 kernel is the same either way (629.4 us staged + TMA store, 631.5
-    // from registers), the block-scaled ones, whose epilogue is not hidden
-    // behind a second accumulator, gain from registers (NVFP4 414.5 -> 400.2,
-    // MXFP8 479.5 -> 463.1 us)
-    kp.d_stage_all = g_env_tma_store >= 0 ? g_env_tma_store : (is_mx(ab_dtype) ? 0 : 1);
+    kp.d_v32 = g_env_st32 && reinterpret_cast<uintptr_t>(D) % 32 == 0 &&
+               (static_cast<long long>(ldd) * elem_bytes(d_dtype)) % 32 == 0;
+    // D's store path: whole chunks from registers (32-byte stores where D's
+    // base and pitch allow) by default.  Measured on GB300 against staging
+    // every chunk for a TMA store (one GPU, median of 30 launches, twice
+    // each): 4095 x 3001 x 1537 51.7-51.8 vs 54.0 us, 16 x 8192 x 8192
+    // 40.1-40.6 vs 41.2, 8192 x 128 x 8192 43.5 vs 43.8, 4096^3 96.5-96.6 vs
+    // 96.7-97.0, 8192^3 GELU 594.4-594.7 vs 595.5, e4m3 and the grouped MoE
+    // within 0.2 %; the block-scaled kernels, whose epilogue is not hidden
+    // behind a second accumulator, gained most from registers when they
+    // moved to them (NVFP4 414.5 -> 400.2, MXFP8 479.5 -> 463.1 us).
+    kp.d_stage_all = g_env_tma_store >= 0 ? g_env_tma_store : 0;
     kp.stages = pl.stages;
     char* ws = static_cast<char*>(workspace);
     kp.status = reinterpret_cast<int*>(ws);
@@ -1339,6 +1348,8 @@ extern "C" tcg_status tcg_gemm_grouped(int num_problems, const tcg_problem* prob
         kp.D = q.D;
         kp.ldd = q.ldd;
         kp.d_inner_aligned = (static_cast<long long>(q.N) * elem_bytes(d_dtype)) % 16 == 0;
+        kp.d_v32 = g_env_st32 && reinterpret_cast<uintptr_t>(q.D) % 32 == 0 &&
+                   (static_cast<long long>(q.ldd) * elem_bytes(d_dtype)) % 32 == 0;
         tile0[g + 1] = tile0[g] + tiles[g];
     }
     // One table in the workspace after the status header: the problems'
