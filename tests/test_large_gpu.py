@@ -1,7 +1,8 @@
 """Extreme sizes.  A GEMM whose output has more than 2^31 elements (49152 x
 49152 fp32 D, 9.7 GB): every offset into D past 2^31 elements must be formed
-in 64 bits, in the TMA-store epilogue (ldd = N) and in the element-wise one
-(ldd = N + 1, whose rows are not 16-byte multiples); 36,864 pair tiles per
+in 64 bits, in the register-store epilogue (ldd = N: 32-byte stores) and in
+the element-wise one (ldd = N + 1, whose rows are not 16-byte multiples);
+36,864 pair tiles per
 launch.  A K of 2^20 (split K) and a D of 2^20 - 3 rows.  Integer operands
 with fp32 D, so the sampled outputs (full rows including the last ones, full
 columns and the four corner tiles) must equal the oracle exactly; the guard
@@ -29,7 +30,7 @@ def _built():
     tcg.debug_set()
 
 
-@pytest.mark.parametrize("pad", [0, 1], ids=["tma_store", "elementwise"])
+@pytest.mark.parametrize("pad", [0, 1], ids=["register_stores", "elementwise"])
 def test_output_beyond_2_31_elements(pad):
     M = N = 49152
     K = 64
