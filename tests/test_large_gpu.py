@@ -1,12 +1,12 @@
 """Extreme sizes.  A GEMM whose output has more than 2^31 elements (49152 x
-49152 fp32 D, 9.7 GB): every offset into D past 2^31 elements must be formed
-in 64 bits, in the register-store epilogue (ldd = N: 32-byte stores) and in
-the element-wise one (ldd = N + 1, whose rows are not 16-byte multiples);
-36,864 pair tiles per
-launch.  A K of 2^20 (split K) and a D of 2^20 - 3 rows.  Integer operands
-with fp32 D, so the sampled outputs (full rows including the last ones, full
-columns and the four corner tiles) must equal the oracle exactly; the guard
-rows around D (and the padding column) must still hold the sentinel."""
+49152 fp32 D, 9.7 GB, 36,864 pair tiles per launch): every offset into D
+past 2^31 elements must be formed in 64 bits, in the register-store epilogue
+(ldd = N: 32-byte stores) and in the element-wise one (ldd = N + 1, whose
+rows are not 16-byte multiples).  A K of 2^20 (split K) and a D of 2^20 - 3
+rows.  Integer operands with fp32 D, so the sampled outputs (full rows
+including the last ones, full columns and the four corner tiles) must equal
+the oracle exactly; the guard rows around D (and the padding column) must
+still hold the sentinel."""
 import pytest
 import torch
 
