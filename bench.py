@@ -198,16 +198,55 @@ def load_peaks():
         return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of the GEMM's sources (every file under csrc/ except the test-only
-    debug_* kernels, which take no part in a GEMM)."""
+def _code_only(src):
+    """C/C++ source without its comments and with its blank space collapsed
+    (string and character literals kept as they are)."""
+    out, i, n, quote = [], 0, len(src), None
+    while i < n:
+        c = src[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(src[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_hash(csrc):
+    """Hash of the code in directory `csrc`: every file except the test-only
+    debug_* kernels (which take no part in a GEMM), without comments and blank
+    space."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "tiled_tensor_core_persistent_gb300", "csrc")
     for name in sorted(n for n in os.listdir(csrc) if not n.startswith("debug_")):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    """Hash of the GEMM's code (source_hash of the package's csrc/): the
+    recorded DRAM traffic stays valid across comment edits and lapses with any
+    change to the code."""
+    return source_hash(os.path.join(ROOT, "tiled_tensor_core_persistent_gb300", "csrc"))
 
 
 def recorded_traffic(key):

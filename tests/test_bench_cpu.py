@@ -1,6 +1,5 @@
 """bench.py's host logic without a GPU: workload descriptions, algorithmic
 bytes, the kernel source hash that keys the recorded DRAM traffic."""
-import hashlib
 import json
 import os
 import sys
@@ -39,14 +38,26 @@ def test_every_workload_has_a_factory_and_flush_flag():
     assert bench.DEFAULT_WORKLOAD in bench.WORKLOADS
 
 
-def test_kernel_source_hash_covers_the_gemm_sources_only():
+def test_kernel_source_hash_follows_the_code_not_the_comments(tmp_path):
+    """A copy of csrc/ hashes like the package's; editing a comment, blank
+    space or a test-only debug_* file keeps the hash, editing code (even inside
+    a string literal that looks like a comment) changes it."""
+    import shutil
     csrc = os.path.join(ROOT, "tiled_tensor_core_persistent_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in sorted(n for n in os.listdir(csrc) if not n.startswith("debug_")):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
-    assert bench.kernel_source_hash() == h.hexdigest()[:16]
+    d = tmp_path / "csrc"
+    shutil.copytree(csrc, d)
+    base = bench.source_hash(str(d))
+    assert base == bench.kernel_source_hash()
+    k = d / "gemm_kernel.cuh"
+    text = k.read_text()
+    k.write_text(text.replace("#pragma once", "#pragma once\n// a new comment\n/* and a block */\n\n", 1))
+    assert bench.source_hash(str(d)) == base
+    (d / "debug_extra.cu").write_text("int x;\n")
+    assert bench.source_hash(str(d)) == base
+    k.write_text(text.replace("#pragma once", "#pragma once\nstatic const char* kTag = \"// not a comment\";", 1))
+    assert bench.source_hash(str(d)) != base
+    k.write_text(text.replace("constexpr int kEpiChunk = 32;", "constexpr int kEpiChunk = 64;", 1))
+    assert bench.source_hash(str(d)) != base
 
 
 def test_recorded_traffic_only_for_the_current_source():

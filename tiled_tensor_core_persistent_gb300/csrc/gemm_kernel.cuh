@@ -14,10 +14,11 @@
 //     issues BK/MMA_K tcgen05.mma into a TMEM accumulator, and commits the
 //     stage back to the producer.  Warp 1 also owns TMEM allocation.
 //   * Warps 2-5: epilogue.  TMEM -> registers (tcgen05.ld), alpha / beta*C /
-//     bias / activation in fp32, cast, then into a swizzled staging tile in
-//     shared memory and out through a TMA store (out-of-range columns
-//     clipped by the hardware); the block-scaled kernels store whole chunks
-//     with 16-byte stores of each thread's row straight from registers.
+//     bias / activation in fp32, cast, then each thread stores its row of
+//     the chunk straight from registers (32-byte stores where D allows); a
+//     ragged last chunk goes into a swizzled staging tile in shared memory
+//     and out through a TMA store (out-of-range columns clipped by the
+//     hardware).
 //   * Two TMEM accumulators: the epilogue of tile i overlaps the mainloop of
 //     tile i+1 (the idea behind the ping-pong schedule, "CUTLASS", Part V
 //     deep dive on collective builder and kernel schedules).
